@@ -1,0 +1,89 @@
+"""CPU oracle for ResidualQuant KV compression and decode attention.
+
+TEST INFRASTRUCTURE ONLY.  This package is plain float64 NumPy written from
+the ResidualQuant pages; it exists to check the CUDA library.  Only the test
+suite, __graft_entry__.smoke() and bench.py's CPU-baseline leg import it.
+The product path (decode_attention_rq_gb300 and its CUDA library) never
+imports, links or runs anything here, and nothing here imports the product.
+
+What each module follows:
+  formats.py  E4M3 and BF16 round-to-nearest-even, from the format definitions.
+  method.py   group quantizer, least-squares coefficient, rotated residual,
+              shared/chained reconstruction, single-query softmax attention.
+  layout.py   the cache's byte layout (this library's format).
+  this file   cache-level steps: compress and pack a loop group, rebuild a
+              loop's K/V from the cache bytes, and decode attention over the
+              cache plus the current token held in BF16.
+"""
+from __future__ import annotations
+
+import numpy as np
+
+from . import formats, method, layout
+from .formats import (e4m3_encode, e4m3_decode, e4m3_round, bf16_encode, bf16_decode, bf16_round)
+from .method import quantize, dequantize, ls_coefficient, compress_group, attention
+from .layout import Geometry, TILE, pack_group, read_plane_tokens, bits_per_element
+
+__all__ = ["formats", "method", "layout", "Geometry", "TILE", "quantize", "dequantize",
+           "ls_coefficient", "compress_group", "attention", "pack_group", "read_plane_tokens",
+           "bits_per_element", "append", "reconstruct", "decode_attention",
+           "e4m3_encode", "e4m3_decode", "e4m3_round", "bf16_encode", "bf16_decode", "bf16_round"]
+
+
+def append(buf: np.ndarray, geom: Geometry, R: np.ndarray, layer: int, group: int,
+           kv: np.ndarray, start, chained: bool = False) -> dict:
+    """Compress the P loops of n new tokens and write them at positions start[b].. .
+
+    kv: float64 [P, 2, B, H, n, d] (exact BF16 values), anchor = last loop.
+    Returns the compress_group result (codes, metadata, reconstructions)."""
+    comp = compress_group(kv, R, geom.group_size, chained=chained)
+    pack_group(buf, geom, layer, group, comp, np.asarray(start, dtype=np.int64))
+    return comp
+
+
+def reconstruct(buf: np.ndarray, geom: Geometry, R: np.ndarray, layer: int, group: int,
+                b: int, h: int, loop: int, n: int, chained: bool = False):
+    """Decoder's view of loop `loop` (0-based; P-1 is the anchor) for positions 0..n-1.
+
+    Shared anchor ([EXPL], shared-master paragraph): K_l = c_l * a_hat + R^T r_hat_l,
+    two planes read.  Chained: K_l = c_l * K_{l+1} + R^T r_hat_l down from the
+    anchor, reading every residual plane between l and the anchor.
+    Returns (K_hat [n, d], V_hat [n, d]) float64."""
+    P, g = geom.loops_per_group, geom.group_size
+    out = []
+    for kv in range(2):
+        codes, s_b, o_b = read_plane_tokens(buf, geom, layer, group, b, h, kv, "anchor", 0, n)
+        x = dequantize(codes, s_b, o_b, g)
+        if loop < P - 1:
+            # shared: one residual plane against the anchor; chained: every
+            # plane from the anchor's neighbour down to this loop
+            js = range(P - 2, loop - 1, -1) if chained else [loop]
+            for j in js:
+                rc, rs, ro, cbits = read_plane_tokens(buf, geom, layer, group, b, h, kv, "res", j, n)
+                r_hat = dequantize(rc, rs, ro, g)
+                x = bf16_decode(cbits)[:, None] * x + r_hat @ R
+        out.append(x)
+    return out[0], out[1]
+
+
+def decode_attention(buf: np.ndarray, geom: Geometry, R: np.ndarray, layer: int, group: int,
+                     loop: int, q: np.ndarray, k_cur: np.ndarray, v_cur: np.ndarray,
+                     seq_lens, scale: float, chained: bool = False,
+                     rows=None) -> np.ndarray:
+    """Attention of one (layer, group, loop) decode call.
+
+    Keys/values: the seq_lens[b] cached tokens rebuilt for this loop, plus the
+    current token's K/V straight from the BF16 temporary buffer ([EXPL]: the
+    current token stays in BF16 until its last loop has run).
+    q, k_cur, v_cur: float64 [B, H, d].  rows: optional iterable of (b, h) to
+    evaluate (others left NaN).  Returns float64 [B, H, d]."""
+    B, H, d = q.shape
+    out = np.full((B, H, d), np.nan)
+    todo = rows if rows is not None else [(b, h) for b in range(B) for h in range(H)]
+    for b, h in todo:
+        n = int(seq_lens[b])
+        K, V = reconstruct(buf, geom, R, layer, group, b, h, loop, n, chained)
+        K = np.concatenate([K, k_cur[b, h][None, :]], axis=0)
+        V = np.concatenate([V, v_cur[b, h][None, :]], axis=0)
+        out[b, h] = attention(q[b, h], K, V, scale)
+    return out

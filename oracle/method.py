@@ -1,0 +1,145 @@
+"""ResidualQuant arithmetic, written out plainly in float64 (oracle).
+
+TEST INFRASTRUCTURE ONLY.  Only tests/, __graft_entry__.smoke() and the
+CPU-baseline leg of bench.py may import this package.  The product path
+(the CUDA library and its Python binding) never does; the two share no code.
+
+Sources, by page and section:
+  [EXPL] "ResidualQuant stores looped-Transformer KV caches as 2-bit
+         residuals" (learnaivisually.com explainer): the paragraph that
+         defines the stored overlay (residual = KV(loop) - c x anchor, c a
+         least-squares coefficient per key or value vector, a rotation
+         applied before quantization, rebuild c x anchor + residual on
+         chip); the paragraph on shared versus chained anchors and the
+         BF16 temporary buffer; the worked storage example (INT4 anchor,
+         INT2 residuals, FP8 scale and offset per channel group, one BF16
+         coefficient per residual vector).
+  [SUMM] ai4snews summary of the arXiv paper: overview (last-loop anchor,
+         least-squares scaling, rotation of the residual rather than of the
+         KV, per-loop INT4/INT2 mixed precision), the main-results paragraph
+         (group size 32/16, effective bits count codes, FP8 scale and
+         offset and the BF16 coefficient).
+
+Readings of what the pages leave open (each one listed in the design doc):
+  * group quantizer: asymmetric min/max.  offset o = E4M3(min), scale
+    s = E4M3((max - min) / (2^b - 1)); both rounded BEFORE coding; codes are
+    the nearest grid point o + k*s of the exact value (ties to even k),
+    clamped to [0, 2^b - 1]; s == 0 gives all-zero codes.
+  * c is computed against the dequantized anchor (the decoder only has it),
+    is 0 when the reference vector is all zero, and is rounded to BF16
+    before the residual is formed, so encoder and decoder agree.
+  * R is applied as u = R (x - c_b * ref); reconstruction uses R^T.
+  * chained variant: loop l is coded against the reconstruction of loop
+    l+1, the last loop being the anchor.
+"""
+from __future__ import annotations
+
+import numpy as np
+
+from .formats import e4m3_round, e4m3_encode, e4m3_decode, bf16_round, bf16_encode, bf16_decode
+
+__all__ = ["quantize", "dequantize", "ls_coefficient", "compress_group", "attention",
+           "ANCHOR_BITS", "RESIDUAL_BITS"]
+
+ANCHOR_BITS = 4     # [EXPL] worked example; [SUMM] overview (INT4 anchor)
+RESIDUAL_BITS = 2   # [EXPL] worked example; [SUMM] overview (INT2 residuals)
+
+
+def _nearest_grid_codes(v: np.ndarray, o: np.ndarray, s: np.ndarray, qmax: int) -> np.ndarray:
+    """k minimising |v - (o + k s)| over integers, ties to even k, then clamped to [0, qmax].
+
+    For v given exactly (bf16 or fp32 values) and E4M3 o, s, the differences
+    below are exact in float64, so this is the nearest point of the exact
+    quotient, not of a rounded one.
+    """
+    t = v - o
+    safe_s = np.where(s > 0, s, 1.0)
+    k = np.rint(t / safe_s)
+    r = t - k * safe_s
+    k = k + (2.0 * r > safe_s) - (2.0 * r < -safe_s)      # one step toward the nearest
+    r = t - k * safe_s
+    tie = (2.0 * np.abs(r) == safe_s)
+    k = np.where(tie & (np.mod(k, 2.0) != 0.0), k + np.sign(r), k)
+    k = np.clip(k, 0, qmax)
+    return np.where(s > 0, k, 0.0).astype(np.uint8)
+
+
+def quantize(v: np.ndarray, bits: int, g: int):
+    """Group quantizer.  v: float64 [..., d]; groups are consecutive runs of g channels.
+
+    Returns (codes uint8 [..., d], scale E4M3 bytes [..., d/g], offset E4M3 bytes [..., d/g]).
+    """
+    v = np.asarray(v, dtype=np.float64)
+    d = v.shape[-1]
+    if d % g:
+        raise ValueError("head_dim must be a multiple of the group size")
+    qmax = (1 << bits) - 1
+    vg = v.reshape(v.shape[:-1] + (d // g, g))
+    lo = vg.min(axis=-1)
+    hi = vg.max(axis=-1)
+    o = e4m3_round(lo)
+    s = e4m3_round((hi - lo) / qmax)
+    codes = _nearest_grid_codes(vg, o[..., None], s[..., None], qmax)
+    return codes.reshape(v.shape), e4m3_encode(s), e4m3_encode(o)
+
+
+def dequantize(codes: np.ndarray, scale_b: np.ndarray, offset_b: np.ndarray, g: int) -> np.ndarray:
+    """x_hat = s * code + o per group, float64 (exact)."""
+    codes = np.asarray(codes)
+    d = codes.shape[-1]
+    s = e4m3_decode(scale_b)[..., None]
+    o = e4m3_decode(offset_b)[..., None]
+    cg = codes.reshape(codes.shape[:-1] + (d // g, g)).astype(np.float64)
+    return (s * cg + o).reshape(codes.shape)
+
+
+def ls_coefficient(x: np.ndarray, y: np.ndarray) -> np.ndarray:
+    """c = <x, y> / <y, y> over the last axis, 0 where <y, y> == 0 ([EXPL]: a
+    least-squares coefficient per key or value vector)."""
+    num = np.sum(x * y, axis=-1)
+    den = np.sum(y * y, axis=-1)
+    return np.where(den > 0, num / np.where(den > 0, den, 1.0), 0.0)
+
+
+def compress_group(x: np.ndarray, R: np.ndarray, g: int, chained: bool = False):
+    """Compress the P loops of one loop group.
+
+    x: float64 [P, ..., d], loop index first, the last loop is the anchor
+       ([EXPL]: the final loop's KV is the INT4 master; [SUMM]: last-loop anchor).
+    R: float64 [d, d], the fixed rotation (as the device receives it).
+    Returns a dict with
+      anchor: (codes, scale_b, offset_b)
+      res[j] for j in 0..P-2: (codes, scale_b, offset_b, c_bf16_bits)
+      u[j]: float64 rotated residual before quantization
+      recon: float64 [P, ..., d], the decoder's view of every loop
+    """
+    x = np.asarray(x, dtype=np.float64)
+    P = x.shape[0]
+    a_codes, a_s, a_o = quantize(x[P - 1], ANCHOR_BITS, g)
+    a_hat = dequantize(a_codes, a_s, a_o, g)
+    recon = np.empty_like(x)
+    recon[P - 1] = a_hat
+    res, us = [None] * (P - 1), [None] * (P - 1)
+    for j in range(P - 2, -1, -1):
+        ref = recon[j + 1] if chained else a_hat
+        c = ls_coefficient(x[j], ref)
+        c_bits = bf16_encode(c)
+        cb = bf16_decode(c_bits)[..., None]
+        e = x[j] - cb * ref                      # residual against the scaled reference
+        u = e @ R.T                              # u = R e for each vector
+        r_codes, r_s, r_o = quantize(u, RESIDUAL_BITS, g)
+        r_hat = dequantize(r_codes, r_s, r_o, g)
+        recon[j] = cb * ref + r_hat @ R          # R^T r_hat for each vector
+        res[j] = (r_codes, r_s, r_o, c_bits)
+        us[j] = u
+    return {"anchor": (a_codes, a_s, a_o), "res": res, "u": us, "recon": recon}
+
+
+def attention(q: np.ndarray, K: np.ndarray, V: np.ndarray, scale: float) -> np.ndarray:
+    """Single-query softmax attention, float64: softmax(scale * K q) V.
+
+    q [d], K [n, d], V [n, d] -> [d].  The maximum is subtracted before exp."""
+    s = scale * (K @ q)
+    m = np.max(s)
+    p = np.exp(s - m)
+    return (p @ V) / np.sum(p)

@@ -1,0 +1,135 @@
+"""Pins for the oracle's cache layout and storage accounting (no GPU)."""
+import json
+import os
+
+import numpy as np
+import pytest
+
+import synth
+import oracle
+from oracle import layout as Lo
+from oracle import method as M
+
+GOLDEN = os.path.join(os.path.dirname(__file__), "golden", "storage_accounting.json")
+
+
+def test_storage_accounting_reproduces_the_pages():
+    gold = {e["quantity"].split(" (")[0]: e for e in json.load(open(GOLDEN))["entries"]}
+    acc = Lo.bits_per_element(128, 32, 4)
+    got = {
+        "uncompressed bits per KV element position over the 4 loops": acc["bf16"],
+        "code bits per element position over the 4 loops": 4 + 2 * 3,
+        "compression ratio before metadata": acc["codes_only_ratio"],
+        "compression ratio with FP8 scale+offset per group and one BF16 coefficient per residual vector": acc["ratio"],
+        "theoretical KV storage reduction vs BF16, percent": 100 * acc["reduction"],
+    }
+    for k, e in gold.items():
+        assert abs(got[k] - e["value"]) <= e["tolerance"], (k, got[k], e["value"])
+    # closed form: 4.5 + 3 x 2.625 = 12.375 bits
+    assert acc["anchor"] == 4.5 and acc["residual"] == 2.625 and acc["total"] == 12.375
+
+
+def test_storage_other_shapes():
+    assert Lo.bits_per_element(128, 16, 4)["total"] == 14.375
+    assert Lo.bits_per_element(96, 32, 4)["total"] == 4.5 + 3 * (2 + 0.5 + 16 / 96)
+
+
+@pytest.mark.parametrize("d,g,per_token", [(128, 32, 396), (128, 16, 2 * 80 + 6 * 50), (96, 32, 2 * 54 + 6 * 32)])
+def test_geometry_bytes_match_the_accounting(d, g, per_token):
+    geom = Lo.Geometry(1, 4, 1, 1, d, g, 1, 640)
+    assert geom.region == 10 * per_token * 64          # 10 tiles of 64 tokens
+    assert geom.region * 8 / (640 * 2 * d) == Lo.bits_per_element(d, g, 4)["total"]
+    for sz in (geom.a_tile, geom.r_tile, geom.a_codes, geom.r_codes, geom.meta):
+        assert sz % 16 == 0
+
+
+def _small_cache(chained, seed=0, n=150, B=2, H=3, d=128, g=32):
+    w = synth.Workload("t", 2, 4, 2, H, d, g, B, n, synth.OURO_ALPHAS, True)
+    geom = Lo.Geometry(2, 4, 2, H, d, g, B, 200)
+    buf = np.zeros(geom.total_bytes, dtype=np.uint8)
+    R = synth.rotation(d).astype(np.float32).astype(np.float64)
+    _, kv = synth.looped_kv(seed, w, batch=B, ntok=n)
+    comps = []
+    # write in two appends (prefill then a few more tokens) to layer 1, group 1
+    comps.append(oracle.append(buf, geom, R, 1, 1, kv[..., :100, :], [0] * B, chained))
+    comps.append(oracle.append(buf, geom, R, 1, 1, kv[..., 100:, :], [100] * B, chained))
+    return geom, buf, R, kv, comps
+
+
+@pytest.mark.parametrize("chained", [False, True])
+def test_pack_read_roundtrip_and_reconstruction(chained):
+    geom, buf, R, kv, comps = _small_cache(chained)
+    recon = np.concatenate([c["recon"] for c in comps], axis=-2)       # [P,2,B,H,n,d]
+    for b in range(2):
+        for h in range(3):
+            for loop in range(4):
+                K, V = oracle.reconstruct(buf, geom, R, 1, 1, b, h, loop, 150, chained)
+                assert np.array_equal(K, recon[loop, 0, b, h])
+                assert np.array_equal(V, recon[loop, 1, b, h])
+    # other (layer, group) regions untouched
+    off = geom.region_offset(1, 1, 0, 0)
+    assert not buf[:off].any()
+
+
+def test_code_positions_in_bytes():
+    """Spot-check the documented bit positions against hand-built bytes."""
+    geom = Lo.Geometry(1, 4, 1, 1, 128, 32, 1, 64)
+    buf = np.zeros(geom.total_bytes, dtype=np.uint8)
+    codes4 = np.zeros((1, 128), dtype=np.uint8)
+    codes4[0, 0], codes4[0, 1], codes4[0, 5] = 3, 12, 7
+    addr, sh = Lo._code_addresses(geom, 0, geom.a_tile, np.array([5]), 4, channel_major=False)
+    Lo._write_codes(buf, addr, sh, codes4, 4)
+    row = 5 * 64
+    assert buf[row] == 3 | (12 << 4) and buf[row + 2] == 7 << 4
+    buf[:] = 0
+    addr, sh = Lo._code_addresses(geom, 0, geom.a_tile, np.array([5]), 4, channel_major=True)
+    Lo._write_codes(buf, addr, sh, codes4, 4)
+    # channel-major: channel 1's row is bytes 32..63, token 5 -> byte 2, high nibble
+    assert buf[32 + 2] == 12 << 4 and buf[0 + 2] == 3 << 4 and buf[5 * 32 + 2] == 7 << 4
+    buf[:] = 0
+    codes2 = np.zeros((1, 128), dtype=np.uint8)
+    codes2[0, 6] = 2
+    base = geom.res_plane(0, 1)
+    addr, sh = Lo._code_addresses(geom, base, geom.r_tile, np.array([7]), 2, channel_major=True)
+    Lo._write_codes(buf, addr, sh, codes2, 2)
+    assert buf[base + 6 * 16 + 1] == 2 << 6      # token 7: byte 1, bits 6-7
+
+
+@pytest.mark.parametrize("chained", [False, True])
+def test_read_counts_shared_vs_chained(chained, monkeypatch):
+    """Shared anchor: a loop reads the anchor plane and its own residual plane
+    (2 reads); chained: the anchor plus every residual plane down to the loop,
+    4 reads for the farthest loop of 4 ([EXPL] shared-master paragraph)."""
+    geom, buf, R, kv, comps = _small_cache(chained)
+    reads = []
+    orig = oracle.read_plane_tokens
+
+    def spy(*a, **k):
+        reads.append(a[7])
+        return orig(*a, **k)
+    monkeypatch.setattr(oracle, "read_plane_tokens", spy)
+    for loop, want_chained in [(0, 4), (1, 3), (2, 2), (3, 1)]:
+        reads.clear()
+        oracle.reconstruct(buf, geom, R, 1, 1, 0, 0, loop, 150, chained)
+        per_kv = len(reads) // 2
+        assert per_kv == (want_chained if chained else (2 if loop < 3 else 1))
+
+
+def test_decode_attention_over_cache():
+    geom, buf, R, kv, comps = _small_cache(False, n=150)
+    recon = np.concatenate([c["recon"] for c in comps], axis=-2)
+    rng = np.random.default_rng(3)
+    q = rng.standard_normal((2, 3, 128))
+    kc = rng.standard_normal((2, 3, 128))
+    vc = rng.standard_normal((2, 3, 128))
+    seq = np.array([150, 37])
+    out = oracle.decode_attention(buf, geom, R, 1, 1, 2, q, kc, vc, seq, 0.0883883)
+    for b in range(2):
+        for h in range(3):
+            n = seq[b]
+            K = np.concatenate([recon[2, 0, b, h, :n], kc[b, h][None]])
+            V = np.concatenate([recon[2, 1, b, h, :n], vc[b, h][None]])
+            assert np.allclose(out[b, h], M.attention(q[b, h], K, V, 0.0883883), rtol=0, atol=1e-13)
+    # an empty cache attends to the current token only
+    out0 = oracle.decode_attention(buf, geom, R, 1, 1, 0, q, kc, vc, np.array([0, 0]), 0.1)
+    assert np.array_equal(out0, vc)
