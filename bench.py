@@ -1,0 +1,469 @@
+"""Decode-step benchmark of the ResidualQuant path on GB300.
+
+One step = what a looped model does to produce one token per sequence: for
+every loop and every layer one rq_decode_attention call over the compressed
+cache (plus the current token from the BF16 temporary buffer), and after each
+layer's last loop one rq_append(n=1) that compresses that token into the cache.
+Ouro-1.4B shape at 8k context: 24 layers x 4 loops = 96 attention calls and 24
+appends per step, batch 4, 16 heads of width 128, INT4 anchor / INT2 residuals,
+g = 32.  The cache is kept at a fixed length (each step overwrites the same
+next slot), so every step does the same work.
+
+Prints one JSON line.  `--impl reference` times the CPU oracle instead.
+"""
+from __future__ import annotations
+
+import argparse
+import json
+import math
+import os
+import statistics
+import subprocess
+import sys
+import threading
+import time
+
+import numpy as np
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+sys.path.insert(0, ROOT)
+
+import synth  # noqa: E402
+
+METRIC = "decode-attn tokens/s and effective HBM GB/s (% GB300 peak) at 8k/16k ctx"
+
+
+def _peaks():
+    p = os.path.join(ROOT, "MEASURED_PEAKS.json")
+    if os.path.exists(p):
+        d = json.load(open(p))
+        return float(d["hbm_gbs"]), "measured"
+    return 6800.0, "fallback"
+
+
+def _algo_bytes_per_token_call(w: synth.Workload, has_res: bool, chained_planes: int = 1) -> int:
+    """Compressed bytes one attention call reads per cached token (K and V)."""
+    d, ng = w.head_dim, w.head_dim // w.group_size
+    anchor = d // 2 + 2 * ng
+    res = d // 4 + 2 * ng + 2
+    return 2 * (anchor + (res * chained_planes if has_res else 0))
+
+
+def algorithmic_bytes_per_step(w: synth.Workload, batch: int, ctx: int) -> dict:
+    """Bytes the step must move at minimum: every attention call reads its
+    planes for all cached tokens, plus the current token, q and out; each
+    append writes one token's records."""
+    P, L, H, d = w.loops_per_group, w.num_layers, w.num_heads, w.head_dim
+    rows = batch * H
+    per_call_res = _algo_bytes_per_token_call(w, True) * ctx * rows
+    per_call_anchor = _algo_bytes_per_token_call(w, False) * ctx * rows
+    small = rows * (3 * d * 2 + d * 4)                      # q, k_cur, v_cur (bf16) + out (fp32)
+    calls = (P - 1) * (per_call_res + small) + (per_call_anchor + small)
+    ng = d // w.group_size
+    append = rows * 2 * ((d // 2 + 2 * ng) + (P - 1) * (d // 4 + 2 * ng + 2)) + rows * P * 2 * d * 2
+    total = L * w.num_groups * (calls + append)
+    return {"step": total, "call_res": per_call_res + small, "call_anchor": per_call_anchor + small}
+
+
+class ClockSampler:
+    """nvidia-smi sampling during the timed region (SM clock, throttle reasons)."""
+
+    def __init__(self, gpu_index: int):
+        self.gpu = gpu_index
+        self.proc = None
+        self.lines = []
+
+    def __enter__(self):
+        q = ("index,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
+             "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
+             "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
+        try:
+            self.proc = subprocess.Popen(["nvidia-smi", "-i", str(self.gpu), f"--query-gpu={q}",
+                                          "--format=csv,noheader,nounits", "-lms", "200"],
+                                         stdout=subprocess.PIPE, stderr=subprocess.DEVNULL, text=True)
+            self.t = threading.Thread(target=self._read, daemon=True)
+            self.t.start()
+        except Exception:
+            self.proc = None
+        return self
+
+    def _read(self):
+        for line in self.proc.stdout:
+            self.lines.append(line.strip())
+
+    def __exit__(self, *a):
+        if self.proc:
+            self.proc.terminate()
+            try:
+                self.proc.wait(timeout=5)
+            except Exception:
+                self.proc.kill()
+
+    def summary(self):
+        sm, mx, reasons = [], None, set()
+        names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
+        for ln in self.lines:
+            f = [x.strip() for x in ln.split(",")]
+            if len(f) < 9:
+                continue
+            try:
+                sm.append(float(f[1]))
+                mx = float(f[2])
+            except ValueError:
+                continue
+            for nm, v in zip(names, f[5:9]):
+                if v.lower().startswith("active"):
+                    reasons.add(nm)
+        return {"sm_mhz": statistics.median(sm) if sm else None, "sm_max_mhz": mx,
+                "reasons": sorted(reasons), "samples": len(sm)}
+
+
+class OracleSample:
+    """The oracle as it stands, on the host cores: rebuild + attend for one
+    (row, head) slice of an attention call at full context.  A step of the
+    workload is batch * heads * calls such slices; timings are extrapolated."""
+
+    def __init__(self, w: synth.Workload, ctx: int):
+        import oracle
+        self.oracle = oracle
+        self.w, self.ctx = w, ctx
+        d, P = w.head_dim, w.loops_per_group
+        self.R = synth.rotation(d).astype(np.float32).astype(np.float64)
+        self.geom = oracle.Geometry(1, P, 1, 1, d, w.group_size, 1, ctx)
+        one = synth.Workload("row", 1, P, 1, 1, d, w.group_size, 1, ctx, w.alphas, w.anchor_is_base)
+        self.buf = np.zeros(self.geom.total_bytes, dtype=np.uint8)
+        _, kv = synth.looped_kv(123, one, batch=1, ntok=ctx)
+        oracle.append(self.buf, self.geom, self.R, 0, 0, kv, [0])
+        _, self.q = synth.queries(5, 1, 1, d)
+        _, self.cur = synth.looped_kv(6, one, batch=1, ntok=1)
+        self.scale = 1.0 / math.sqrt(d)
+        self.n = 0
+
+    def run(self, budget_s: float):
+        """Row-calls for about budget_s seconds; returns (row_calls, seconds)."""
+        P = self.w.loops_per_group
+        n, t0 = 0, time.perf_counter()
+        while True:
+            loop = (self.n + n) % P
+            self.oracle.decode_attention(self.buf, self.geom, self.R, 0, 0, loop, self.q,
+                                         self.cur[loop, 0, :, :, 0], self.cur[loop, 1, :, :, 0],
+                                         [self.ctx], self.scale)
+            n += 1
+            el = time.perf_counter() - t0
+            if el >= budget_s:
+                break
+        self.n += n
+        return n, el
+
+    def row_calls_per_step(self, batch):
+        return batch * self.w.num_heads * self.w.calls_per_step
+
+
+def cpu_baseline(w: synth.Workload, batch: int, ctx: int, budget_s: float = 15.0) -> dict:
+    smp = OracleSample(w, ctx)
+    n, el = smp.run(budget_s)
+    step_s = el / n * smp.row_calls_per_step(batch)
+    return {"value": batch / step_s, "unit": "tokens/s", "cores": len(os.sched_getaffinity(0)), "kind": "oracle",
+            "sample": f"{n} (row, head) attention calls at {ctx} tokens (float64 NumPy rebuild from the "
+                      f"cache bytes + softmax), {el:.1f} s, extrapolated to "
+                      f"{smp.row_calls_per_step(batch)} row-calls per step"}
+
+
+def run_reference(args, w):
+    rank = int(os.environ.get("RANK", "0"))
+    if rank != 0:
+        return
+    smp = OracleSample(w, w.context)
+    per_step = smp.row_calls_per_step(w.batch)
+    times, total_n, total_s = [], 0, 0.0
+    for i in range(args.warmup + args.steps):
+        n, el = smp.run(args.ref_budget)
+        if i >= args.warmup:
+            times.append(el / n * per_step)
+            total_n += n
+            total_s += el
+    ms = 1000 * statistics.mean(times)
+    val = w.batch / (ms / 1000)
+    sample = (f"each step: about {args.ref_budget:.0f} s of (row, head) attention calls at {w.context} tokens "
+              f"(float64 NumPy rebuild from the cache bytes + softmax), extrapolated to {per_step} row-calls; "
+              f"{total_n} row-calls in {total_s:.1f} s over the timed steps")
+    line = {"metric": METRIC, "value": val, "unit": "tokens/s", "impl": "reference", "n_gpus": args.gpus,
+            "steps": args.steps, "warmup": args.warmup, "ms_per_step": ms, "higher_is_better": True,
+            "scaling": "weak", "vs_baseline": None, "dtype": "f64", "data": "synthetic",
+            "config": _config(w),
+            "cpu_baseline": {"value": val, "unit": "tokens/s", "cores": len(os.sched_getaffinity(0)),
+                             "kind": "oracle", "sample": sample},
+            "e2e": {"value": val, "unit": "tokens/s", "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0}}
+    print(json.dumps(line))
+
+
+def _config(w):
+    return {"workload": f"{w.name}: {w.num_layers} layers x {w.loops_per_group} loops x {w.num_groups} groups, "
+                        f"{w.num_heads} KV heads x {w.head_dim}, batch {w.batch}, {w.context}-token context, "
+                        f"INT4 anchor + INT2 residuals, group {w.group_size}, shared anchor",
+            "global_batch": w.batch, "seq_len": w.context, "parallelism": "replicas",
+            "l2": "inputs larger than L2 (every step streams the whole compressed cache)"}
+
+
+def main():
+    ap = argparse.ArgumentParser()
+    ap.add_argument("--gpus", type=int, default=1)
+    ap.add_argument("--steps", type=int, default=20)
+    ap.add_argument("--warmup", type=int, default=5)
+    ap.add_argument("--impl", default="rq", choices=["rq", "reference"])
+    ap.add_argument("--workload", default="ouro8k", choices=sorted(synth.WORKLOADS))
+    ap.add_argument("--batch", type=int, default=None)
+    ap.add_argument("--group-size", type=int, default=None)
+    ap.add_argument("--no-bf16", action="store_true", help="skip the BF16 comparator")
+    ap.add_argument("--no-cpu", action="store_true", help="skip the CPU-oracle baseline")
+    ap.add_argument("--no-e2e", action="store_true")
+    ap.add_argument("--ref-budget", type=float, default=2.0)
+    ap.add_argument("--quiet", action="store_true")
+    args = ap.parse_args()
+    w = synth.WORKLOADS[args.workload]
+    if args.batch or args.group_size:
+        import dataclasses
+        w = dataclasses.replace(w, batch=args.batch or w.batch, group_size=args.group_size or w.group_size)
+    if args.impl == "reference":
+        run_reference(args, w)
+        return
+    run_rq(args, w)
+
+
+def run_rq(args, w):
+    import torch
+    world = int(os.environ.get("WORLD_SIZE", "1"))
+    rank = int(os.environ.get("RANK", "0"))
+    local = int(os.environ.get("LOCAL_RANK", "0"))
+    torch.cuda.set_device(local)
+    dev = torch.device("cuda", local)
+    if world > 1:
+        import torch.distributed as dist
+        dist.init_process_group("nccl")
+    import decode_attention_rq_gb300 as rq
+
+    L, P, G, H, d, g, B, N = (w.num_layers, w.loops_per_group, w.num_groups, w.num_heads, w.head_dim,
+                              w.group_size, w.batch, w.context)
+    gen = torch.Generator(device=dev)
+    gen.manual_seed(1234 + rank)
+    R32 = torch.from_numpy(synth.rotation(d).astype(np.float32)).to(dev)
+    cfg = rq.rq_config(L, P, G, H, d, g, B, N + 64, rq.RQ_MODE_SHARED)
+    nbytes = rq.rq_cache_bytes(cfg)
+    cache_buf = torch.empty(nbytes, dtype=torch.uint8, device=dev)
+    handle = rq.rq_cache_create(cfg, cache_buf, nbytes, R32)
+    ws_bytes = rq.rq_decode_workspace_bytes(cfg, B)
+    ws = torch.zeros(ws_bytes, dtype=torch.uint8, device=dev)
+    status = ws[:16].view(torch.int32)
+    seq0 = torch.zeros(B, dtype=torch.int32, device=dev)
+    # prefill: compress N tokens per (layer, group)
+    t0 = time.perf_counter()
+    for layer in range(L):
+        for grp in range(G):
+            kv = synth.looped_kv_torch(gen, w, B, N, dev)
+            rq.rq_append(handle, layer, grp, B, kv, seq0, N, status)
+            del kv
+    torch.cuda.synchronize()
+    prefill_s = time.perf_counter() - t0
+    seq = torch.full((B,), N, dtype=torch.int32, device=dev)
+    scale = 1.0 / math.sqrt(d)
+    ncalls = L * G * P
+    # per-step inputs: queries per call, the BF16 temporary buffer per (layer, group)
+    q_all = torch.randn((ncalls, B, H, d), generator=gen, device=dev).to(torch.bfloat16)
+    temp_all = torch.stack([synth.looped_kv_torch(gen, w, B, 1, dev) for _ in range(L * G)])  # [LG,P,2,B,H,1,d]
+    out_all = torch.empty((ncalls, B, H, d), dtype=torch.float32, device=dev)
+
+    order = [(lp, layer, grp) for grp in range(G) for lp in range(P) for layer in range(L)]
+
+    def step(stream):
+        i = 0
+        for (lp, layer, grp) in order:
+            t = temp_all[layer * G + grp]
+            rq.rq_decode_attention(handle, layer, grp, lp, B, q_all[i], t[lp, 0, :, :, 0], t[lp, 1, :, :, 0], seq,
+                                   scale, out_all[i], ws, ws_bytes, stream)
+            i += 1
+            if lp == P - 1:
+                rq.rq_append(handle, layer, grp, B, t, seq, 1, status, stream)
+
+    launches_per_step = ncalls + L * G
+    s = torch.cuda.Stream(device=dev)
+    torch.cuda.synchronize()
+    with torch.cuda.stream(s):
+        step(s.cuda_stream)   # eager once (also sets kernel attributes before capture)
+    torch.cuda.synchronize()
+    graph = torch.cuda.CUDAGraph()
+    with torch.cuda.graph(graph, stream=s):
+        step(s.cuda_stream)
+    torch.cuda.synchronize()
+
+    # warm-up
+    for _ in range(args.warmup):
+        graph.replay()
+    torch.cuda.synchronize()
+    # timed region
+    e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    with ClockSampler(local) as clk:
+        if world > 1:
+            torch.distributed.barrier()
+        torch.cuda.synchronize()
+        e0.record(s)
+        for _ in range(args.steps):
+            graph.replay()
+        e1.record(s)
+        torch.cuda.synchronize()
+        if world > 1:
+            torch.distributed.barrier()
+    ms_total = e0.elapsed_time(e1)
+    if world > 1:
+        t = torch.tensor([ms_total], device=dev)
+        torch.distributed.all_reduce(t, op=torch.distributed.ReduceOp.MAX)
+        ms_total = float(t.item())
+    ms_step = ms_total / args.steps
+    st = status.cpu().numpy()
+    if st.any():
+        raise RuntimeError(f"device status word reports an error: {st.tolist()}")
+
+    # per-launch duration of the dominant kernel (decode split-K), CUDA events on its stream
+    dur = []
+    ev = [torch.cuda.Event(enable_timing=True) for _ in range(2 * ncalls)]
+    with torch.cuda.stream(s):
+        for r in range(3):
+            i = 0
+            for (lp, layer, grp) in order:
+                t = temp_all[layer * G + grp]
+                ev[2 * i].record(s)
+                rq.rq_decode_attention(handle, layer, grp, lp, B, q_all[i], t[lp, 0, :, :, 0], t[lp, 1, :, :, 0],
+                                       seq, scale, out_all[i], ws, ws_bytes, s.cuda_stream)
+                ev[2 * i + 1].record(s)
+                i += 1
+            torch.cuda.synchronize()
+            if r > 0:
+                dur += [ev[2 * k].elapsed_time(ev[2 * k + 1]) for k in range(ncalls)]
+    byts = algorithmic_bytes_per_step(w, B, N)
+    per_launch_bytes = ((P - 1) * byts["call_res"] + byts["call_anchor"]) / P
+    avg_launch_ms = statistics.mean(dur)
+    peak, peak_kind = _peaks()
+    achieved = per_launch_bytes / (avg_launch_ms / 1e3) / 1e9
+    traffic = None
+    tp = os.path.join(ROOT, "profiles", "traffic_per_launch.json")
+    if os.path.exists(tp):
+        try:
+            tj = json.load(open(tp))
+            if tj.get("workload") == w.name and tj.get("kernel_source_hash") == _kernel_hash():
+                traffic = tj.get("bytes_per_launch")
+        except Exception:
+            traffic = None
+
+    step_gbs = byts["step"] / (ms_step / 1e3) / 1e9
+    value = world * B / (ms_step / 1e3)
+    line = {
+        "metric": METRIC, "value": value, "unit": "tokens/s", "n_gpus": world, "steps": args.steps,
+        "warmup": args.warmup, "ms_per_step": ms_step, "higher_is_better": True, "scaling": "weak",
+        "vs_baseline": None, "dtype": "fp32", "data": "synthetic", "config": _config(w),
+        "effective_gbps": step_gbs, "frac_of_hbm_peak": step_gbs / peak,
+        "roofline": {"bound": "hbm", "achieved": achieved, "peak": peak, "unit": "GB/s",
+                     "frac": achieved / peak, "traffic": traffic,
+                     "kernel": "rq decode split-K (decode_kernel)",
+                     "peak_source": f"MEASURED_PEAKS.json hbm_gbs ({peak_kind})",
+                     "avg_launch_ms": avg_launch_ms, "bytes_per_launch": per_launch_bytes},
+        "gpu_launches": launches_per_step * args.steps,
+        "clocks": clk.summary(),
+        "prefill_s": prefill_s,
+    }
+    # BF16 comparator: the same 96 calls over uncompressed K/V
+    if not args.no_bf16:
+        line["bf16_comparator"] = bench_bf16(args, w, dev, gen, scale)
+        # whole compressed step (appends included) against the BF16 attention calls alone
+        line["speedup_vs_bf16"] = line["bf16_comparator"]["ms_per_step_attention"] / ms_step
+    if not args.no_e2e:
+        line["e2e"] = bench_e2e(args, graph, s, q_all, temp_all, out_all, B)
+    if rank == 0 and not args.no_cpu and world == 1:
+        line["cpu_baseline"] = cpu_baseline(w, B, N, budget_s=15.0)
+    rq.rq_cache_destroy(handle)
+    if rank == 0:
+        print(json.dumps(line))
+
+
+def bench_bf16(args, w, dev, gen, scale):
+    """The library's BF16 decode kernel over the same calls (K/V [B,H,N,d] per call)."""
+    import torch
+    import decode_attention_rq_gb300 as rq
+    L, P, G, H, d, B, N = w.num_layers, w.loops_per_group, w.num_groups, w.num_heads, w.head_dim, w.batch, w.context
+    ncalls = L * G * P
+    kv = torch.empty((ncalls, 2, B, H, N, d), dtype=torch.bfloat16, device=dev)
+    kv.normal_(generator=gen)
+    q = torch.randn((ncalls, B, H, d), generator=gen, device=dev).to(torch.bfloat16)
+    cur = torch.randn((ncalls, 2, B, H, d), generator=gen, device=dev).to(torch.bfloat16)
+    out = torch.empty((B, H, d), dtype=torch.float32, device=dev)
+    seq = torch.full((B,), N, dtype=torch.int32, device=dev)
+    ws_bytes = rq.rq_bf16_workspace_bytes(B, H, d)
+    ws = torch.zeros(ws_bytes, dtype=torch.uint8, device=dev)
+    s = torch.cuda.Stream(device=dev)
+
+    def step(st):
+        for i in range(ncalls):
+            rq.rq_decode_attention_bf16(kv[i, 0], kv[i, 1], cur[i, 0], cur[i, 1], q[i], seq, B, H, d, N, scale,
+                                        out, ws, ws_bytes, st)
+    with torch.cuda.stream(s):
+        step(s.cuda_stream)
+    torch.cuda.synchronize()
+    graph = torch.cuda.CUDAGraph()
+    with torch.cuda.graph(graph, stream=s):
+        step(s.cuda_stream)
+    for _ in range(args.warmup):
+        graph.replay()
+    torch.cuda.synchronize()
+    e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    e0.record(s)
+    for _ in range(args.steps):
+        graph.replay()
+    e1.record(s)
+    torch.cuda.synchronize()
+    ms = e0.elapsed_time(e1) / args.steps
+    byts = ncalls * B * H * (N * 2 * d * 2 + 3 * d * 2 + d * 4)
+    peak, _ = _peaks()
+    del kv
+    torch.cuda.empty_cache()
+    return {"ms_per_step_attention": ms, "tokens_per_s": B / (ms / 1e3), "calls": ncalls,
+            "effective_gbps": byts / (ms / 1e3) / 1e9, "frac_of_hbm_peak": byts / (ms / 1e3) / 1e9 / peak}
+
+
+def bench_e2e(args, graph, s, q_all, temp_all, out_all, B):
+    """Same step with its per-step inputs coming from pinned host memory and the
+    step's attention outputs read back, copies inside the timed region."""
+    import torch
+    q_h = q_all.cpu().pin_memory()
+    t_h = temp_all.cpu().pin_memory()
+    o_h = torch.empty(out_all.shape, dtype=out_all.dtype).pin_memory()
+    for _ in range(args.warmup):
+        graph.replay()
+    torch.cuda.synchronize()
+    t0 = time.perf_counter()
+    e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    with torch.cuda.stream(s):
+        e0.record(s)
+        for _ in range(args.steps):
+            q_all.copy_(q_h, non_blocking=True)
+            temp_all.copy_(t_h, non_blocking=True)
+            graph.replay()
+            o_h.copy_(out_all, non_blocking=True)
+        e1.record(s)
+    torch.cuda.synchronize()
+    ms = e0.elapsed_time(e1) / args.steps
+    wall = (time.perf_counter() - t0) / args.steps * 1e3
+    h2d = q_all.numel() * q_all.element_size() + temp_all.numel() * temp_all.element_size()
+    d2h = out_all.numel() * out_all.element_size()
+    return {"value": B / (ms / 1e3), "unit": "tokens/s", "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h,
+            "ms_per_step": ms, "wall_ms_per_step": wall}
+
+
+def _kernel_hash():
+    import hashlib
+    h = hashlib.sha256()
+    csrc = os.path.join(ROOT, "decode_attention_rq_gb300", "csrc")
+    for f in sorted(os.listdir(csrc)):
+        h.update(open(os.path.join(csrc, f), "rb").read())
+    return h.hexdigest()[:16]
+
+
+if __name__ == "__main__":
+    main()

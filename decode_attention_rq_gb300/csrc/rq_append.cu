@@ -1,0 +1,341 @@
+// rq_append: compress new tokens of one (layer, loop group) into the cache.
+//
+// Follows the stored-overlay paragraph of the explainer "ResidualQuant stores
+// looped-Transformer KV caches as 2-bit residuals": the group's last loop is
+// the INT4 anchor; every earlier loop l stores c_l (BF16 least-squares
+// coefficient against the dequantized anchor, or in chained mode against the
+// rebuilt loop l+1), and the 2-bit code of u_l = R (kv_l - c_l * ref).
+// Group quantizer per rq.h: E4M3 offset = min, E4M3 scale = range / (2^b-1),
+// code = exact nearest grid point, ties to even.
+//
+// Precision: every decision that fixes a stored byte (min/max, the E4M3
+// roundings, the nearest code, the BF16 coefficient) is taken exactly -- the
+// scalar steps run in float64 where float32 could round -- so stored bytes
+// match the exact-arithmetic reading for a given rotated residual.  The
+// rotation itself (d x d per vector) runs in float32 FMA.
+//
+// Grid: x = block of 4-position quads of one row, y = row * H + head, z = K/V.
+// A CTA owns whole aligned quads of positions, so the channel-major V bytes
+// it writes (2 or 4 positions per byte) are touched by no other CTA.
+#include <cuda_fp8.h>
+
+#include "rq_internal.cuh"
+
+namespace rq {
+namespace {
+
+constexpr int kThreads = 128;      // one thread per channel (d <= 128)
+constexpr int kQuadsPerCta = 4;    // 16 positions per CTA
+constexpr int kTok = 4 * kQuadsPerCta;
+
+__device__ __forceinline__ uint8_t f32_to_e4m3(float x) {
+  return (uint8_t)__nv_cvt_float_to_fp8(x, __NV_SATFINITE, __NV_E4M3);
+}
+__device__ __forceinline__ float e4m3_to_f32(uint8_t b) {
+  __half_raw hr = __nv_cvt_fp8_to_halfraw((__nv_fp8_storage_t)b, __NV_E4M3);
+  return __half2float(__half(hr));
+}
+
+// E4M3 byte nearest to D / qmax (D >= 0 exact in float64), ties to the even
+// code, saturating at 448.  A float32 estimate gives a candidate; the exact
+// comparison |D - qmax * v(c)| over the candidate and its two neighbours
+// (all products exact: 4-bit significand times a 4-bit integer) decides.
+__device__ uint8_t e4m3_nearest_ratio(double D, int qmax) {
+  float est = __fdiv_rn((float)D, (float)qmax);
+  int c0 = f32_to_e4m3(est);
+  int best = -1;
+  double best_d = 0.0;
+  for (int c = c0 - 1; c <= c0 + 1; ++c) {
+    if (c < 0 || c > 0x7E) continue;
+    double dist = fabs(D - (double)qmax * (double)e4m3_to_f32((uint8_t)c));
+    if (best < 0 || dist < best_d || (dist == best_d && (c & 1) == 0)) {
+      best = c;
+      best_d = dist;
+    }
+  }
+  return (uint8_t)best;
+}
+
+// Nearest k of v to o + k s (exact), ties to even k, clamped to [0, qmax].
+__device__ int nearest_code(float v, float o, float s, int qmax) {
+  if (!(s > 0.f)) return 0;
+  double t = (double)v - (double)o;                 // exact: fp32 minus an E4M3 value
+  float kf = rintf(__fdiv_rn((float)t, s));
+  kf = fminf(fmaxf(kf, -1.f), (float)(qmax + 1));
+  int k = (int)kf;
+  double sd = (double)s;
+  double r = t - (double)k * sd;                    // exact
+  if (2.0 * r > sd) ++k;
+  else if (2.0 * r < -sd) --k;
+  r = t - (double)k * sd;
+  if (2.0 * fabs(r) == sd && (k & 1)) k += (r > 0.0) ? 1 : -1;
+  return min(max(k, 0), qmax);
+}
+
+// Group quantizer for one element per lane; the g lanes of a group are
+// consecutive lanes of one warp (g = 16 or 32).  Returns the code; writes
+// the dequantized value and (on every lane) the scale/offset bytes.
+__device__ int quantize_lane(float v, bool active, int g, int qmax, uint8_t* s_byte,
+                             uint8_t* o_byte, float* vhat) {
+  float lo = active ? v : INFINITY, hi = active ? v : -INFINITY;
+  for (int off = g / 2; off > 0; off >>= 1) {
+    lo = fminf(lo, __shfl_xor_sync(0xffffffffu, lo, off, g));
+    hi = fmaxf(hi, __shfl_xor_sync(0xffffffffu, hi, off, g));
+  }
+  uint8_t ob = f32_to_e4m3(lo);
+  uint8_t sb = e4m3_nearest_ratio((double)hi - (double)lo, qmax);
+  float o = e4m3_to_f32(ob), s = e4m3_to_f32(sb);
+  int code = nearest_code(v, o, s, qmax);
+  *s_byte = sb;
+  *o_byte = ob;
+  *vhat = fmaf(s, (float)code, o);                  // exact (few significant bits)
+  return code;
+}
+
+// BF16 bits of the float64 value x, round to nearest even: round-to-odd to
+// float32 first (exact for the later 8-bit rounding), then RNE to BF16.
+__device__ uint16_t f64_to_bf16_bits(double x) {
+  float f = __double2float_rz(x);
+  if ((double)f != x) f = __uint_as_float(__float_as_uint(f) | 1u);
+  __nv_bfloat16 b = __float2bfloat16_rn(f);
+  return *reinterpret_cast<uint16_t*>(&b);
+}
+
+struct AppendArgs {
+  Geom g;
+  uint8_t* base;
+  const float* R;
+  const __nv_bfloat16* kv;
+  const int32_t* seq_lens;
+  int32_t* status;
+  int layer, group, batch, n;
+};
+
+__device__ __forceinline__ float load_x(const AppendArgs& a, int p, int kvi, int b, int h, int t,
+                                        int k) {
+  size_t idx = ((((size_t)p * 2 + kvi) * a.batch + b) * a.g.H + h) * (size_t)a.n + t;
+  return __bfloat162float(a.kv[idx * a.g.d + k]);
+}
+
+// Write the codes / metadata (and c) of the CTA's tokens into one plane.
+__device__ void write_plane(const AppendArgs& a, uint8_t* plane, int64_t tile_bytes,
+                            int64_t codes_bytes, int bits, bool channel_major, int p0,
+                            const bool* valid, const uint8_t (*codes)[128],
+                            const uint16_t (*meta)[8], const uint16_t* cbits) {
+  const int d = a.g.d, ng = a.g.ng, tid = threadIdx.x;
+  const int per_byte = 8 / bits;
+  if (!channel_major) {
+    // token-major rows: thread handles byte `tid` of every token row
+    const int row_bytes = d / per_byte;
+    for (int t = 0; t < kTok; ++t) {
+      if (!valid[t] || tid >= row_bytes) continue;
+      int pos = p0 + t;
+      uint8_t* row = plane + (int64_t)(pos / kTile) * tile_bytes + (pos % kTile) * row_bytes;
+      uint32_t byte = 0;
+      for (int m = 0; m < per_byte; ++m) byte |= (uint32_t)codes[t][tid * per_byte + m] << (bits * m);
+      row[tid] = (uint8_t)byte;
+    }
+  } else {
+    // channel-major rows: thread = channel, one byte per `per_byte` positions
+    if (tid < d) {
+      const int row_bytes = kTile / per_byte;
+      for (int t0 = 0; t0 < kTok; t0 += per_byte) {
+        bool any = false;
+        for (int m = 0; m < per_byte; ++m) any |= valid[t0 + m];
+        if (!any) continue;
+        int pos0 = p0 + t0;   // aligned to per_byte (p0 is quad-aligned)
+        uint8_t* byte_ptr = plane + (int64_t)(pos0 / kTile) * tile_bytes + tid * row_bytes +
+                            (pos0 % kTile) / per_byte;
+        uint32_t byte = *byte_ptr;
+        for (int m = 0; m < per_byte; ++m) {
+          if (!valid[t0 + m]) continue;
+          uint32_t mask = ((1u << bits) - 1u) << (bits * m);
+          byte = (byte & ~mask) | ((uint32_t)codes[t0 + m][tid] << (bits * m));
+        }
+        *byte_ptr = (uint8_t)byte;
+      }
+    }
+  }
+  // metadata (scale, offset) per group, and c
+  for (int i = tid; i < kTok * ng; i += kThreads) {
+    int t = i / ng, gi = i % ng;
+    if (!valid[t]) continue;
+    int pos = p0 + t;
+    uint8_t* tile = plane + (int64_t)(pos / kTile) * tile_bytes;
+    *reinterpret_cast<uint16_t*>(tile + codes_bytes + (pos % kTile) * ng * 2 + gi * 2) = meta[t][gi];
+  }
+  if (cbits) {
+    for (int t = tid; t < kTok; t += kThreads) {
+      if (!valid[t]) continue;
+      int pos = p0 + t;
+      uint8_t* tile = plane + (int64_t)(pos / kTile) * tile_bytes;
+      *reinterpret_cast<uint16_t*>(tile + codes_bytes + a.g.meta + (pos % kTile) * 2) = cbits[t];
+    }
+  }
+}
+
+__global__ void __launch_bounds__(kThreads) append_kernel(AppendArgs a) {
+  const int d = a.g.d, gs = a.g.g, P = a.g.P, tid = threadIdx.x;
+  const int b = blockIdx.y / a.g.H, h = blockIdx.y % a.g.H, kvi = blockIdx.z;
+  const bool chained = a.g.mode == RQ_MODE_CHAINED;
+
+  __shared__ float ref_s[kTok][128];     // anchor_hat (shared) or rebuilt loop l+1 (chained)
+  __shared__ float x_s[kTok][128];       // current loop, then its residual
+  __shared__ float u_s[kTok][128];       // rotated residual
+  __shared__ uint8_t codes_s[kTok][128];
+  __shared__ uint16_t meta_s[kTok][8];
+  __shared__ uint16_t c_s[kTok];
+  __shared__ float cb_s[kTok];
+  __shared__ bool valid_s[kTok];
+
+  const int start = a.seq_lens[b];
+  if (start < 0 || start + a.n > a.g.Nmax) {
+    if (blockIdx.x == 0 && h == 0 && kvi == 0 && tid == 0 && a.status) atomicExch(&a.status[1], 1);
+    return;
+  }
+  const int q_first = start / 4, q_last = (start + a.n - 1) / 4;
+  const int q0 = q_first + blockIdx.x * kQuadsPerCta;
+  if (q0 > q_last) return;
+  const int p0 = q0 * 4;
+  if (tid < kTok) {
+    int pos = p0 + tid;
+    valid_s[tid] = pos >= start && pos < start + a.n;
+  }
+  __syncthreads();
+
+  uint8_t* region = a.base + a.g.region_offset(a.layer, a.group, b, h);
+  const bool act = tid < d;
+
+  // ---- anchor: loop P-1, 4-bit ----
+  for (int t = 0; t < kTok; ++t) {
+    float v = (act && valid_s[t]) ? load_x(a, P - 1, kvi, b, h, p0 + t - start, tid) : 0.f;
+    uint8_t sb, ob;
+    float vh;
+    int code = quantize_lane(v, act, gs, 15, &sb, &ob, &vh);
+    if (act) {
+      codes_s[t][tid] = (uint8_t)code;
+      ref_s[t][tid] = vh;
+      if (tid % gs == 0) meta_s[t][tid / gs] = (uint16_t)sb | ((uint16_t)ob << 8);
+    }
+  }
+  __syncthreads();
+  write_plane(a, region + a.g.anchor_plane(kvi), a.g.a_tile, a.g.a_codes, 4, kvi == 1, p0, valid_s,
+              codes_s, meta_s, nullptr);
+  __syncthreads();
+
+  // ---- earlier loops: shared mode any order; chained from P-2 down ----
+  for (int j = P - 2; j >= 0; --j) {
+    if (act)
+      for (int t = 0; t < kTok; ++t)
+        x_s[t][tid] = valid_s[t] ? load_x(a, j, kvi, b, h, p0 + t - start, tid) : 0.f;
+    __syncthreads();
+    // least-squares coefficient per token (float64: the products are exact
+    // and their sums exact for data of moderate dynamic range)
+    {
+      const int warp = tid / 32, lane = tid % 32;
+      for (int t = warp; t < kTok; t += kThreads / 32) {
+        double num = 0.0, den = 0.0;
+        for (int k = lane; k < d; k += 32) {
+          double y = ref_s[t][k], x = x_s[t][k];
+          num = fma(x, y, num);
+          den = fma(y, y, den);
+        }
+        for (int off = 16; off > 0; off >>= 1) {
+          num += __shfl_xor_sync(0xffffffffu, num, off);
+          den += __shfl_xor_sync(0xffffffffu, den, off);
+        }
+        if (lane == 0) {
+          double c = den > 0.0 ? num / den : 0.0;
+          uint16_t bits = f64_to_bf16_bits(c);
+          c_s[t] = bits;
+          cb_s[t] = bf16_bits_to_f32(bits);
+        }
+      }
+    }
+    __syncthreads();
+    // residual e = x - cb * ref (float32, one rounding)
+    if (act)
+      for (int t = 0; t < kTok; ++t) x_s[t][tid] = fmaf(-cb_s[t], ref_s[t][tid], x_s[t][tid]);
+    __syncthreads();
+    // rotation u = R e, thread = output channel, sequential FMA over k
+    if (act) {
+      float acc[kTok];
+#pragma unroll
+      for (int t = 0; t < kTok; ++t) acc[t] = 0.f;
+      const float4* Rrow = reinterpret_cast<const float4*>(a.R + (size_t)tid * d);
+      for (int k4 = 0; k4 < d / 4; ++k4) {
+        float4 r = __ldg(Rrow + k4);
+#pragma unroll
+        for (int t = 0; t < kTok; ++t) {
+          float4 e = *reinterpret_cast<const float4*>(&x_s[t][4 * k4]);
+          acc[t] = fmaf(r.x, e.x, acc[t]);
+          acc[t] = fmaf(r.y, e.y, acc[t]);
+          acc[t] = fmaf(r.z, e.z, acc[t]);
+          acc[t] = fmaf(r.w, e.w, acc[t]);
+        }
+      }
+#pragma unroll
+      for (int t = 0; t < kTok; ++t) u_s[t][tid] = acc[t];
+    }
+    __syncthreads();
+    // 2-bit quantization of u
+    for (int t = 0; t < kTok; ++t) {
+      float v = (act && valid_s[t]) ? u_s[t][tid] : 0.f;
+      uint8_t sb, ob;
+      float vh;
+      int code = quantize_lane(v, act, gs, 3, &sb, &ob, &vh);
+      if (act) {
+        codes_s[t][tid] = (uint8_t)code;
+        u_s[t][tid] = vh;                     // r_hat, for the chained rebuild
+        if (tid % gs == 0) meta_s[t][tid / gs] = (uint16_t)sb | ((uint16_t)ob << 8);
+      }
+    }
+    __syncthreads();
+    write_plane(a, region + a.g.res_plane(j, kvi), a.g.r_tile, a.g.r_codes, 2, kvi == 1, p0,
+                valid_s, codes_s, meta_s, c_s);
+    if (chained && j > 0) {
+      // rebuilt loop j = cb * ref + R^T r_hat becomes the reference of loop j-1
+      float acc[kTok];
+#pragma unroll
+      for (int t = 0; t < kTok; ++t) acc[t] = 0.f;
+      if (act) {
+        for (int k = 0; k < d; ++k) {
+          float r = __ldg(a.R + (size_t)k * d + tid);
+#pragma unroll
+          for (int t = 0; t < kTok; ++t) acc[t] = fmaf(r, u_s[t][k], acc[t]);
+        }
+      }
+      __syncthreads();   // everyone has read ref_s / u_s of this loop
+      if (act) {
+#pragma unroll
+        for (int t = 0; t < kTok; ++t) ref_s[t][tid] = fmaf(cb_s[t], ref_s[t][tid], acc[t]);
+      }
+    }
+    __syncthreads();
+  }
+}
+
+}  // namespace
+
+cudaError_t launch_append(const rq_cache& c, int layer, int group, int batch,
+                          const __nv_bfloat16* kv, const int32_t* seq_lens, int n_tokens,
+                          int32_t* status, cudaStream_t stream) {
+  AppendArgs a;
+  a.g = c.geom;
+  a.base = c.base;
+  a.R = c.R;
+  a.kv = kv;
+  a.seq_lens = seq_lens;
+  a.status = status;
+  a.layer = layer;
+  a.group = group;
+  a.batch = batch;
+  a.n = n_tokens;
+  // quads touched by n tokens starting anywhere: at most (n + 3) / 4 + 1
+  int quads = (n_tokens + 3) / 4 + 1;
+  dim3 grid((quads + kQuadsPerCta - 1) / kQuadsPerCta, batch * c.geom.H, 2);
+  append_kernel<<<grid, kThreads, 0, stream>>>(a);
+  return cudaGetLastError();
+}
+
+}  // namespace rq

@@ -1,0 +1,130 @@
+// Internal declarations shared by the librq translation units (not installed).
+#pragma once
+
+#include <cstddef>
+#include <cstdint>
+#include <cuda_runtime.h>
+#include <cuda_bf16.h>
+#include <cuda_fp16.h>
+
+#include "rq.h"
+
+namespace rq {
+
+constexpr int kTile = 64;            // token slots per tile (layout constant, see rq.h)
+constexpr int kAnchorBits = 4;
+constexpr int kResBits = 2;
+constexpr int kMaxLoops = 8;
+constexpr int kStatusWords = 4;      // int32 status word at the start of a workspace
+constexpr unsigned long long kWaitNs = 2000000000ull;  // give up an mbarrier wait after 2 s
+
+// Byte geometry of a cache (mirrors the layout statement in rq.h).
+struct Geom {
+  int L, P, G, H, d, g, ng, Bmax, Nmax, ntiles, mode;
+  int64_t a_codes, r_codes, meta, a_tile, r_tile;   // per tile, bytes
+  int64_t plane_a, plane_r, region;                 // bytes
+
+  __host__ __device__ int64_t region_offset(int layer, int group, int b, int h) const {
+    return ((((int64_t)layer * G + group) * Bmax + b) * H + h) * region;
+  }
+  __host__ __device__ int64_t anchor_plane(int kv) const { return (int64_t)kv * plane_a; }
+  __host__ __device__ int64_t res_plane(int j, int kv) const {
+    return 2 * plane_a + (int64_t)(2 * j + kv) * plane_r;
+  }
+};
+
+// Returns false when the shape is outside the supported set.
+bool make_geom(const rq_config& c, Geom* g);
+
+}  // namespace rq
+
+struct rq_cache {
+  rq_config cfg;
+  rq::Geom geom;
+  uint8_t* base;
+  const float* R;
+  int device;
+  int num_sms;
+};
+
+namespace rq {
+
+// ---- launchers (one per translation unit) ----
+cudaError_t launch_append(const rq_cache& c, int layer, int group, int batch,
+                          const __nv_bfloat16* kv, const int32_t* seq_lens, int n_tokens,
+                          int32_t* status, cudaStream_t stream);
+
+size_t decode_workspace_bytes(const Geom& g, int batch, int num_sms);
+cudaError_t launch_decode(const rq_cache& c, int layer, int group, int loop, int batch,
+                          const __nv_bfloat16* q, const __nv_bfloat16* k_cur,
+                          const __nv_bfloat16* v_cur, const int32_t* seq_lens, float scale,
+                          float* out, void* workspace, cudaStream_t stream);
+
+size_t bf16_workspace_bytes(int batch, int heads, int d, int num_sms);
+cudaError_t launch_bf16(const __nv_bfloat16* k, const __nv_bfloat16* v,
+                        const __nv_bfloat16* k_cur, const __nv_bfloat16* v_cur,
+                        const __nv_bfloat16* q, const int32_t* seq_lens, int batch, int heads,
+                        int d, int max_seq, float scale, float* out, void* workspace,
+                        int num_sms, cudaStream_t stream);
+
+// ---- device helpers: shared-memory TMA bulk copies and mbarriers ----
+#if defined(__CUDACC__)
+__device__ __forceinline__ uint32_t smem_u32(const void* p) {
+  return static_cast<uint32_t>(__cvta_generic_to_shared(p));
+}
+__device__ __forceinline__ void mbar_init(uint64_t* bar, uint32_t count) {
+  asm volatile("mbarrier.init.shared::cta.b64 [%0], %1;" ::"r"(smem_u32(bar)), "r"(count) : "memory");
+}
+__device__ __forceinline__ void fence_mbar_init() {
+  asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
+}
+__device__ __forceinline__ void mbar_arrive_expect_tx(uint64_t* bar, uint32_t bytes) {
+  asm volatile("mbarrier.arrive.expect_tx.shared::cta.b64 _, [%0], %1;" ::"r"(smem_u32(bar)), "r"(bytes)
+               : "memory");
+}
+__device__ __forceinline__ bool mbar_try_wait(uint64_t* bar, uint32_t parity) {
+  uint32_t ok;
+  asm volatile(
+      "{\n\t.reg .pred p;\n\t"
+      "mbarrier.try_wait.parity.shared::cta.b64 p, [%1], %2;\n\t"
+      "selp.u32 %0, 1, 0, p;\n\t}"
+      : "=r"(ok)
+      : "r"(smem_u32(bar)), "r"(parity)
+      : "memory");
+  return ok != 0;
+}
+__device__ __forceinline__ unsigned long long global_ns() {
+  unsigned long long t;
+  asm volatile("mov.u64 %0, %globaltimer;" : "=l"(t));
+  return t;
+}
+// Waits for the phase with the given parity; gives up after kWaitNs of wall time.
+__device__ __forceinline__ bool mbar_wait_bounded(uint64_t* bar, uint32_t parity) {
+  if (mbar_try_wait(bar, parity)) return true;
+  const unsigned long long t0 = global_ns();
+  while (!mbar_try_wait(bar, parity))
+    if (global_ns() - t0 > kWaitNs) return false;
+  return true;
+}
+// 1-D bulk copy global -> this CTA's shared memory, completing on `bar`.
+// dst, src 16-byte aligned; bytes a multiple of 16.
+__device__ __forceinline__ void bulk_g2s(void* dst, const void* src, uint32_t bytes, uint64_t* bar) {
+  asm volatile(
+      "cp.async.bulk.shared::cluster.global.mbarrier::complete_tx::bytes [%0], [%1], %2, [%3];" ::"r"(
+          smem_u32(dst)),
+      "l"(src), "r"(bytes), "r"(smem_u32(bar))
+      : "memory");
+}
+__device__ __forceinline__ float bf16_bits_to_f32(uint32_t bits16) {
+  return __uint_as_float(bits16 << 16);
+}
+// Two E4M3 bytes (low byte first) -> two floats, exact.
+__device__ __forceinline__ float2 e4m3x2_to_f32x2(uint16_t v) {
+  uint32_t h2;
+  asm("{\n\t.reg .b16 t;\n\tmov.b16 t, %1;\n\tcvt.rn.f16x2.e4m3x2 %0, t;\n\t}" : "=r"(h2) : "h"(v));
+  __half2 hh = *reinterpret_cast<__half2*>(&h2);
+  return __half22float2(hh);
+}
+#endif
+
+}  // namespace rq

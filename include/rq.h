@@ -1,0 +1,182 @@
+/*
+ * rq.h - ResidualQuant KV cache and decode attention for NVIDIA GB300 (sm_103a).
+ *
+ * ResidualQuant (the learnaivisually explainer "ResidualQuant stores
+ * looped-Transformer KV caches as 2-bit residuals", and the ai4snews summary
+ * of the arXiv paper) compresses the KV cache of a looped Transformer.  The
+ * last loop of each loop group is stored as an INT4 "anchor"; every earlier
+ * loop l is stored as a 2-bit code of the rotated residual
+ *     u_l = R (kv_l - c_l * anchor_hat),  c_l = <kv_l, anchor_hat> / <anchor_hat, anchor_hat>,
+ * with c_l kept in BF16 and R a fixed orthogonal rotation.  Channels are
+ * grouped (g = 32 or 16) with an FP8-E4M3 scale and offset per group.
+ * Decode attention rebuilds c * anchor_hat + R^T dequant(u) on chip and never
+ * writes the rebuilt K/V to memory.
+ *
+ * Conventions for every entry point
+ *   - Device pointers are caller-owned device memory (e.g. from PyTorch);
+ *     the library never allocates or frees device memory and never
+ *     synchronizes the device.  Host pointers are marked "host".
+ *   - `stream` is a cudaStream_t passed as void* (NULL = legacy default
+ *     stream).  Work is enqueued asynchronously on it.
+ *   - Argument errors are found on the host before anything is enqueued and
+ *     return a status; nothing is launched then.  A failed launch returns
+ *     RQ_ERR_CUDA.  Faults inside a kernel surface on a later CUDA call.
+ *   - Device pointers must be 16-byte aligned (RQ_ERR_ALIGNMENT).
+ *   - Supported shapes: head_dim in {96, 128}; group_size in {16, 32} dividing
+ *     head_dim; loops_per_group in [1, 8].  Others: RQ_ERR_UNSUPPORTED.
+ *
+ * ---------------------------------------------------------------------------
+ * Cache byte layout (this library's format; the pages fix the record
+ * contents, not their placement)
+ *   The cache is L x G x max_batch x H regions, index
+ *   ((layer * G + group) * max_batch + b) * H + h, each `region` bytes.
+ *   A region holds planes AK, AV, then RK_j, RV_j for j = 0 .. P-2.
+ *   Each plane is ntiles = ceil(max_seq_len / 64) tiles of 64 token slots;
+ *   tile t holds positions 64t .. 64t+63.
+ *     anchor tile  (AK, AV)  : codes[64 * d/2] | meta[64 * ng * 2]
+ *     residual tile (RK, RV) : codes[64 * d/4] | meta[64 * ng * 2] | c[64 * 2]
+ *   K codes are token-major: row r = the token's d codes;
+ *     INT4 byte i = ch 2i (bits 0-3) | ch 2i+1 (bits 4-7);
+ *     INT2 byte i = ch 4i+m in bits 2m..2m+1.
+ *   V codes are channel-major: row ch = that channel's 64 token codes;
+ *     INT4 byte i = token 2i | token 2i+1 << 4; INT2 byte i = token 4i+m in bits 2m.
+ *   meta row r: for each channel group, the E4M3 scale byte then the E4M3
+ *     offset byte.  c slot r: BF16, little-endian.
+ *   Every tile and sub-block size is a multiple of 16 bytes.
+ *
+ * Quantizer (both code widths): per group, o = E4M3(min), s = E4M3((max-min)/(2^b-1)),
+ * rounded to nearest even and saturating at +-448; code = the nearest grid
+ * point o + k*s to the exact value, ties to even k, clamped to [0, 2^b-1];
+ * s == 0 gives code 0.  Dequantized value: s * code + o.
+ * ---------------------------------------------------------------------------
+ */
+#ifndef RQ_H_
+#define RQ_H_
+
+#include <stddef.h>
+#include <stdint.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+typedef enum rq_status {
+  RQ_OK = 0,
+  RQ_ERR_INVALID_ARG = 1,   /* null pointer, index out of range, bad count */
+  RQ_ERR_ALIGNMENT = 2,     /* a device pointer is not 16-byte aligned */
+  RQ_ERR_CAPACITY = 3,      /* batch > max_batch, or a write past max_seq_len */
+  RQ_ERR_WORKSPACE = 4,     /* workspace smaller than the *_workspace_bytes value */
+  RQ_ERR_CUDA = 5,          /* a CUDA runtime call or kernel launch failed */
+  RQ_ERR_UNSUPPORTED = 6,   /* head_dim / group_size / loops outside the supported set */
+  RQ_ERR_TIMEOUT = 7        /* a device-side wait gave up (reported via the status word) */
+} rq_status;
+
+typedef enum rq_mode {
+  RQ_MODE_SHARED = 0,   /* every earlier loop coded against the anchor: 2 plane reads per loop */
+  RQ_MODE_CHAINED = 1   /* loop l coded against the rebuilt loop l+1: reads grow with distance */
+} rq_mode;
+
+/* Shape of one cache.  The anchor is 4-bit and residuals 2-bit (fixed). */
+typedef struct rq_config {
+  int32_t num_layers;       /* L: layers of the shared block */
+  int32_t loops_per_group;  /* P: loops per anchor group; the last one is the anchor */
+  int32_t num_groups;       /* G: loop groups (Ouro-1.4B: 1 group of 4; Huginn-3.5B: 8 of 4) */
+  int32_t num_heads;        /* H: KV heads (= query heads; multi-head attention) */
+  int32_t head_dim;         /* d: 96 or 128 */
+  int32_t group_size;       /* g: 16 or 32 channels per quantization group */
+  int32_t max_batch;        /* rows of the cache */
+  int32_t max_seq_len;      /* token capacity per (layer, group, row, head) */
+  int32_t mode;             /* rq_mode */
+} rq_config;
+
+typedef struct rq_cache rq_cache;   /* opaque host-side handle; holds no device memory */
+
+/* Bytes of device memory a cache of this shape needs (0 if the shape is invalid).
+ * Host only; no CUDA call. */
+size_t rq_cache_bytes(const rq_config* cfg);
+
+/* Bind a cache to caller memory.
+ *   cfg    host; copied.
+ *   dev_buf device, >= rq_cache_bytes(cfg) bytes, 16-byte aligned.  Its
+ *          contents are the cache; the caller zero-fills it before first use
+ *          (only needed for byte-exact comparisons: unwritten slots are never read).
+ *   R_dev  device float32 [d][d] row-major, the rotation (orthogonal); caller
+ *          keeps it alive and unchanged while the cache is used.
+ *   out    host; receives the handle.  Free it with rq_cache_destroy.
+ * Errors: INVALID_ARG (null), UNSUPPORTED (shape), CAPACITY (bytes too small),
+ * ALIGNMENT. */
+rq_status rq_cache_create(const rq_config* cfg, void* dev_buf, size_t bytes,
+                          const float* R_dev, rq_cache** out);
+
+/* Free the host handle (not the caller's device memory).  NULL is accepted. */
+rq_status rq_cache_destroy(rq_cache* cache);
+
+/* Compress n_tokens new tokens of one (layer, group) for rows 0..batch-1 and
+ * write them at positions seq_lens[b] .. seq_lens[b] + n_tokens - 1.
+ * Follows the explainer's stored-overlay paragraph: anchor = last loop, INT4;
+ * every earlier loop: LS coefficient (BF16), rotated residual, INT2.
+ *   kv        device bf16 [P][2][batch][H][n_tokens][d] (loop, K/V, row, head, token, channel);
+ *             at decode time this is the BF16 temporary buffer with n_tokens = 1.
+ *   seq_lens  device int32 [batch], tokens already cached per row (not modified;
+ *             the caller advances it afterwards).  Every seq_lens[b] + n_tokens
+ *             must be <= max_seq_len: the host cannot see device values, so the
+ *             kernel skips a row that would overflow and sets status[1] = 1.
+ *   status    device int32[4] or NULL; see the status word under
+ *             rq_decode_workspace_bytes (the workspace's first 16 bytes serve).
+ * Errors: INVALID_ARG, CAPACITY (batch > max_batch or n_tokens > max_seq_len),
+ * ALIGNMENT, CUDA. */
+rq_status rq_append(rq_cache* cache, int32_t layer, int32_t group, int32_t batch,
+                    const void* kv, const int32_t* seq_lens, int32_t n_tokens,
+                    int32_t* status, void* stream);
+
+/* Workspace (device bytes) one rq_decode_attention call needs for `batch` rows
+ * on the current device.  The workspace must be zero-filled once before its
+ * first use; every call leaves its counters at zero again.  Its first 16 bytes
+ * are the status word (int32[4]): [0] != 0 after a device-side wait timed out,
+ * [1] != 0 after an append skipped a row that would overflow. */
+size_t rq_decode_workspace_bytes(const rq_config* cfg, int32_t batch);
+
+/* One decode-attention call: query loop `loop` (0-based; loop == P-1 is the
+ * anchor loop) of (layer, group), for rows 0..batch-1, all heads.
+ * Keys/values are the seq_lens[b] cached tokens rebuilt for this loop, plus
+ * the current token's BF16 K/V (the temporary buffer: the explainer's paragraph
+ * on why the last-loop anchor forces the current token to stay in BF16).
+ *   q              device bf16 [batch][H][d]
+ *   k_cur, v_cur   device bf16 [batch][H][d], this loop's K/V of the current token
+ *   seq_lens       device int32 [batch]
+ *   softmax_scale  e.g. 1/sqrt(d)
+ *   out            device float32 [batch][H][d]
+ *   workspace      device, >= rq_decode_workspace_bytes(cfg, batch), zeroed once
+ * Split-K over the sequence: each CTA of a balanced grid streams its range of
+ * tiles; the last CTA to finish a (row, head) merges the partial softmax
+ * states, adds the current token and applies R^T once.
+ * Errors: INVALID_ARG, CAPACITY (batch > max_batch), WORKSPACE, ALIGNMENT, CUDA. */
+rq_status rq_decode_attention(rq_cache* cache, int32_t layer, int32_t group, int32_t loop,
+                              int32_t batch, const void* q, const void* k_cur, const void* v_cur,
+                              const int32_t* seq_lens, float softmax_scale, float* out,
+                              void* workspace, size_t workspace_bytes, void* stream);
+
+/* Workspace (device bytes) for rq_decode_attention_bf16; same zero-once rule. */
+size_t rq_bf16_workspace_bytes(int32_t batch, int32_t num_heads, int32_t head_dim);
+
+/* Uncompressed comparator: the same split-K decode attention over plain BF16
+ * K/V (the role the pages give vLLM's BF16 FlashAttention baseline).
+ *   k_cache, v_cache  device bf16 [batch][H][max_seq][d]
+ *   k_cur, v_cur, q   device bf16 [batch][H][d]
+ *   seq_lens          device int32 [batch] (each <= max_seq)
+ *   out               device float32 [batch][H][d]
+ * Errors: INVALID_ARG, UNSUPPORTED (head_dim), WORKSPACE, ALIGNMENT, CUDA. */
+rq_status rq_decode_attention_bf16(const void* k_cache, const void* v_cache,
+                                   const void* k_cur, const void* v_cur, const void* q,
+                                   const int32_t* seq_lens, int32_t batch, int32_t num_heads,
+                                   int32_t head_dim, int32_t max_seq, float softmax_scale,
+                                   float* out, void* workspace, size_t workspace_bytes,
+                                   void* stream);
+
+/* Static description of a status code (never NULL). */
+const char* rq_status_string(rq_status status);
+
+#ifdef __cplusplus
+}
+#endif
+#endif /* RQ_H_ */

@@ -1,0 +1,279 @@
+"""GPU parity: the CUDA library (through the C ABI) against the CPU oracle.
+
+Bars (from the benchmark spec of the method and the oracle's readings):
+  * anchor planes (INT4 codes, E4M3 metadata): bit-exact, byte for byte;
+  * residual planes: the BF16 coefficient bytes bit-exact (shared mode);
+    codes and metadata equal except where the oracle's own float64 rotated
+    residual lies within a rounding tolerance of a rounding boundary (the
+    device rotates in float32) -- every such difference must be explained by
+    that, the differing code must be a neighbour, and they must be rare;
+  * attention outputs: max |gpu - oracle| <= 2e-3 (float32 output, O(1) data).
+"""
+import math
+
+import numpy as np
+import pytest
+import torch
+
+import oracle
+import synth
+from oracle import formats as F
+from rq_harness import Case, GpuCache, kv_for, plane_views, rotation32
+
+pytestmark = pytest.mark.gpu
+
+ATOL = 2e-3
+
+
+def _geom(case: Case):
+    return oracle.Geometry(case.L, case.P, case.G, case.H, case.d, case.g, case.B, case.Nmax)
+
+
+def _near_e4m3_midpoint(x, rel=1e-4):
+    """True where x is within rel of an E4M3 rounding boundary (midpoint of two neighbours)."""
+    x = np.abs(np.asarray(x, dtype=np.float64))
+    codes, vals = oracle.formats.e4m3_all_finite()
+    mids = (vals[:-1] + vals[1:]) / 2
+    i = np.searchsorted(mids, x)
+    d = np.full(x.shape, np.inf)
+    for k in (i - 1, i):
+        k = np.clip(k, 0, len(mids) - 1)
+        d = np.minimum(d, np.abs(x - mids[k]))
+    return d <= rel * np.maximum(x, 2.0 ** -9)
+
+
+def check_residual_parity(gbuf, obuf, geom, comp_u, layer, group, n, B, H, chained=False, max_rate=1e-3):
+    """comp_u[j]: oracle float64 rotated residual [2, B, H, n, d] for loop j."""
+    g, d, ng = geom.group_size, geom.head_dim, geom.ng
+    total, bad_codes, bad_groups, c_diff = 0, 0, 0, 0
+    for b in range(B):
+        for h in range(H):
+            for kv in range(2):
+                for j in range(geom.loops_per_group - 1):
+                    gc, gs, go, gcb = oracle.read_plane_tokens(gbuf, geom, layer, group, b, h, kv, "res", j, n)
+                    oc, os_, oo, ocb = oracle.read_plane_tokens(obuf, geom, layer, group, b, h, kv, "res", j, n)
+                    total += gc.size
+                    cd = gcb != ocb
+                    c_diff += int(cd.sum())
+                    if not chained:
+                        assert not cd.any(), f"BF16 coefficient differs (b={b} h={h} kv={kv} j={j})"
+                    u = comp_u[j][kv, b, h]                      # [n, d]
+                    ug = u.reshape(n, ng, g)
+                    meta_diff = (gs != os_) | (go != oo)         # [n, ng]
+                    tok_c = cd[:, None] & np.ones((1, ng), bool)
+                    if meta_diff.any():
+                        lo = ug.min(-1)
+                        rng = (ug.max(-1) - lo) / 3.0
+                        ok = _near_e4m3_midpoint(lo) | _near_e4m3_midpoint(rng) | tok_c
+                        assert ok[meta_diff].all(), "metadata differs away from an E4M3 rounding boundary"
+                        bad_groups += int(meta_diff.sum())
+                    code_diff = (gc != oc).reshape(n, ng, g) & ~meta_diff[..., None] & ~tok_c[..., None]
+                    if code_diff.any():
+                        s = F.e4m3_decode(os_)[..., None]
+                        o = F.e4m3_decode(oo)[..., None]
+                        qt = (ug - o) / np.where(s > 0, s, 1)
+                        frac = np.abs(qt - np.floor(qt) - 0.5)
+                        near = frac < 1e-3
+                        step = np.abs(gc.reshape(n, ng, g).astype(int) - oc.reshape(n, ng, g).astype(int))
+                        assert (near & (step == 1))[code_diff].all(), "code differs away from a rounding boundary"
+                        bad_codes += int(code_diff.sum())
+    rate = (bad_codes + bad_groups * g) / max(total, 1)
+    assert rate <= max_rate, f"boundary mismatches too frequent: {rate:.2e}"
+    return {"codes": total, "code_mismatch": bad_codes, "group_mismatch": bad_groups, "c_mismatch": c_diff}
+
+
+def _build_both(case: Case, chunks, seq_start=None, anchor_is_base=True):
+    """Append the same tokens (in the given chunk sizes) on both sides; return everything."""
+    R32, R = rotation32(case.d)
+    gpu = GpuCache(case, R32)
+    geom = _geom(case)
+    obuf = np.zeros(geom.total_bytes, dtype=np.uint8)
+    start = np.zeros(case.B, dtype=np.int64) if seq_start is None else np.array(seq_start)
+    us = [None] * (case.P - 1)
+    seed = case.seed
+    for layer in range(case.L):
+        for group in range(case.G):
+            pos = start.copy()
+            for ci, n in enumerate(chunks):
+                kv_bf16, kv = kv_for(case, seed * 1000 + layer * 100 + group * 10 + ci, n, anchor_is_base)
+                gpu.append(layer, group, kv_bf16, pos)
+                comp = oracle.append(obuf, geom, R, layer, group, kv, pos, chained=case.chained)
+                if layer == 0 and group == 0:
+                    for j in range(case.P - 1):
+                        us[j] = comp["u"][j] if us[j] is None else np.concatenate([us[j], comp["u"][j]], axis=-2)
+                pos = pos + n
+    st = gpu.status.cpu().numpy()
+    assert st[1] == 0, "append reported a capacity overflow"
+    return gpu, geom, obuf, R, us
+
+
+@pytest.mark.parametrize("d,g", [(128, 32), (128, 16), (96, 32)])
+def test_append_anchor_bitexact_and_residual_parity(d, g):
+    case = Case(L=1, P=4, G=1, H=3, d=d, g=g, B=2, Nmax=320, seed=1)
+    gpu, geom, obuf, R, us = _build_both(case, chunks=[200, 1, 37])
+    gbuf = gpu.bytes_host()
+    n = 238
+    for b in range(case.B):
+        for h in range(case.H):
+            gv = plane_views(gbuf, geom, 0, 0, b, h)
+            ov = plane_views(obuf, geom, 0, 0, b, h)
+            for nm in ("AK", "AV"):
+                assert np.array_equal(gv[nm], ov[nm]), f"anchor plane {nm} differs (b={b}, h={h})"
+    stats = check_residual_parity(gbuf, obuf, geom, us, 0, 0, n, case.B, case.H)
+    print("residual parity", stats)
+
+
+def test_append_ragged_starts():
+    """Rows start at different positions (unaligned), appended in uneven chunks."""
+    case = Case(L=1, P=4, G=1, H=2, d=128, g=32, B=3, Nmax=256, seed=2)
+    gpu, geom, obuf, R, us = _build_both(case, chunks=[5, 1, 60], seq_start=[0, 3, 130])
+    gbuf = gpu.bytes_host()
+    assert np.array_equal(gbuf[: geom.region_offset(0, 0, 0, 0)], obuf[: geom.region_offset(0, 0, 0, 0)])
+    for b in range(case.B):
+        for h in range(case.H):
+            gv, ov = plane_views(gbuf, geom, 0, 0, b, h), plane_views(obuf, geom, 0, 0, b, h)
+            assert np.array_equal(gv["AK"], ov["AK"]) and np.array_equal(gv["AV"], ov["AV"])
+
+
+def test_append_exact_rotation_is_bitexact():
+    """With R a signed permutation the float32 rotation is exact, so every byte of
+    every plane must match the oracle (residual codes included)."""
+    case = Case(L=1, P=4, G=1, H=2, d=128, g=32, B=2, Nmax=192, seed=3)
+    rng = np.random.default_rng(7)
+    perm = rng.permutation(128)
+    Rp = np.zeros((128, 128), dtype=np.float32)
+    Rp[np.arange(128), perm] = rng.choice([-1.0, 1.0], 128)
+    gpu = GpuCache(case, Rp)
+    geom = _geom(case)
+    obuf = np.zeros(geom.total_bytes, dtype=np.uint8)
+    kv_bf16, kv = kv_for(case, 11, 150)
+    # keep only vectors whose residual x - c*a_hat is exact in float32 on the oracle side
+    gpu.append(0, 0, kv_bf16, [0, 0])
+    comp = oracle.append(obuf, geom, Rp.astype(np.float64), 0, 0, kv, [0, 0])
+    gbuf = gpu.bytes_host()
+    a_hat = oracle.dequantize(*comp["anchor"], 32)
+    exact = np.ones((2, 2, 2, 150), bool)
+    for j in range(3):
+        cb = oracle.bf16_decode(comp["res"][j][3])[..., None]
+        e = kv[j] - cb * a_hat
+        exact &= np.all(e.astype(np.float32).astype(np.float64) == e, axis=-1)
+    assert exact.mean() > 0.9
+    for b in range(2):
+        for h in range(2):
+            for kvi in range(2):
+                for j in range(3):
+                    gc, gs, go, gcb = oracle.read_plane_tokens(gbuf, geom, 0, 0, b, h, kvi, "res", j, 150)
+                    oc, os_, oo, ocb = oracle.read_plane_tokens(obuf, geom, 0, 0, b, h, kvi, "res", j, 150)
+                    m = exact[kvi, b, h]
+                    assert np.array_equal(gc[m], oc[m]) and np.array_equal(gs[m], os_[m])
+                    assert np.array_equal(go[m], oo[m]) and np.array_equal(gcb, ocb)
+
+
+def _queries(case, seed, loop):
+    qb, q = synth.queries(seed * 7 + loop, case.B, case.H, case.d)
+    kvb, kv = synth.looped_kv(seed * 13 + 1, case.workload(), batch=case.B, ntok=1)
+    return qb, q, kvb[loop, 0, :, :, 0], kv[loop, 0, :, :, 0], kvb[loop, 1, :, :, 0], kv[loop, 1, :, :, 0]
+
+
+@pytest.mark.parametrize("d,g,H,B", [(128, 32, 2, 1), (128, 16, 3, 2), (96, 32, 5, 2)])
+def test_decode_attention_matches_oracle(d, g, H, B):
+    case = Case(L=2, P=4, G=1, H=H, d=d, g=g, B=B, Nmax=400, seed=4)
+    n = 333
+    gpu, geom, obuf, R, _ = _build_both(case, chunks=[n])
+    scale = 1.0 / math.sqrt(d)
+    seq = np.full(B, n)
+    worst = 0.0
+    for layer in range(2):
+        for loop in range(4):
+            qb, q, kcb, kc, vcb, vc = _queries(case, layer + 10, loop)
+            out = gpu.decode(layer, 0, loop, qb, kcb, vcb, seq, scale).cpu().numpy()
+            ref = oracle.decode_attention(obuf, geom, R, layer, 0, loop, q, kc, vc, seq, scale)
+            err = float(np.abs(out - ref).max())
+            worst = max(worst, err)
+            assert err <= ATOL, f"layer {layer} loop {loop}: max abs err {err:.3e}"
+    print("worst max-abs error", worst)
+    assert int(gpu.status.cpu()[0]) == 0
+
+
+def test_decode_on_oracle_bytes_isolates_the_kernel():
+    """Upload the oracle's cache bytes; the kernel must reproduce the oracle's attention
+    over those exact bytes."""
+    case = Case(L=1, P=4, G=1, H=4, d=128, g=32, B=2, Nmax=640, seed=5)
+    R32, R = rotation32(128)
+    geom = _geom(case)
+    obuf = np.zeros(geom.total_bytes, dtype=np.uint8)
+    kvb, kv = kv_for(case, 21, 600)
+    oracle.append(obuf, geom, R, 0, 0, kv, [0, 0])
+    gpu = GpuCache(case, R32)
+    gpu.buf.copy_(torch.from_numpy(obuf))
+    seq = np.array([600, 517])
+    worst = 0.0
+    for loop in range(4):
+        qb, q, kcb, kc, vcb, vc = _queries(case, 3, loop)
+        out = gpu.decode(0, 0, loop, qb, kcb, vcb, seq, 0.0883883476).cpu().numpy()
+        ref = oracle.decode_attention(obuf, geom, R, 0, 0, loop, q, kc, vc, seq, 0.0883883476)
+        worst = max(worst, float(np.abs(out - ref).max()))
+    assert worst <= 1e-4, worst
+
+
+@pytest.mark.parametrize("seq", [[0, 1, 63, 64], [65, 127, 128, 129], [1, 0, 0, 200]])
+def test_decode_ragged_and_empty(seq):
+    case = Case(L=1, P=4, G=1, H=2, d=128, g=32, B=4, Nmax=256, seed=6)
+    R32, R = rotation32(128)
+    geom = _geom(case)
+    obuf = np.zeros(geom.total_bytes, dtype=np.uint8)
+    kvb, kv = kv_for(case, 31, 200)
+    oracle.append(obuf, geom, R, 0, 0, kv, [0, 0, 0, 0])
+    gpu = GpuCache(case, R32)
+    gpu.buf.copy_(torch.from_numpy(obuf))
+    seq = np.array(seq)
+    for loop in (0, 3):
+        qb, q, kcb, kc, vcb, vc = _queries(case, 5, loop)
+        out = gpu.decode(0, 0, loop, qb, kcb, vcb, seq, 0.09).cpu().numpy()
+        ref = oracle.decode_attention(obuf, geom, R, 0, 0, loop, q, kc, vc, seq, 0.09)
+        assert np.abs(out - ref).max() <= 1e-4
+    # an empty row returns the current token's value exactly
+    for b in np.nonzero(seq == 0)[0]:
+        assert np.array_equal(out[b], vc[b].astype(np.float32))
+
+
+def test_decode_repeated_calls_reuse_workspace():
+    """Counters left at zero: the same call twice gives the same bits."""
+    case = Case(L=1, P=4, G=1, H=3, d=128, g=32, B=2, Nmax=2048, seed=7)
+    gpu, geom, obuf, R, _ = _build_both(case, chunks=[1500])
+    qb, q, kcb, kc, vcb, vc = _queries(case, 9, 1)
+    a = gpu.decode(0, 0, 1, qb, kcb, vcb, [1500, 1500], 0.08)
+    b = gpu.decode(0, 0, 1, qb, kcb, vcb, [1500, 1500], 0.08)
+    assert torch.equal(a, b)
+    ws = gpu.ws[256: 256 + 4 * case.B * case.H].view(torch.int32)
+    assert int(ws.abs().sum()) == 0
+
+
+def test_bf16_comparator_matches_softmax_attention():
+    import decode_attention_rq_gb300 as rq
+    rng = np.random.default_rng(8)
+    for d in (128, 96):
+        B, H, S = 3, 4, 300
+        seq = np.array([300, 1, 0])
+        k = torch.from_numpy(rng.standard_normal((B, H, S, d), dtype=np.float32)).to(torch.bfloat16)
+        v = torch.from_numpy(rng.standard_normal((B, H, S, d), dtype=np.float32)).to(torch.bfloat16)
+        q = torch.from_numpy(rng.standard_normal((B, H, d), dtype=np.float32)).to(torch.bfloat16)
+        kc = torch.from_numpy(rng.standard_normal((B, H, d), dtype=np.float32)).to(torch.bfloat16)
+        vc = torch.from_numpy(rng.standard_normal((B, H, d), dtype=np.float32)).to(torch.bfloat16)
+        dev = "cuda:0"
+        ws_bytes = rq.rq_bf16_workspace_bytes(B, H, d)
+        ws = torch.zeros(ws_bytes, dtype=torch.uint8, device=dev)
+        out = torch.empty((B, H, d), dtype=torch.float32, device=dev)
+        sl = torch.as_tensor(seq.astype(np.int32), device=dev)
+        scale = 1 / math.sqrt(d)
+        rq.rq_decode_attention_bf16(k.to(dev), v.to(dev), kc.to(dev), vc.to(dev), q.to(dev), sl, B, H, d, S,
+                                    scale, out, ws, ws_bytes)
+        o = out.cpu().numpy()
+        K, V, Q = k.double().numpy(), v.double().numpy(), q.double().numpy()
+        KC, VC = kc.double().numpy(), vc.double().numpy()
+        for b in range(B):
+            for h in range(H):
+                n = seq[b]
+                ref = oracle.attention(Q[b, h], np.concatenate([K[b, h, :n], KC[b, h][None]]),
+                                       np.concatenate([V[b, h, :n], VC[b, h][None]]), scale)
+                assert np.abs(o[b, h] - ref).max() <= 1e-4
