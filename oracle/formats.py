@@ -23,7 +23,7 @@ from __future__ import annotations
 import numpy as np
 
 __all__ = ["E4M3_MAX", "e4m3_encode", "e4m3_decode", "e4m3_round",
-           "bf16_encode", "bf16_decode", "bf16_round", "e4m3_all_finite"]
+           "bf16_encode", "bf16_decode", "bf16_round", "e4m3_all_finite", "fma_f32"]
 
 E4M3_MAX = 448.0
 _E4M3_MIN_NORMAL_EXP = -6   # smallest normal 2^-6
@@ -119,3 +119,29 @@ def bf16_encode(x) -> np.ndarray:
 def bf16_decode(bits) -> np.ndarray:
     b = np.asarray(bits, dtype=np.uint16).astype(np.uint32) << 16
     return b.view(np.float32).astype(np.float64)
+
+
+def _round_to_odd_sum(a: np.ndarray, b: np.ndarray) -> np.ndarray:
+    """a + b rounded to float64 with round-to-odd: the exact sum if representable,
+    else whichever neighbouring float64 has an odd significand (TwoSum gives the
+    exact rounding error of the nearest-even sum)."""
+    s = a + b
+    bb = s - a
+    err = (a - (s - bb)) + (b - bb)
+    odd = (s.view(np.uint64) & np.uint64(1)).astype(bool)
+    toward = np.where(err > 0, np.inf, -np.inf)
+    return np.where((err == 0) | odd, s, np.nextafter(s, toward))
+
+
+def fma_f32(a, b, c) -> np.ndarray:
+    """IEEE binary32 fused multiply-add round(a*b + c), nearest-even, one rounding.
+
+    a, b, c must hold binary32 values (any float dtype).  a*b is exact in
+    float64 (24 + 24 bits); adding c with round-to-odd keeps a sticky bit, so
+    the final cast to float32 rounds exactly once (float64 carries more than
+    two bits beyond binary32's 24)."""
+    a = np.asarray(a, dtype=np.float64)
+    b = np.asarray(b, dtype=np.float64)
+    c = np.asarray(c, dtype=np.float64)
+    p = a * b
+    return _round_to_odd_sum(p, np.broadcast_to(c, p.shape).astype(np.float64)).astype(np.float32)

@@ -31,15 +31,24 @@ Readings of what the pages leave open (each one listed in the design doc):
   * R is applied as u = R (x - c_b * ref); reconstruction uses R^T.
   * chained variant: loop l is coded against the reconstruction of loop
     l+1, the last loop being the anchor.
+  * precision of the residual and its rotation: the pages do not fix it.  The
+    codes are decided by u, so the oracle takes u in the precision the device
+    computes it: IEEE binary32, e = fma(-c_b, ref, x) rounded once, and each
+    u_i = sum_k R[i,k] e_k as a chain of binary32 fused multiply-adds in
+    channel order k = 0..d-1 (the plain definition of the sum).  In chained
+    mode the encoder's reference for loop l-1 is rebuilt the same way
+    (acc_i = sum_k R[k,i] r_hat_k in order, then fma(c_b, ref, acc)).
+    precision="f64" keeps the float64 reading of the same formulas, used to
+    bound the binary32 one.
 """
 from __future__ import annotations
 
 import numpy as np
 
-from .formats import e4m3_round, e4m3_encode, e4m3_decode, bf16_round, bf16_encode, bf16_decode
+from .formats import e4m3_round, e4m3_encode, e4m3_decode, bf16_round, bf16_encode, bf16_decode, fma_f32
 
 __all__ = ["quantize", "dequantize", "ls_coefficient", "compress_group", "attention",
-           "ANCHOR_BITS", "RESIDUAL_BITS"]
+           "rotate_f32", "rotate_back_f32", "ANCHOR_BITS", "RESIDUAL_BITS"]
 
 ANCHOR_BITS = 4     # [EXPL] worked example; [SUMM] overview (INT4 anchor)
 RESIDUAL_BITS = 2   # [EXPL] worked example; [SUMM] overview (INT2 residuals)
@@ -101,35 +110,72 @@ def ls_coefficient(x: np.ndarray, y: np.ndarray) -> np.ndarray:
     return np.where(den > 0, num / np.where(den > 0, den, 1.0), 0.0)
 
 
-def compress_group(x: np.ndarray, R: np.ndarray, g: int, chained: bool = False):
+def rotate_f32(R: np.ndarray, e: np.ndarray) -> np.ndarray:
+    """u = R e per vector in binary32: u_i accumulates fma(R[i,k], e_k, u_i) for
+    k = 0..d-1.  R [d, d] and e [..., d] hold binary32 values; returns float32."""
+    R = np.asarray(R, dtype=np.float32)
+    e = np.asarray(e, dtype=np.float32)
+    u = np.zeros(e.shape, dtype=np.float32)
+    for k in range(e.shape[-1]):
+        u = fma_f32(R[:, k], e[..., k:k + 1], u)
+    return u
+
+
+def rotate_back_f32(R: np.ndarray, r: np.ndarray) -> np.ndarray:
+    """acc = R^T r per vector in binary32: acc_i accumulates fma(R[k,i], r_k, acc_i)
+    for k = 0..d-1; returns float32."""
+    R = np.asarray(R, dtype=np.float32)
+    r = np.asarray(r, dtype=np.float32)
+    acc = np.zeros(r.shape, dtype=np.float32)
+    for k in range(r.shape[-1]):
+        acc = fma_f32(R[k, :], r[..., k:k + 1], acc)
+    return acc
+
+
+def compress_group(x: np.ndarray, R: np.ndarray, g: int, chained: bool = False, precision: str = "f32"):
     """Compress the P loops of one loop group.
 
     x: float64 [P, ..., d], loop index first, the last loop is the anchor
        ([EXPL]: the final loop's KV is the INT4 master; [SUMM]: last-loop anchor).
-    R: float64 [d, d], the fixed rotation (as the device receives it).
+    R: [d, d], the fixed rotation as the device receives it (binary32 values).
+    precision: "f32" (the residual and rotation as the device computes them,
+       see the module docstring) or "f64".
     Returns a dict with
       anchor: (codes, scale_b, offset_b)
       res[j] for j in 0..P-2: (codes, scale_b, offset_b, c_bf16_bits)
-      u[j]: float64 rotated residual before quantization
-      recon: float64 [P, ..., d], the decoder's view of every loop
+      u[j]: the rotated residual before quantization (float64 array)
+      recon: float64 [P, ..., d], the decoder's view of every loop, computed
+             in float64 from the stored values (c_b * ref_hat + R^T r_hat)
     """
     x = np.asarray(x, dtype=np.float64)
+    R = np.asarray(R, dtype=np.float64)
     P = x.shape[0]
     a_codes, a_s, a_o = quantize(x[P - 1], ANCHOR_BITS, g)
     a_hat = dequantize(a_codes, a_s, a_o, g)
     recon = np.empty_like(x)
     recon[P - 1] = a_hat
     res, us = [None] * (P - 1), [None] * (P - 1)
+    enc_ref = a_hat                                   # the encoder's reference (chained: rebuilt loop)
     for j in range(P - 2, -1, -1):
-        ref = recon[j + 1] if chained else a_hat
+        ref = enc_ref if chained else a_hat
         c = ls_coefficient(x[j], ref)
         c_bits = bf16_encode(c)
         cb = bf16_decode(c_bits)[..., None]
-        e = x[j] - cb * ref                      # residual against the scaled reference
-        u = e @ R.T                              # u = R e for each vector
+        if precision == "f32":
+            e = fma_f32(-cb, ref, x[j])               # residual, one binary32 rounding
+            u = rotate_f32(R, e).astype(np.float64)
+        else:
+            e = x[j] - cb * ref
+            u = e @ R.T
         r_codes, r_s, r_o = quantize(u, RESIDUAL_BITS, g)
         r_hat = dequantize(r_codes, r_s, r_o, g)
-        recon[j] = cb * ref + r_hat @ R          # R^T r_hat for each vector
+        dec_ref = recon[j + 1] if chained else a_hat
+        recon[j] = cb * dec_ref + r_hat @ R           # R^T r_hat for each vector, float64
+        if chained:
+            if precision == "f32":
+                enc_ref = fma_f32(cb, enc_ref, rotate_back_f32(R, r_hat)).astype(np.float64)
+            else:
+                enc_ref = recon[j]
         res[j] = (r_codes, r_s, r_o, c_bits)
         us[j] = u
     return {"anchor": (a_codes, a_s, a_o), "res": res, "u": us, "recon": recon}

@@ -121,6 +121,8 @@ def test_append_anchor_bitexact_and_residual_parity(d, g):
                 assert np.array_equal(gv[nm], ov[nm]), f"anchor plane {nm} differs (b={b}, h={h})"
     stats = check_residual_parity(gbuf, obuf, geom, us, 0, 0, n, case.B, case.H)
     print("residual parity", stats)
+    # the oracle takes the residual in the device's precision: every byte must match
+    assert np.array_equal(gbuf, obuf), f"{int((gbuf != obuf).sum())} cache bytes differ"
 
 
 def test_append_ragged_starts():
@@ -136,8 +138,8 @@ def test_append_ragged_starts():
 
 
 def test_append_exact_rotation_is_bitexact():
-    """With R a signed permutation the float32 rotation is exact, so every byte of
-    every plane must match the oracle (residual codes included)."""
+    """With R a signed permutation the rotation is exact in any precision, so
+    every byte of every plane matches the float64 reading of the oracle too."""
     case = Case(L=1, P=4, G=1, H=2, d=128, g=32, B=2, Nmax=192, seed=3)
     rng = np.random.default_rng(7)
     perm = rng.permutation(128)
@@ -149,7 +151,7 @@ def test_append_exact_rotation_is_bitexact():
     kv_bf16, kv = kv_for(case, 11, 150)
     # keep only vectors whose residual x - c*a_hat is exact in float32 on the oracle side
     gpu.append(0, 0, kv_bf16, [0, 0])
-    comp = oracle.append(obuf, geom, Rp.astype(np.float64), 0, 0, kv, [0, 0])
+    comp = oracle.append(obuf, geom, Rp.astype(np.float64), 0, 0, kv, [0, 0], precision="f64")
     gbuf = gpu.bytes_host()
     a_hat = oracle.dequantize(*comp["anchor"], 32)
     exact = np.ones((2, 2, 2, 150), bool)
@@ -175,14 +177,19 @@ def _queries(case, seed, loop):
     return qb, q, kvb[loop, 0, :, :, 0], kv[loop, 0, :, :, 0], kvb[loop, 1, :, :, 0], kv[loop, 1, :, :, 0]
 
 
-@pytest.mark.parametrize("d,g,H,B", [(128, 32, 2, 1), (128, 16, 3, 2), (96, 32, 5, 2)])
+@pytest.mark.parametrize("d,g,H,B", [(128, 32, 2, 1), (128, 16, 3, 2), (96, 32, 5, 2), (96, 16, 2, 1)])
 def test_decode_attention_matches_oracle(d, g, H, B):
+    """End to end: GPU-built cache + GPU attention against oracle cache + oracle
+    attention; and the GPU kernel on the oracle's bytes (isolates the kernel)."""
     case = Case(L=2, P=4, G=1, H=H, d=d, g=g, B=B, Nmax=400, seed=4)
     n = 333
     gpu, geom, obuf, R, _ = _build_both(case, chunks=[n])
+    gbuf = gpu.bytes_host()
     scale = 1.0 / math.sqrt(d)
     seq = np.full(B, n)
-    worst = 0.0
+    worst, worst_iso = 0.0, 0.0
+    iso = GpuCache(case, rotation32(d)[0])
+    iso.buf.copy_(torch.from_numpy(obuf))
     for layer in range(2):
         for loop in range(4):
             qb, q, kcb, kc, vcb, vc = _queries(case, layer + 10, loop)
@@ -190,8 +197,14 @@ def test_decode_attention_matches_oracle(d, g, H, B):
             ref = oracle.decode_attention(obuf, geom, R, layer, 0, loop, q, kc, vc, seq, scale)
             err = float(np.abs(out - ref).max())
             worst = max(worst, err)
+            out_iso = iso.decode(layer, 0, loop, qb, kcb, vcb, seq, scale).cpu().numpy()
+            worst_iso = max(worst_iso, float(np.abs(out_iso - ref).max()))
             assert err <= ATOL, f"layer {layer} loop {loop}: max abs err {err:.3e}"
-    print("worst max-abs error", worst)
+    diff_bytes = int((gbuf != obuf).sum())
+    print(f"worst max-abs error {worst:.3e} (kernel on oracle bytes {worst_iso:.3e}); "
+          f"cache bytes differing {diff_bytes} of {obuf.size}")
+    assert diff_bytes == 0
+    assert worst_iso <= 1e-4
     assert int(gpu.status.cpu()[0]) == 0
 
 

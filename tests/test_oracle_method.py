@@ -170,7 +170,7 @@ def test_reconstruction_error_is_the_residual_quantization_error(chained):
     w = synth.WORKLOADS["toy"]
     _, kv = synth.looped_kv(0, w, batch=1, ntok=64)
     R = synth.rotation(128)
-    comp = M.compress_group(kv, R, 32, chained=chained)
+    comp = M.compress_group(kv, R, 32, chained=chained, precision="f64")
     for j in range(3):
         r_codes, r_s, r_o, _ = comp["res"][j]
         r_hat = M.dequantize(r_codes, r_s, r_o, 32)
@@ -191,7 +191,7 @@ def test_residual_uses_bf16_coefficient_and_dequantized_anchor():
     w = synth.WORKLOADS["toy"]
     _, kv = synth.looped_kv(1, w, batch=1, ntok=8)
     R = synth.rotation(128)
-    comp = M.compress_group(kv, R, 32)
+    comp = M.compress_group(kv, R, 32, precision="f64")
     a_hat = M.dequantize(*comp["anchor"], 32)
     for j in range(3):
         c = M.ls_coefficient(kv[j], a_hat)
@@ -218,3 +218,71 @@ def test_attention_special_cases():
     s = 0.125 * K @ q
     lse = scipy.special.logsumexp(s)
     assert np.allclose(M.attention(q, K, V, 0.125), np.exp(s - lse) @ V, rtol=1e-12, atol=1e-13)
+
+
+def test_fma_f32_is_one_rounding_of_the_exact_value():
+    """Against exact rationals (Fraction) and a binary32 round-to-nearest-even
+    written from the format (24-bit significand)."""
+    from fractions import Fraction
+
+    def rne32(fr):
+        if fr == 0:
+            return 0.0
+        sgn, fr = (-1 if fr < 0 else 1), abs(fr)
+        e = fr.numerator.bit_length() - fr.denominator.bit_length()
+        while Fraction(2) ** e > fr:
+            e -= 1
+        while Fraction(2) ** (e + 1) <= fr:
+            e += 1
+        q = Fraction(2) ** (e - 23)
+        k = fr / q
+        fl = k.numerator // k.denominator
+        rem = k - fl
+        if rem > Fraction(1, 2) or (rem == Fraction(1, 2) and fl % 2 == 1):
+            fl += 1
+        return sgn * float(fl * q)
+
+    rng = np.random.default_rng(21)
+    for i in range(6000):
+        a, b, c = rng.standard_normal(3).astype(np.float32)
+        if i % 3 == 0:
+            c = np.float32(-(np.float64(a) * np.float64(b)))     # near-total cancellation
+        if i % 7 == 0:
+            c = np.float32(c * 1e-8)
+        want = rne32(Fraction(float(a)) * Fraction(float(b)) + Fraction(float(c)))
+        assert float(F.fma_f32(a, b, c)) == want
+
+
+def test_f32_rotation_special_cases_and_error_bound():
+    rng = np.random.default_rng(22)
+    e = rng.standard_normal((50, 128)).astype(np.float32)
+    # identity and signed permutation: exact
+    assert np.array_equal(M.rotate_f32(np.eye(128, dtype=np.float32), e), e)
+    perm = rng.permutation(128)
+    Pm = np.zeros((128, 128), np.float32)
+    Pm[np.arange(128), perm] = rng.choice([-1.0, 1.0], 128).astype(np.float32)
+    assert np.array_equal(M.rotate_f32(Pm, e), e @ Pm.T)
+    assert np.array_equal(M.rotate_back_f32(Pm, e), e @ Pm)
+    # general R: within the textbook bound of a binary32 recursive sum, d * 2^-24 * sum|R_ik e_k|
+    R = synth.rotation(128).astype(np.float32)
+    u32 = M.rotate_f32(R, e).astype(np.float64)
+    u64 = e.astype(np.float64) @ R.astype(np.float64).T
+    bound = 128 * 2.0 ** -24 * (np.abs(e.astype(np.float64)) @ np.abs(R.astype(np.float64)).T)
+    assert np.all(np.abs(u32 - u64) <= bound)
+    assert np.abs(u32 - u64).max() > 0      # it is a genuinely different rounding
+
+
+@pytest.mark.parametrize("chained", [False, True])
+def test_f32_and_f64_readings_agree_up_to_rounding(chained):
+    """The binary32 reading of the residual changes codes only where the float64
+    reading sits on a rounding boundary."""
+    w = synth.WORKLOADS["toy"]
+    _, kv = synth.looped_kv(3, w, batch=1, ntok=64)
+    R = synth.rotation(128).astype(np.float32).astype(np.float64)
+    c32 = M.compress_group(kv, R, 32, chained=chained, precision="f32")
+    c64 = M.compress_group(kv, R, 32, chained=chained, precision="f64")
+    assert np.array_equal(c32["anchor"][0], c64["anchor"][0])
+    for j in range(3):
+        assert np.allclose(c32["u"][j], c64["u"][j], rtol=0, atol=1e-4)
+        diff = (c32["res"][j][0] != c64["res"][j][0]).mean()
+        assert diff < 1e-3
