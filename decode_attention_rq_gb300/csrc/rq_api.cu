@@ -119,6 +119,7 @@ rq_status rq_decode_attention(rq_cache* cache, int32_t layer, int32_t group, int
       batch <= 0)
     return RQ_ERR_INVALID_ARG;
   if (batch > g.Bmax) return RQ_ERR_CAPACITY;
+  if (g.mode == RQ_MODE_CHAINED && g.P > decode_max_chained_loops()) return RQ_ERR_UNSUPPORTED;
   if (workspace_bytes < decode_workspace_bytes(g, batch, cache->num_sms)) return RQ_ERR_WORKSPACE;
   if (!aligned16(q) || !aligned16(k_cur) || !aligned16(v_cur) || !aligned16(seq_lens) ||
       !aligned16(out) || !aligned16(workspace))

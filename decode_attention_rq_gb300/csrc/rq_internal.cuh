@@ -55,6 +55,7 @@ cudaError_t launch_append(const rq_cache& c, int layer, int group, int batch,
                           int32_t* status, cudaStream_t stream);
 
 size_t decode_workspace_bytes(const Geom& g, int batch, int num_sms);
+int decode_max_chained_loops();   // chained-mode decode reads at most this many loops' planes
 cudaError_t launch_decode(const rq_cache& c, int layer, int group, int loop, int batch,
                           const __nv_bfloat16* q, const __nv_bfloat16* k_cur,
                           const __nv_bfloat16* v_cur, const int32_t* seq_lens, float scale,

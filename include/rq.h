@@ -150,7 +150,10 @@ size_t rq_decode_workspace_bytes(const rq_config* cfg, int32_t batch);
  * Split-K over the sequence: each CTA of a balanced grid streams its range of
  * tiles; the last CTA to finish a (row, head) merges the partial softmax
  * states, adds the current token and applies R^T once.
- * Errors: INVALID_ARG, CAPACITY (batch > max_batch), WORKSPACE, ALIGNMENT, CUDA. */
+ * Chained mode reads the anchor and every residual plane from this loop to
+ * the anchor; decode supports it for loops_per_group <= 4 (UNSUPPORTED beyond).
+ * Errors: INVALID_ARG, CAPACITY (batch > max_batch), WORKSPACE, ALIGNMENT,
+ * UNSUPPORTED, CUDA. */
 rq_status rq_decode_attention(rq_cache* cache, int32_t layer, int32_t group, int32_t loop,
                               int32_t batch, const void* q, const void* k_cur, const void* v_cur,
                               const int32_t* seq_lens, float softmax_scale, float* out,

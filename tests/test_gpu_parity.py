@@ -177,11 +177,13 @@ def _queries(case, seed, loop):
     return qb, q, kvb[loop, 0, :, :, 0], kv[loop, 0, :, :, 0], kvb[loop, 1, :, :, 0], kv[loop, 1, :, :, 0]
 
 
-@pytest.mark.parametrize("d,g,H,B", [(128, 32, 2, 1), (128, 16, 3, 2), (96, 32, 5, 2), (96, 16, 2, 1)])
-def test_decode_attention_matches_oracle(d, g, H, B):
+@pytest.mark.parametrize("d,g,H,B,chained", [(128, 32, 2, 1, False), (128, 16, 3, 2, False),
+                                             (96, 32, 5, 2, False), (96, 16, 2, 1, False),
+                                             (128, 32, 2, 2, True), (96, 16, 3, 1, True)])
+def test_decode_attention_matches_oracle(d, g, H, B, chained):
     """End to end: GPU-built cache + GPU attention against oracle cache + oracle
     attention; and the GPU kernel on the oracle's bytes (isolates the kernel)."""
-    case = Case(L=2, P=4, G=1, H=H, d=d, g=g, B=B, Nmax=400, seed=4)
+    case = Case(L=2, P=4, G=1, H=H, d=d, g=g, B=B, Nmax=400, seed=4, chained=chained)
     n = 333
     gpu, geom, obuf, R, _ = _build_both(case, chunks=[n])
     gbuf = gpu.bytes_host()
@@ -194,7 +196,8 @@ def test_decode_attention_matches_oracle(d, g, H, B):
         for loop in range(4):
             qb, q, kcb, kc, vcb, vc = _queries(case, layer + 10, loop)
             out = gpu.decode(layer, 0, loop, qb, kcb, vcb, seq, scale).cpu().numpy()
-            ref = oracle.decode_attention(obuf, geom, R, layer, 0, loop, q, kc, vc, seq, scale)
+            ref = oracle.decode_attention(obuf, geom, R, layer, 0, loop, q, kc, vc, seq, scale,
+                                          chained=chained)
             err = float(np.abs(out - ref).max())
             worst = max(worst, err)
             out_iso = iso.decode(layer, 0, loop, qb, kcb, vcb, seq, scale).cpu().numpy()
@@ -204,7 +207,7 @@ def test_decode_attention_matches_oracle(d, g, H, B):
     print(f"worst max-abs error {worst:.3e} (kernel on oracle bytes {worst_iso:.3e}); "
           f"cache bytes differing {diff_bytes} of {obuf.size}")
     assert diff_bytes == 0
-    assert worst_iso <= 1e-4
+    assert worst_iso <= 1e-3   # 16-bit fixed-point query and value weights
     assert int(gpu.status.cpu()[0]) == 0
 
 
@@ -226,7 +229,7 @@ def test_decode_on_oracle_bytes_isolates_the_kernel():
         out = gpu.decode(0, 0, loop, qb, kcb, vcb, seq, 0.0883883476).cpu().numpy()
         ref = oracle.decode_attention(obuf, geom, R, 0, 0, loop, q, kc, vc, seq, 0.0883883476)
         worst = max(worst, float(np.abs(out - ref).max()))
-    assert worst <= 1e-4, worst
+    assert worst <= 1e-3, worst   # 16-bit fixed-point query and value weights
 
 
 @pytest.mark.parametrize("seq", [[0, 1, 63, 64], [65, 127, 128, 129], [1, 0, 0, 200]])
@@ -244,7 +247,7 @@ def test_decode_ragged_and_empty(seq):
         qb, q, kcb, kc, vcb, vc = _queries(case, 5, loop)
         out = gpu.decode(0, 0, loop, qb, kcb, vcb, seq, 0.09).cpu().numpy()
         ref = oracle.decode_attention(obuf, geom, R, 0, 0, loop, q, kc, vc, seq, 0.09)
-        assert np.abs(out - ref).max() <= 1e-4
+        assert np.abs(out - ref).max() <= 1e-3
     # an empty row returns the current token's value exactly
     for b in np.nonzero(seq == 0)[0]:
         assert np.array_equal(out[b], vc[b].astype(np.float32))
@@ -290,3 +293,26 @@ def test_bf16_comparator_matches_softmax_attention():
                 ref = oracle.attention(Q[b, h], np.concatenate([K[b, h, :n], KC[b, h][None]]),
                                        np.concatenate([V[b, h, :n], VC[b, h][None]]), scale)
                 assert np.abs(o[b, h] - ref).max() <= 1e-4
+
+
+def test_chained_append_bitexact():
+    """Chained mode: each loop coded against the rebuilt next loop; every byte matches."""
+    case = Case(L=1, P=4, G=1, H=2, d=128, g=32, B=2, Nmax=256, seed=9, chained=True)
+    gpu, geom, obuf, R, us = _build_both(case, chunks=[130, 3])
+    gbuf = gpu.bytes_host()
+    assert np.array_equal(gbuf, obuf), f"{int((gbuf != obuf).sum())} cache bytes differ"
+
+
+def test_huginn_groups_and_layers():
+    """Several loop groups and layers: regions do not overlap, each group decodes right."""
+    case = Case(L=2, P=4, G=3, H=3, d=96, g=32, B=2, Nmax=192, seed=10)
+    gpu, geom, obuf, R, _ = _build_both(case, chunks=[150], anchor_is_base=False)
+    gbuf = gpu.bytes_host()
+    assert np.array_equal(gbuf, obuf)
+    seq = np.array([150, 97])
+    for layer, group in [(0, 0), (1, 2), (0, 1)]:
+        for loop in (0, 3):
+            qb, q, kcb, kc, vcb, vc = _queries(case, layer * 3 + group, loop)
+            out = gpu.decode(layer, group, loop, qb, kcb, vcb, seq, 1 / math.sqrt(96)).cpu().numpy()
+            ref = oracle.decode_attention(obuf, geom, R, layer, group, loop, q, kc, vc, seq, 1 / math.sqrt(96))
+            assert np.abs(out - ref).max() <= ATOL
