@@ -174,6 +174,30 @@ __device__ void write_plane(const AppendArgs& a, uint8_t* plane, int64_t tile_by
   }
 }
 
+// u[t][i] = sum_k R[i][k] e[t][k] for the first NT token slots; thread = output
+// channel i; the sum runs k = 0..d-1 as a chain of float32 fused multiply-adds.
+template <int NT>
+__device__ __forceinline__ void rotate_rows(const float* R, int d, int i, const float (*e)[128],
+                                            float (*u)[128]) {
+  float acc[NT];
+#pragma unroll
+  for (int t = 0; t < NT; ++t) acc[t] = 0.f;
+  const float4* Rrow = reinterpret_cast<const float4*>(R + (size_t)i * d);
+  for (int k4 = 0; k4 < d / 4; ++k4) {
+    float4 r = __ldg(Rrow + k4);
+#pragma unroll
+    for (int t = 0; t < NT; ++t) {
+      float4 x = *reinterpret_cast<const float4*>(&e[t][4 * k4]);
+      acc[t] = fmaf(r.x, x.x, acc[t]);
+      acc[t] = fmaf(r.y, x.y, acc[t]);
+      acc[t] = fmaf(r.z, x.z, acc[t]);
+      acc[t] = fmaf(r.w, x.w, acc[t]);
+    }
+  }
+#pragma unroll
+  for (int t = 0; t < NT; ++t) u[t][i] = acc[t];
+}
+
 __global__ void __launch_bounds__(kThreads) append_kernel(AppendArgs a) {
   const int d = a.g.d, gs = a.g.g, P = a.g.P, tid = threadIdx.x;
   const int b = blockIdx.y / a.g.H, h = blockIdx.y % a.g.H, kvi = blockIdx.z;
@@ -201,14 +225,22 @@ __global__ void __launch_bounds__(kThreads) append_kernel(AppendArgs a) {
     int pos = p0 + tid;
     valid_s[tid] = pos >= start && pos < start + a.n;
   }
+  for (int i = tid; i < kTok * 128; i += kThreads) {   // defined values in unused slots
+    (&ref_s[0][0])[i] = 0.f;
+    cb_s[i % kTok] = 0.f;
+  }
   __syncthreads();
 
   uint8_t* region = a.base + a.g.region_offset(a.layer, a.group, b, h);
+  // every valid slot in the first quad: rotate 4 slots instead of 16
+  bool few = true;
+  for (int t = 4; t < kTok; ++t) few = few && !valid_s[t];
   const bool act = tid < d;
 
-  // ---- anchor: loop P-1, 4-bit ----
+  // ---- anchor: loop P-1, 4-bit (slots outside the appended range are skipped) ----
   for (int t = 0; t < kTok; ++t) {
-    float v = (act && valid_s[t]) ? load_x(a, P - 1, kvi, b, h, p0 + t - start, tid) : 0.f;
+    if (!valid_s[t]) continue;   // same for every thread of the CTA
+    float v = act ? load_x(a, P - 1, kvi, b, h, p0 + t - start, tid) : 0.f;
     uint8_t sb, ob;
     float vh;
     int code = quantize_lane(v, act, gs, 15, &sb, &ob, &vh);
@@ -234,6 +266,7 @@ __global__ void __launch_bounds__(kThreads) append_kernel(AppendArgs a) {
     {
       const int warp = tid / 32, lane = tid % 32;
       for (int t = warp; t < kTok; t += kThreads / 32) {
+        if (!valid_s[t]) continue;   // same for every lane of the warp
         double num = 0.0, den = 0.0;
         for (int k = lane; k < d; k += 32) {
           double y = ref_s[t][k], x = x_s[t][k];
@@ -259,28 +292,14 @@ __global__ void __launch_bounds__(kThreads) append_kernel(AppendArgs a) {
     __syncthreads();
     // rotation u = R e, thread = output channel, sequential FMA over k
     if (act) {
-      float acc[kTok];
-#pragma unroll
-      for (int t = 0; t < kTok; ++t) acc[t] = 0.f;
-      const float4* Rrow = reinterpret_cast<const float4*>(a.R + (size_t)tid * d);
-      for (int k4 = 0; k4 < d / 4; ++k4) {
-        float4 r = __ldg(Rrow + k4);
-#pragma unroll
-        for (int t = 0; t < kTok; ++t) {
-          float4 e = *reinterpret_cast<const float4*>(&x_s[t][4 * k4]);
-          acc[t] = fmaf(r.x, e.x, acc[t]);
-          acc[t] = fmaf(r.y, e.y, acc[t]);
-          acc[t] = fmaf(r.z, e.z, acc[t]);
-          acc[t] = fmaf(r.w, e.w, acc[t]);
-        }
-      }
-#pragma unroll
-      for (int t = 0; t < kTok; ++t) u_s[t][tid] = acc[t];
+      if (few) rotate_rows<4>(a.R, d, tid, x_s, u_s);
+      else rotate_rows<kTok>(a.R, d, tid, x_s, u_s);
     }
     __syncthreads();
     // 2-bit quantization of u
     for (int t = 0; t < kTok; ++t) {
-      float v = (act && valid_s[t]) ? u_s[t][tid] : 0.f;
+      if (!valid_s[t]) continue;
+      float v = act ? u_s[t][tid] : 0.f;
       uint8_t sb, ob;
       float vh;
       int code = quantize_lane(v, act, gs, 3, &sb, &ob, &vh);

@@ -28,15 +28,16 @@ struct Bf16Args {
   float qscale;
 };
 
-__device__ __forceinline__ int cta_of(long long u, long long U, int C) {
-  return (int)(((u + 1) * C - 1) / U);
-}
-// CTA c's range [floor(cU/C), floor((c+1)U/C)) intersects [s0, s1) (ranges may be
-// empty when there are fewer units than CTAs; such CTAs contribute nothing)
-__device__ __forceinline__ bool contributes(int c, long long s0, long long s1, long long U, int C) {
-  long long r0 = (long long)c * U / C, r1 = (long long)(c + 1) * U / C;
-  return (r0 > s0 ? r0 : s0) < (r1 < s1 ? r1 : s1);
-}
+// Balanced split of U units over C CTAs: CTA c takes [start(c), start(c+1)) with
+// start(c) = c*q + min(c, rem), q = U / C, rem = U % C (32-bit arithmetic only).
+struct Split {
+  int q, rem;
+  __device__ __forceinline__ int start(int c) const { return c * q + min(c, rem); }
+  __device__ __forceinline__ int owner(int u) const {
+    const int big = (q + 1) * rem;
+    return u < big ? u / (q + 1) : rem + (u - big) / q;
+  }
+};
 
 __device__ __forceinline__ float2 bf2_to_f2(uint32_t x) {
   return make_float2(__uint_as_float(x << 16), __uint_as_float(x & 0xFFFF0000u));
@@ -76,17 +77,18 @@ __global__ void __launch_bounds__(kThreads, kCtasPerSm) bf16_kernel(Bf16Args a) 
     pre_s[B] = acc;
   }
   __syncthreads();
-  const long long U = pre_s[B];
+  const int U = pre_s[B];
   for (int bh = cta; bh < B * H; bh += Cn) {
     if (nt_s[bh / H] != 0) continue;
     for (int k = tid; k < D; k += kThreads)
       a.out[(size_t)bh * D + k] = __bfloat162float(a.v_cur[(size_t)bh * D + k]);
   }
   if (U == 0) return;
-  const long long u0 = (long long)cta * U / Cn, u1 = (long long)(cta + 1) * U / Cn;
+  const Split split{U / Cn, U % Cn};
+  const int u0 = split.start(cta), u1 = split.start(cta + 1);
   if (u0 >= u1) return;
 
-  auto locate = [&](long long u, int* bh, int* tile) {
+  auto locate = [&](int u, int* bh, int* tile) {
     int lo = 0, hi = B - 1;
     while (lo < hi) {
       int mid = (lo + hi + 1) >> 1;
@@ -99,7 +101,7 @@ __global__ void __launch_bounds__(kThreads, kCtasPerSm) bf16_kernel(Bf16Args a) 
   auto rows_of = [&](int bh, int tile) {
     return min(kTile, min(a.max_seq, a.seq_lens[bh / H]) - tile * kTile);
   };
-  auto issue = [&](long long u, int stage) {
+  auto issue = [&](int u, int stage) {
     int bh, tile;
     locate(u, &bh, &tile);
     // copy only the rows that exist in the caller's buffer (and are valid)
@@ -123,7 +125,7 @@ __global__ void __launch_bounds__(kThreads, kCtasPerSm) bf16_kernel(Bf16Args a) 
   float acc0 = 0.f, acc1 = 0.f;
   int cur_bh = -1;
   bool aborted = false;
-  long long fail_u = 0;
+  int fail_u = 0;
   const int tok1 = tid % kTile, part1 = tid / kTile;      // phase 1: (token, quarter row)
   const int ch2 = tid % (D / 2), qt2 = tid / (D / 2);     // phase 2: (channel pair, token quarter)
   const bool p2_active = tid < NPAIR2;
@@ -137,13 +139,9 @@ __global__ void __launch_bounds__(kThreads, kCtasPerSm) bf16_kernel(Bf16Args a) 
     __threadfence();
     __syncthreads();
     const int b = bh / H, h = bh % H;
-    const long long s0 = pre_s[b] + (long long)h * nt_s[b], s1 = s0 + nt_s[b];
-    const int c_lo = cta_of(s0, U, Cn), c_hi = cta_of(s1 - 1, U, Cn);
-    if (tid == 0) {
-      int needed = 0;
-      for (int c = c_lo; c <= c_hi; ++c) needed += contributes(c, s0, s1, U, Cn);
-      flag_s = (atomicAdd(&a.counters[bh], 1) == needed - 1);
-    }
+    const int s0 = pre_s[b] + h * nt_s[b], s1 = s0 + nt_s[b];
+    const int c_lo = split.owner(s0), c_hi = split.owner(s1 - 1);
+    if (tid == 0) flag_s = (atomicAdd(&a.counters[bh], 1) == c_hi - c_lo);
     __syncthreads();
     if (!flag_s) return;
     __threadfence();
@@ -156,11 +154,9 @@ __global__ void __launch_bounds__(kThreads, kCtasPerSm) bf16_kernel(Bf16Args a) 
       float s_cur = 0.f;
       for (int w = 0; w < kThreads / 32; ++w) s_cur += red_s[w];
       float M = s_cur;
-      for (int c = c_lo; c <= c_hi; ++c)
-        if (contributes(c, s0, s1, U, Cn)) M = fmaxf(M, __ldcg(a.partials + (size_t)(c + bh) * a.pstride));
+      for (int c = c_lo; c <= c_hi; ++c) M = fmaxf(M, __ldcg(a.partials + (size_t)(c + bh) * a.pstride));
       float L = exp2f(s_cur - M);
       for (int c = c_lo; c <= c_hi; ++c) {
-        if (!contributes(c, s0, s1, U, Cn)) continue;
         const float* pc = a.partials + (size_t)(c + bh) * a.pstride;
         L += __ldcg(pc + 1) * exp2f(__ldcg(pc) - M);
       }
@@ -171,7 +167,6 @@ __global__ void __launch_bounds__(kThreads, kCtasPerSm) bf16_kernel(Bf16Args a) 
       const float M = m_sh;
       float o = exp2f(red_s[0] - M) * __bfloat162float(a.v_cur[(size_t)bh * D + tid]);
       for (int c = c_lo; c <= c_hi; ++c) {
-        if (!contributes(c, s0, s1, U, Cn)) continue;
         const float* pc = a.partials + (size_t)(c + bh) * a.pstride;
         o = fmaf(exp2f(__ldcg(pc) - M), __ldcg(pc + 2 + tid), o);
       }
@@ -181,7 +176,7 @@ __global__ void __launch_bounds__(kThreads, kCtasPerSm) bf16_kernel(Bf16Args a) 
     __syncthreads();
   };
 
-  for (long long u = u0; u < u1; ++u) {
+  for (int u = u0; u < u1; ++u) {
     const int it = (int)(u - u0), stage = it % kStages;
     int bh, tile;
     locate(u, &bh, &tile);
@@ -259,7 +254,7 @@ __global__ void __launch_bounds__(kThreads, kCtasPerSm) bf16_kernel(Bf16Args a) 
   }
   if (aborted) {
     if (tid == 0)
-      for (long long v = fail_u; v < u1 && v < fail_u + kStages; ++v)
+      for (int v = fail_u; v < u1 && v < fail_u + kStages; ++v)
         (void)mbar_wait_bounded(&full_bar[(v - u0) % kStages], (uint32_t)(((v - u0) / kStages) & 1));
     __syncthreads();
     return;

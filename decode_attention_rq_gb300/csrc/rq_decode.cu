@@ -89,15 +89,17 @@ __device__ __forceinline__ float2 meta2(const uint8_t* p) {   // (scale, offset)
   return e4m3x2_to_f32x2(*reinterpret_cast<const uint16_t*>(p));
 }
 
-// flattened unit u -> CTA that owns it, for ranges [floor(cU/C), floor((c+1)U/C))
-__device__ __forceinline__ int cta_of(long long u, long long U, int C) {
-  return (int)(((u + 1) * C - 1) / U);
-}
-// CTA c's range intersects [s0, s1) (ranges are empty when units < CTAs)
-__device__ __forceinline__ bool contributes(int c, long long s0, long long s1, long long U, int C) {
-  long long r0 = (long long)c * U / C, r1 = (long long)(c + 1) * U / C;
-  return (r0 > s0 ? r0 : s0) < (r1 < s1 ? r1 : s1);
-}
+// Balanced split of U units over C CTAs: CTA c takes [start(c), start(c+1)) with
+// start(c) = c*q + min(c, rem), q = U / C, rem = U % C (32-bit arithmetic only).
+struct Split {
+  int q, rem;
+  __device__ __forceinline__ int start(int c) const { return c * q + min(c, rem); }
+  // CTA owning unit u (u < U)
+  __device__ __forceinline__ int owner(int u) const {
+    const int big = (q + 1) * rem;            // units held by the first rem CTAs
+    return u < big ? u / (q + 1) : rem + (u - big) / q;
+  }
+};
 
 template <int D, int GS, int NRES>
 struct Cfg {
@@ -108,12 +110,18 @@ struct Cfg {
   static constexpr int META = kTile * NG * 2;
   static constexpr int A_TILE = A_CODES + META;
   static constexpr int R_TILE = R_CODES + META + kTile * 2;
-  static constexpr int STAGES = NRES >= 2 ? 3 : 4;
-  static constexpr int STAGE = 2 * A_TILE + 2 * NRES * R_TILE;
-  static constexpr int PPT = kTile * NGP / kThreads;        // (token, group) pairs per thread
+  static constexpr int SUB = 2 * A_TILE + 2 * NRES * R_TILE;      // one 64-token layout tile
+  static constexpr int UT = 2;                                    // layout tiles per work unit
+  static constexpr int UTOK = UT * kTile;                         // tokens per work unit
+  static constexpr int STAGE = UT * SUB;
+  static constexpr int STAGES = NRES >= 2 ? 2 : 3;
+  static constexpr int PPT = UTOK * NGP / kThreads;               // (token, group) pairs per thread
+  static constexpr int TPL = UTOK / 32;                           // tokens per lane in the weight pass
   static constexpr int AW = GS / 8;              // 32-bit words of INT4 codes per (token, group)
   static constexpr int RW = GS / 16;             // 32-bit words of INT2 codes per (token, group)
-  static constexpr int NITEM = NG * (1 + NRES);  // (kind, group) value-weight items per tile
+  static constexpr int NITEM = NG * (1 + NRES);  // (kind, group) value-weight items per unit
+  static constexpr int IPW = (NITEM + kThreads / 32 - 1) / (kThreads / 32);   // items per warp
+  static constexpr int PACK = UTOK / 2;          // dp4a operand words per item and unit
   static constexpr int SMEM = STAGES * STAGE;
 };
 
@@ -121,21 +129,23 @@ template <int D, int GS, int NRES>
 __global__ void __launch_bounds__(kThreads, kCtasPerSm) decode_kernel(DecodeArgs a) {
   using C = Cfg<D, GS, NRES>;
   constexpr int NG = C::NG, NGP = C::NGP, AW = C::AW, RW = C::RW, STAGES = C::STAGES;
-  constexpr int NITEM = C::NITEM;
+  constexpr int NITEM = C::NITEM, UTOK = C::UTOK, TPL = C::TPL, IPW = C::IPW, PACK = C::PACK;
   extern __shared__ __align__(128) uint8_t smem[];
   __shared__ uint64_t full_bar[STAGES];
   __shared__ int pre_s[kMaxRows + 1];
-  __shared__ int nt_s[kMaxRows];
+  __shared__ int nt_s[kMaxRows + 1];        // work units (128-token) per row; then a sentinel
+  __shared__ int sl_s[kMaxRows];
   __shared__ __align__(16) float q_s[D];
   __shared__ __align__(16) float qr_s[D];
-  // per-tile scratch, double-buffered by tile parity
-  __shared__ float s_s[2][kTile];                  // token scores (base-2 logits)
+  // per-unit scratch, double-buffered by unit parity
+  __shared__ float s_s[2][UTOK];                   // token scores (base-2 logits)
   __shared__ float red_s[2][kThreads / 32];        // per-warp score maxima
-  __shared__ float tau_s[2][NITEM], off_s[2][NITEM];
-  // dp4a operands of the value weights, one 32-bit word per lane of the item's warp:
-  // anchor item: [8 words][E.hi, E.lo, O.hi, O.lo]; residual item: [4 words][mask m][hi, lo]
-  __shared__ __align__(16) uint32_t pack_s[2][NITEM][32];
+  __shared__ float tau_s[2][NITEM];
+  // dp4a operands of the value weights (see the weight pass for the word order)
+  __shared__ __align__(16) uint32_t pack_s[2][NITEM][PACK];
+  __shared__ float off_s[NITEM + 1];               // per-segment offset sums; [NITEM] = softmax sum
   __shared__ float mrg_s[8];
+  __shared__ float rt_s[D];
   __shared__ float m_sh, l_sh;
   __shared__ int flag_s;
 
@@ -143,11 +153,12 @@ __global__ void __launch_bounds__(kThreads, kCtasPerSm) decode_kernel(DecodeArgs
   const int H = a.g.H, B = a.batch;
   const int Cn = gridDim.x, cta = blockIdx.x;
 
-  // ---- per-row tile counts and prefix over (row, head) ----
+  // ---- per-row unit counts and prefix over (row, head) ----
   for (int b = tid; b < B; b += kThreads) {
     int n = a.seq_lens[b];
     n = n < 0 ? 0 : (n > a.g.Nmax ? a.g.Nmax : n);
-    nt_s[b] = (n + kTile - 1) / kTile;
+    sl_s[b] = n;
+    nt_s[b] = (n + UTOK - 1) / UTOK;
   }
   __syncthreads();
   if (tid == 0) {
@@ -157,9 +168,10 @@ __global__ void __launch_bounds__(kThreads, kCtasPerSm) decode_kernel(DecodeArgs
       acc += H * nt_s[b];
     }
     pre_s[B] = acc;
+    nt_s[B] = 1;   // sentinel for the row walk below
   }
   __syncthreads();
-  const long long U = pre_s[B];
+  const int U = pre_s[B];
 
   // ---- (row, head) pairs with an empty cache: the output is the current V ----
   for (int bh = cta; bh < B * H; bh += Cn) {
@@ -168,36 +180,52 @@ __global__ void __launch_bounds__(kThreads, kCtasPerSm) decode_kernel(DecodeArgs
       a.out[(size_t)bh * D + k] = __bfloat162float(a.v_cur[(size_t)bh * D + k]);
   }
   if (U == 0) return;
-  const long long u0 = (long long)cta * U / Cn, u1 = (long long)(cta + 1) * U / Cn;
+  const Split split{U / Cn, U % Cn};
+  const int u0 = split.start(cta), u1 = split.start(cta + 1);
   if (u0 >= u1) return;
 
-  auto locate = [&](long long u, int* bh, int* tile) {
+  // unit cursor (row, head, unit), advanced without divisions
+  struct Cursor { int b, h, t; };
+  auto locate = [&](int u) {
     int lo = 0, hi = B - 1;
-    while (lo < hi) {   // last row b with pre_s[b] <= u (rows with no tiles are skipped)
+    while (lo < hi) {   // last row b with pre_s[b] <= u (rows with no units are skipped)
       int mid = (lo + hi + 1) >> 1;
       if (pre_s[mid] <= u) lo = mid; else hi = mid - 1;
     }
     int rem = (int)(u - pre_s[lo]);
-    *bh = lo * H + rem / nt_s[lo];
-    *tile = rem % nt_s[lo];
+    return Cursor{lo, rem / nt_s[lo], rem % nt_s[lo]};
   };
-  auto issue = [&](long long u, int stage) {
-    int bh, tile;
-    locate(u, &bh, &tile);
-    const uint8_t* region = a.base + a.g.region_offset(a.layer, a.group, bh / H, bh % H);
-    uint8_t* dst = smem + stage * C::STAGE;
-    mbar_arrive_expect_tx(&full_bar[stage], C::STAGE);
-    bulk_g2s(dst, region + a.g.anchor_plane(0) + (int64_t)tile * C::A_TILE, C::A_TILE, &full_bar[stage]);
-    bulk_g2s(dst + C::A_TILE, region + a.g.anchor_plane(1) + (int64_t)tile * C::A_TILE, C::A_TILE,
-             &full_bar[stage]);
-#pragma unroll
-    for (int r = 0; r < NRES; ++r) {
-      uint8_t* d0 = dst + 2 * C::A_TILE + 2 * r * C::R_TILE;
-      bulk_g2s(d0, region + a.g.res_plane(a.res0 + r, 0) + (int64_t)tile * C::R_TILE, C::R_TILE,
-               &full_bar[stage]);
-      bulk_g2s(d0 + C::R_TILE, region + a.g.res_plane(a.res0 + r, 1) + (int64_t)tile * C::R_TILE,
-               C::R_TILE, &full_bar[stage]);
+  auto advance = [&](Cursor& c) {
+    if (++c.t == nt_s[c.b]) {
+      c.t = 0;
+      if (++c.h == H) {
+        c.h = 0;
+        do { ++c.b; } while (nt_s[c.b] == 0);   // nt_s[B] = 1 stops the walk
+      }
     }
+  };
+  Cursor pc = locate(u0);   // producer cursor (thread 0 only)
+  auto issue = [&](int stage) {
+    const uint8_t* region = a.base + a.g.region_offset(a.layer, a.group, pc.b, pc.h);
+    const int t0 = pc.t * C::UT;
+    // layout tiles of this unit that hold tokens (the last unit of a row may have one)
+    const int ntile = min(C::UT, (sl_s[pc.b] - t0 * kTile + kTile - 1) / kTile);
+    uint8_t* dst = smem + stage * C::STAGE;
+    mbar_arrive_expect_tx(&full_bar[stage], (uint32_t)(ntile * C::SUB));
+    for (int k = 0; k < ntile; ++k) {
+      uint8_t* d = dst + k * C::SUB;
+      const int64_t tile = t0 + k;
+      bulk_g2s(d, region + a.g.anchor_plane(0) + tile * C::A_TILE, C::A_TILE, &full_bar[stage]);
+      bulk_g2s(d + C::A_TILE, region + a.g.anchor_plane(1) + tile * C::A_TILE, C::A_TILE, &full_bar[stage]);
+#pragma unroll
+      for (int r = 0; r < NRES; ++r) {
+        uint8_t* d0 = d + 2 * C::A_TILE + 2 * r * C::R_TILE;
+        bulk_g2s(d0, region + a.g.res_plane(a.res0 + r, 0) + tile * C::R_TILE, C::R_TILE, &full_bar[stage]);
+        bulk_g2s(d0 + C::R_TILE, region + a.g.res_plane(a.res0 + r, 1) + tile * C::R_TILE, C::R_TILE,
+                 &full_bar[stage]);
+      }
+    }
+    advance(pc);
   };
 
   if (tid == 0) {
@@ -206,7 +234,8 @@ __global__ void __launch_bounds__(kThreads, kCtasPerSm) decode_kernel(DecodeArgs
   }
   __syncthreads();
   if (tid == 0)
-    for (int s = 0; s < STAGES && u0 + s < u1; ++s) issue(u0 + s, s);
+    for (int s = 0; s < STAGES && u0 + s < u1; ++s) issue(s);
+  Cursor cc = locate(u0);   // consumer cursor
 
   // ---- per-thread state ----
   const int gi1 = tid % NGP;              // phase-1 group of this thread (same for every pair)
@@ -216,34 +245,62 @@ __global__ void __launch_bounds__(kThreads, kCtasPerSm) decode_kernel(DecodeArgs
   uint32_t qrp[RW][4][2];
   float sig_a = 0.f, sig_r = 0.f, qsum = 0.f, qrsum = 0.f;
   float acc = 0.f;          // phase-2 accumulator: (channel, anchor|residual)
-  float m_run = -INFINITY, l_run = 0.f;   // l_run is kept by thread 0
+  float m_run = -INFINITY;
+  float off_part[IPW];      // lane partials of the offset sums of this warp's items
+  float l_part = 0.f;       // lane partial of the softmax denominator (warp 0)
+#pragma unroll
+  for (int j = 0; j < IPW; ++j) off_part[j] = 0.f;
   int cur_bh = -1;
   bool aborted = false;
-  long long fail_u = 0;
+  int fail_u = 0;
 
   const int p2_ch = tid < D ? tid : tid - D;
   const bool p2_anchor = tid < D;
   const bool p2_active = tid < (NRES > 0 ? 2 * D : D);
 
   auto flush = [&](int bh) {
+    // finish the segment's lane partials: offset sums per item and the denominator
+#pragma unroll
+    for (int j = 0; j < IPW; ++j) {
+      const int item = warp + j * (kThreads / 32);
+      float x = off_part[j];
+      for (int off = 16; off > 0; off >>= 1) x += __shfl_xor_sync(0xffffffffu, x, off);
+      if (item < NITEM && lane == 0) off_s[item] = x;
+    }
+    if (warp == 0) {
+      float x = l_part;
+      for (int off = 16; off > 0; off >>= 1) x += __shfl_xor_sync(0xffffffffu, x, off);
+      if (lane == 0) off_s[NITEM] = x;
+    }
+    __syncthreads();
     // write this CTA's partial for bh, then the last CTA merges
     float* part = a.partials + (size_t)(cta + bh) * a.pstride;
     if (tid == 0) {
       part[0] = m_run;
-      part[1] = l_run;
+      part[1] = off_s[NITEM];
     }
-    if (p2_active) part[2 + (p2_anchor ? 0 : D) + p2_ch] = acc;
+    if (p2_active) {
+      const int gi = p2_ch / GS;
+      float v = acc;
+      if (p2_anchor) {
+        v += off_s[gi];
+      } else {
+#pragma unroll
+        for (int r = 0; r < NRES; ++r) v += off_s[(1 + r) * NG + gi];
+      }
+      part[2 + (p2_anchor ? 0 : D) + p2_ch] = v;
+    }
     __threadfence();
     __syncthreads();
     const int b = bh / H, h = bh % H;
-    const long long s0 = pre_s[b] + (long long)h * nt_s[b];
-    const long long s1 = s0 + nt_s[b];
-    const int c_lo = cta_of(s0, U, Cn), c_hi = cta_of(s1 - 1, U, Cn);
+    const int s0 = pre_s[b] + h * nt_s[b];
+    const int s1 = s0 + nt_s[b];
+    // contributors: the CTAs owning units s0 .. s1-1 (every CTA in between owns at least
+    // one of them, as ranges are contiguous and cover every unit)
+    const int c_lo = split.owner(s0), c_hi = split.owner(s1 - 1);
     if (tid == 0) {
-      int needed = 0;
-      for (int c = c_lo; c <= c_hi; ++c) needed += contributes(c, s0, s1, U, Cn);
       int prev = atomicAdd(&a.counters[bh], 1);
-      flag_s = (prev == needed - 1);
+      flag_s = (prev == c_hi - c_lo);
     }
     __syncthreads();
     if (!flag_s) return;
@@ -258,13 +315,11 @@ __global__ void __launch_bounds__(kThreads, kCtasPerSm) decode_kernel(DecodeArgs
       float s_cur = 0.f;
       for (int w = 0; w < kThreads / 32; ++w) s_cur += mrg_s[w];
       float M = s_cur;
-      for (int c = c_lo; c <= c_hi; ++c)
-        if (contributes(c, s0, s1, U, Cn)) M = fmaxf(M, __ldcg(a.partials + (size_t)(c + bh) * a.pstride));
+      for (int c = c_lo; c <= c_hi; ++c) M = fmaxf(M, __ldcg(a.partials + (size_t)(c + bh) * a.pstride));
       float L = exp2f(s_cur - M);
       for (int c = c_lo; c <= c_hi; ++c) {
-        if (!contributes(c, s0, s1, U, Cn)) continue;
-        const float* pc = a.partials + (size_t)(c + bh) * a.pstride;
-        L += __ldcg(pc + 1) * exp2f(__ldcg(pc) - M);
+        const float* pc2 = a.partials + (size_t)(c + bh) * a.pstride;
+        L += __ldcg(pc2 + 1) * exp2f(__ldcg(pc2) - M);
       }
       m_sh = M;
       l_sh = L;
@@ -275,31 +330,32 @@ __global__ void __launch_bounds__(kThreads, kCtasPerSm) decode_kernel(DecodeArgs
     if (tid < D) {
       float va = 0.f, vr = 0.f;
       for (int c = c_lo; c <= c_hi; ++c) {
-        if (!contributes(c, s0, s1, U, Cn)) continue;
-        const float* pc = a.partials + (size_t)(c + bh) * a.pstride;
-        float w = exp2f(__ldcg(pc) - M);
-        va = fmaf(w, __ldcg(pc + 2 + tid), va);
-        if (NRES > 0) vr = fmaf(w, __ldcg(pc + 2 + D + tid), vr);
+        const float* pc2 = a.partials + (size_t)(c + bh) * a.pstride;
+        float w = exp2f(__ldcg(pc2) - M);
+        va = fmaf(w, __ldcg(pc2 + 2 + tid), va);
+        if (NRES > 0) vr = fmaf(w, __ldcg(pc2 + 2 + D + tid), vr);
       }
       va = fmaf(exp2f(s_cur - M), __bfloat162float(a.v_cur[(size_t)bh * D + tid]), va);
       if (NRES > 0) qr_s[tid] = vr;
       q_s[tid] = va;
     }
     __syncthreads();
-    if (tid < D) {
-      float o = q_s[tid];
-      if (NRES > 0) {
-        float t0 = 0.f, t1 = 0.f, t2 = 0.f, t3 = 0.f;   // (R^T acc_r)[tid], loads coalesced over tid
-#pragma unroll 4
-        for (int k = 0; k < D; k += 4) {
-          t0 = fmaf(__ldg(a.R + (size_t)(k + 0) * D + tid), qr_s[k + 0], t0);
-          t1 = fmaf(__ldg(a.R + (size_t)(k + 1) * D + tid), qr_s[k + 1], t1);
-          t2 = fmaf(__ldg(a.R + (size_t)(k + 2) * D + tid), qr_s[k + 2], t2);
-          t3 = fmaf(__ldg(a.R + (size_t)(k + 3) * D + tid), qr_s[k + 3], t3);
-        }
-        o += (t0 + t1) + (t2 + t3);
+    if (NRES > 0) {
+      // (R^T acc_r)[c]: thread = (column c, half of the rows); loads coalesced over c,
+      // issued 16 at a time
+      const int c = tid % D, hh = tid / D;
+      float t = 0.f;
+      if (tid < 2 * D) {
+        const float* rc = a.R + (size_t)hh * (D / 2) * D + c;
+        const float* ar = qr_s + hh * (D / 2);
+#pragma unroll 16
+        for (int k = 0; k < D / 2; ++k) t = fmaf(__ldg(rc + (size_t)k * D), ar[k], t);
+        if (hh == 1) rt_s[c] = t;
       }
-      a.out[(size_t)bh * D + tid] = o / L;
+      __syncthreads();
+      if (tid < D) a.out[(size_t)bh * D + c] = (q_s[c] + t + rt_s[c]) / L;
+    } else if (tid < D) {
+      a.out[(size_t)bh * D + tid] = q_s[tid] / L;
     }
     if (tid == 0) a.counters[bh] = 0;
     __syncthreads();
@@ -309,17 +365,24 @@ __global__ void __launch_bounds__(kThreads, kCtasPerSm) decode_kernel(DecodeArgs
     for (int k = tid; k < D; k += kThreads) q_s[k] = __bfloat162float(a.q[(size_t)bh * D + k]) * a.qscale;
     __syncthreads();
     if (NRES > 0) {
-      // q' = R q: warp w takes rows w, w+8, ...; one coalesced float4 per lane
-      for (int i = warp; i < D; i += kThreads / 32) {
-        float t = 0.f;
-        if (lane < D / 4) {
-          float4 r = __ldg(reinterpret_cast<const float4*>(a.R + (size_t)i * D) + lane);
-          float4 qv = *reinterpret_cast<const float4*>(&q_s[4 * lane]);
-          t = r.x * qv.x + r.y * qv.y + r.z * qv.z + r.w * qv.w;
+      // q' = R q: two threads per row, each with all its row loads in flight at once
+      constexpr int NV = D / 8;                 // float4 loads per half row
+      const int i = tid >> 1, hh = tid & 1;
+      float t = 0.f;
+      if (i < D) {
+        const float4* rp = reinterpret_cast<const float4*>(a.R + (size_t)i * D + hh * (D / 2));
+        const float4* qp = reinterpret_cast<const float4*>(q_s + hh * (D / 2));
+        float4 rv[NV];
+#pragma unroll
+        for (int v = 0; v < NV; ++v) rv[v] = __ldg(rp + v);
+#pragma unroll
+        for (int v = 0; v < NV; ++v) {
+          const float4 qv = qp[v];
+          t = fmaf(rv[v].x, qv.x, fmaf(rv[v].y, qv.y, fmaf(rv[v].z, qv.z, fmaf(rv[v].w, qv.w, t))));
         }
-        for (int off = 16; off > 0; off >>= 1) t += __shfl_xor_sync(0xffffffffu, t, off);
-        if (lane == 0) qr_s[i] = t;
       }
+      t += __shfl_xor_sync(0xffffffffu, t, 1);
+      if (i < D && hh == 0) qr_s[i] = t;
       __syncthreads();
     }
     // fixed-point packs of this thread's phase-1 group
@@ -366,44 +429,45 @@ __global__ void __launch_bounds__(kThreads, kCtasPerSm) decode_kernel(DecodeArgs
         }
     }
     m_run = -INFINITY;
-    l_run = 0.f;
+    l_part = 0.f;
+#pragma unroll
+    for (int j = 0; j < IPW; ++j) off_part[j] = 0.f;
     acc = 0.f;
     cur_bh = bh;
     __syncthreads();   // q_s / qr_s may be rewritten by the next merge only after all packs are read
   };
 
-  for (long long u = u0; u < u1; ++u) {
+  for (int u = u0; u < u1; ++u, advance(cc)) {
     const int it = (int)(u - u0), stage = it % STAGES, buf = it & 1;
-    int bh, tile;
-    locate(u, &bh, &tile);
+    const int bh = cc.b * H + cc.h;
     if (bh != cur_bh) {
       if (cur_bh >= 0) flush(cur_bh);
       begin_segment(bh);
     }
-    const int n_valid = min(kTile, a.seq_lens[bh / H] - tile * kTile);
+    const int n_valid = min(UTOK, sl_s[cc.b] - cc.t * UTOK);
 
     if (!mbar_wait_bounded(&full_bar[stage], (uint32_t)((it / STAGES) & 1))) aborted = true;
 
     const uint8_t* st = smem + stage * C::STAGE;
-    const uint8_t* AK = st;
-    const uint8_t* AV = st + C::A_TILE;
-    const uint8_t* RES = st + 2 * C::A_TILE;     // plane r: K at RES + 2r*R_TILE, V right after
 
     // ---- phase 1: score of each token; a token's NGP groups sit in adjacent lanes ----
     float wmax = -INFINITY;
 #pragma unroll
     for (int pp = 0; pp < C::PPT; ++pp) {
       const int tok = (tid + pp * kThreads) / NGP;
+      const uint8_t* sub = st + (tok >> 6) * C::SUB;   // layout tile of this token
+      const int row = tok & (kTile - 1);
       float score = 0.f;
-      if (g_ok && !aborted) {
+      if (g_ok && !aborted && tok < n_valid) {
         const int gi = gi1;
+        const uint8_t* AK = sub;
         // anchor: INT4 token-major; masks give the even / (16 x) odd channels as bytes
         uint32_t aw[4];
         if (AW == 4) {
-          uint4 v = *reinterpret_cast<const uint4*>(AK + tok * (D / 2) + gi * (GS / 2));
+          uint4 v = *reinterpret_cast<const uint4*>(AK + row * (D / 2) + gi * (GS / 2));
           aw[0] = v.x; aw[1] = v.y; aw[2] = v.z; aw[3] = v.w;
         } else {
-          uint2 v = *reinterpret_cast<const uint2*>(AK + tok * (D / 2) + gi * (GS / 2));
+          uint2 v = *reinterpret_cast<const uint2*>(AK + row * (D / 2) + gi * (GS / 2));
           aw[0] = v.x; aw[1] = v.y; aw[2] = 0u; aw[3] = 0u;
         }
         int eh = 0, el = 0, oh = 0, ol = 0;
@@ -416,20 +480,20 @@ __global__ void __launch_bounds__(kThreads, kCtasPerSm) decode_kernel(DecodeArgs
           ol = dp4a_uu(hi4, qa[w][3], ol);
         }
         const int ta = shl(shl(eh, 8) + el, 4) + shl(oh, 8) + ol;     // 16 x sum(q_fix * code)
-        const float2 ma = meta2(AK + C::A_CODES + tok * NG * 2 + gi * 2);
+        const float2 ma = meta2(AK + C::A_CODES + row * NG * 2 + gi * 2);
         const float score_a = fmaf(ma.x, (float)ta * sig_a, ma.y * qsum);
         score = score_a;
         if (NRES > 0) {
           float cprod = 1.f, sres = 0.f;
 #pragma unroll
           for (int r = 0; r < NRES; ++r) {
-            const uint8_t* RK = RES + 2 * r * C::R_TILE;
+            const uint8_t* RK = sub + 2 * C::A_TILE + 2 * r * C::R_TILE;
             uint32_t rw[2];
             if (RW == 2) {
-              uint2 v = *reinterpret_cast<const uint2*>(RK + tok * (D / 4) + gi * (GS / 4));
+              uint2 v = *reinterpret_cast<const uint2*>(RK + row * (D / 4) + gi * (GS / 4));
               rw[0] = v.x; rw[1] = v.y;
             } else {
-              rw[0] = *reinterpret_cast<const uint32_t*>(RK + tok * (D / 4) + gi * (GS / 4));
+              rw[0] = *reinterpret_cast<const uint32_t*>(RK + row * (D / 4) + gi * (GS / 4));
               rw[1] = 0u;
             }
             int hm[4] = {0, 0, 0, 0}, lm[4] = {0, 0, 0, 0};
@@ -443,8 +507,8 @@ __global__ void __launch_bounds__(kThreads, kCtasPerSm) decode_kernel(DecodeArgs
               }
             const int tr = shl(shl(hm[0], 8) + lm[0], 6) + shl(shl(hm[1], 8) + lm[1], 4) +
                            shl(shl(hm[2], 8) + lm[2], 2) + (shl(hm[3], 8) + lm[3]);   // 64 x dot
-            const float2 mr = meta2(RK + C::R_CODES + tok * NG * 2 + gi * 2);
-            const float cr = bf16_bits_to_f32(*reinterpret_cast<const uint16_t*>(RK + C::R_CODES + C::META + tok * 2));
+            const float2 mr = meta2(RK + C::R_CODES + row * NG * 2 + gi * 2);
+            const float cr = bf16_bits_to_f32(*reinterpret_cast<const uint16_t*>(RK + C::R_CODES + C::META + row * 2));
             // chained: plane r weighs the product of the coefficients before it
             sres = fmaf(cprod, fmaf(mr.x, (float)tr * sig_r, mr.y * qrsum), sres);
             cprod *= cr;
@@ -460,88 +524,103 @@ __global__ void __launch_bounds__(kThreads, kCtasPerSm) decode_kernel(DecodeArgs
     }
     for (int off = 16; off > 0; off >>= 1) wmax = fmaxf(wmax, __shfl_xor_sync(0xffffffffu, wmax, off));
     if (lane == 0) red_s[buf][warp] = wmax;
-    if (__syncthreads_or(aborted)) {                   // B1: scores of the tile are in s_s
+    if (__syncthreads_or(aborted)) {                   // B1: scores of the unit are in s_s
       fail_u = u;
       aborted = true;
       if (tid == 0) atomicExch(&a.status[0], 1);
       break;
     }
-    // every warp has finished the previous tile: its stage can be refilled
-    if (tid == 0 && it >= 1 && u - 1 + STAGES < u1) issue(u - 1 + STAGES, (it - 1) % STAGES);
+    // every warp has finished the previous unit: its stage can be refilled
+    if (tid == 0 && it >= 1 && u - 1 + STAGES < u1) issue((it - 1) % STAGES);
 
     float m_tile = red_s[buf][0];
 #pragma unroll
     for (int w = 1; w < kThreads / 32; ++w) m_tile = fmaxf(m_tile, red_s[buf][w]);
     const float m_new = fmaxf(m_run, m_tile);
-    const float alpha = exp2f(m_run - m_new);   // 0 on the first tile (m_run = -inf)
+    const float alpha = exp2f(m_run - m_new);   // 0 on the first unit (m_run = -inf)
     m_run = m_new;
 
     // ---- value weights: warp w takes items w, w+8, ... (item = (kind, group)) ----
-    for (int item = warp; item < NITEM; item += kThreads / 32) {
-      const int r = item / NG, gi = item % NG;      // r = 0 anchor, r >= 1 residual plane r-1
-      float wv[2], ov[2];
+    // lane holds tokens lane + 32k; p and the coefficient products per token
+    float pt[TPL];
 #pragma unroll
-      for (int hlf = 0; hlf < 2; ++hlf) {
-        const int tok = lane + 32 * hlf;
-        const float pt = exp2f(s_s[buf][tok] - m_new);   // 0 for masked tokens (-inf)
+    for (int k = 0; k < TPL; ++k) pt[k] = exp2f(s_s[buf][lane + 32 * k] - m_new);   // 0 if masked
+    if (warp == 0) {
+      float ps = 0.f;
+#pragma unroll
+      for (int k = 0; k < TPL; ++k) ps += pt[k];
+      l_part = fmaf(l_part, alpha, ps);
+    }
+#pragma unroll
+    for (int j = 0; j < IPW; ++j) {
+      const int item = warp + j * (kThreads / 32);
+      if (item >= NITEM) break;
+      const int r = item / NG, gi = item % NG;      // r = 0 anchor, r >= 1 residual plane r-1
+      float wv[TPL];
+      float osum = 0.f, mx = 0.f;
+#pragma unroll
+      for (int k = 0; k < TPL; ++k) {
+        const int tok = lane + 32 * k;
+        const uint8_t* sub = st + (tok >> 6) * C::SUB;
+        const int row = tok & (kTile - 1);
         float w = 0.f, o = 0.f;
         if (tok < n_valid) {
           float cprod = 1.f;   // product of the coefficients of the planes before this one
           const int upto = r == 0 ? NRES : r - 1;
 #pragma unroll
-          for (int k = 0; k < NRES; ++k)
-            if (k < upto)
+          for (int q = 0; q < NRES; ++q)
+            if (q < upto)
               cprod *= bf16_bits_to_f32(*reinterpret_cast<const uint16_t*>(
-                  RES + (2 * k + 1) * C::R_TILE + C::R_CODES + C::META + tok * 2));
-          const uint8_t* mp = r == 0 ? AV + C::A_CODES : RES + (2 * (r - 1) + 1) * C::R_TILE + C::R_CODES;
-          const float2 mv = meta2(mp + tok * NG * 2 + gi * 2);
-          w = pt * cprod * mv.x;
-          o = pt * cprod * mv.y;
+                  sub + 2 * C::A_TILE + (2 * q + 1) * C::R_TILE + C::R_CODES + C::META + row * 2));
+          const uint8_t* mp = r == 0 ? sub + C::A_TILE + C::A_CODES
+                                     : sub + 2 * C::A_TILE + (2 * (r - 1) + 1) * C::R_TILE + C::R_CODES;
+          const float2 mv = meta2(mp + row * NG * 2 + gi * 2);
+          const float pc = pt[k] * cprod;
+          w = pc * mv.x;
+          o = pc * mv.y;
         }
-        wv[hlf] = w;
-        ov[hlf] = o;
-        if (item == 0) {   // the warp of item 0 also sums p for the softmax denominator
-          float ps = pt;
-          for (int off = 16; off > 0; off >>= 1) ps += __shfl_xor_sync(0xffffffffu, ps, off);
-          if (lane == 0) l_run = (hlf == 0 ? l_run * alpha : l_run) + ps;
-        }
+        wv[k] = w;
+        osum += o;
+        mx = fmaxf(mx, fabsf(w));
       }
-      float mx = fmaxf(fabsf(wv[0]), fabsf(wv[1]));
-      float os = ov[0] + ov[1];
-      for (int off = 16; off > 0; off >>= 1) {
-        mx = fmaxf(mx, __shfl_xor_sync(0xffffffffu, mx, off));
-        os += __shfl_xor_sync(0xffffffffu, os, off);
-      }
+      off_part[j] = fmaf(off_part[j], alpha, osum);
+      // |w| >= 0 compares like its bit pattern: one warp-wide integer max
+      mx = __uint_as_float(__reduce_max_sync(0xffffffffu, __float_as_uint(mx)));
       const float inv = mx > 0.f ? kFix / mx : 0.f;
-      // both tokens' 16-bit fixed-point values in one word: token lane | token lane+32 << 16
-      const uint32_t pv = ((uint32_t)to_fix(wv[0], inv) & 0xFFFFu) | ((uint32_t)to_fix(wv[1], inv) << 16);
-      uint32_t word = 0;
-      if (r == 0) {
-        // lane = word w (8) x kind k: tokens 8w + 2i + (k >> 1), byte hi (k even) or lo
-        const int w8 = lane >> 2, k = lane & 3, half = w8 >> 2;
+      // two tokens' 16-bit fixed-point values per word: pv[h] = token lane+64h | token lane+64h+32 << 16
+      uint32_t pv[TPL / 2];
 #pragma unroll
-        for (int i = 0; i < 4; ++i) {
-          const int tk = 8 * w8 + 2 * i + (k >> 1);
-          const uint32_t x = __shfl_sync(0xffffffffu, pv, tk & 31);
-          const int v = (int)(int16_t)(x >> (16 * half));
-          word |= ((k & 1) ? fix_lo(v) : fix_hi(v)) << (8 * i);
-        }
-      } else {
-        // lane = word j (4) x mask m (4) x part: tokens 16j + 4i + m
-        const int j = lane >> 3, m = (lane >> 1) & 3, part = lane & 1, half = j >> 1;
+      for (int h = 0; h < TPL / 2; ++h)
+        pv[h] = ((uint32_t)to_fix(wv[2 * h], inv) & 0xFFFFu) | ((uint32_t)to_fix(wv[2 * h + 1], inv) << 16);
+      // each lane builds PACK/32 operand words; word idx covers tokens inside one 64-token half
 #pragma unroll
-        for (int i = 0; i < 4; ++i) {
-          const int tk = 16 * j + 4 * i + m;
-          const uint32_t x = __shfl_sync(0xffffffffu, pv, tk & 31);
-          const int v = (int)(int16_t)(x >> (16 * half));
-          word |= (part ? fix_lo(v) : fix_hi(v)) << (8 * i);
+      for (int h = 0; h < TPL / 2; ++h) {
+        const int idx = lane + 32 * h;
+        uint32_t word = 0;
+        if (r == 0) {
+          // anchor: idx = word w (0..15) x kind k: tokens 8w + 2i + (k >> 1), hi (k even) / lo byte
+          const int w8 = idx >> 2, k = idx & 3;
+#pragma unroll
+          for (int i = 0; i < 4; ++i) {
+            const int tk = 8 * w8 + 2 * i + (k >> 1);
+            const uint32_t x = __shfl_sync(0xffffffffu, pv[h], tk & 31);
+            const int v = (int)(int16_t)(x >> (16 * ((tk >> 5) & 1)));
+            word |= ((k & 1) ? fix_lo(v) : fix_hi(v)) << (8 * i);
+          }
+        } else {
+          // residual: idx = word j (0..7) x mask m (4) x part: tokens 16j + 4i + m
+          const int j8 = idx >> 3, m = (idx >> 1) & 3, part = idx & 1;
+#pragma unroll
+          for (int i = 0; i < 4; ++i) {
+            const int tk = 16 * j8 + 4 * i + m;
+            const uint32_t x = __shfl_sync(0xffffffffu, pv[h], tk & 31);
+            const int v = (int)(int16_t)(x >> (16 * ((tk >> 5) & 1)));
+            word |= (part ? fix_lo(v) : fix_hi(v)) << (8 * i);
+          }
         }
+        pack_s[buf][item][idx] = word;
       }
-      pack_s[buf][item][lane] = word;
-      if (lane == 0) {
-        tau_s[buf][item] = mx / kFix;
-        off_s[buf][item] = os;
-      }
+      if (lane == 0) tau_s[buf][item] = mx / kFix;
     }
     __syncthreads();                                   // B2: weight operands are in pack_s
 
@@ -550,60 +629,68 @@ __global__ void __launch_bounds__(kThreads, kCtasPerSm) decode_kernel(DecodeArgs
       const int gi = p2_ch / GS;
       float add = 0.f;
       if (p2_anchor) {
-        const uint4* row = reinterpret_cast<const uint4*>(AV + p2_ch * (kTile / 2));
         const uint32_t* pw = pack_s[buf][gi];
         int eh = 0, el = 0, oh = 0, ol = 0;
 #pragma unroll
-        for (int h2 = 0; h2 < 2; ++h2) {
-          const uint4 x4 = row[h2];
-          const uint32_t xs[4] = {x4.x, x4.y, x4.z, x4.w};
+        for (int sb = 0; sb < C::UT; ++sb) {
+          const uint4* row = reinterpret_cast<const uint4*>(st + sb * C::SUB + C::A_TILE + p2_ch * (kTile / 2));
 #pragma unroll
-          for (int q4 = 0; q4 < 4; ++q4) {
-            const int w = h2 * 4 + q4;
-            const uint4 pk = *reinterpret_cast<const uint4*>(pw + 4 * w);
-            const uint32_t lo4 = xs[q4] & 0x0F0F0F0Fu, hi4 = xs[q4] & 0xF0F0F0F0u;
-            eh = dp4a_us(lo4, pk.x, eh);
-            el = dp4a_uu(lo4, pk.y, el);
-            oh = dp4a_us(hi4, pk.z, oh);
-            ol = dp4a_uu(hi4, pk.w, ol);
+          for (int h2 = 0; h2 < 2; ++h2) {
+            const uint4 x4 = row[h2];
+            const uint32_t xs[4] = {x4.x, x4.y, x4.z, x4.w};
+#pragma unroll
+            for (int q4 = 0; q4 < 4; ++q4) {
+              const int w = sb * 8 + h2 * 4 + q4;
+              const uint4 pk = *reinterpret_cast<const uint4*>(pw + 4 * w);
+              const uint32_t lo4 = xs[q4] & 0x0F0F0F0Fu, hi4 = xs[q4] & 0xF0F0F0F0u;
+              eh = dp4a_us(lo4, pk.x, eh);
+              el = dp4a_uu(lo4, pk.y, el);
+              oh = dp4a_us(hi4, pk.z, oh);
+              ol = dp4a_uu(hi4, pk.w, ol);
+            }
           }
         }
         const int t = shl(shl(eh, 8) + el, 4) + shl(oh, 8) + ol;        // 16 x sum(w_fix * code)
-        add = fmaf((float)t, tau_s[buf][gi] * (1.f / 16.f), off_s[buf][gi]);
+        add = (float)t * (tau_s[buf][gi] * (1.f / 16.f));
       } else {
 #pragma unroll
         for (int r = 0; r < NRES; ++r) {
           const int item = (1 + r) * NG + gi;
           const uint32_t* pw = pack_s[buf][item];
-          const uint4 x4 = *reinterpret_cast<const uint4*>(RES + (2 * r + 1) * C::R_TILE + p2_ch * (kTile / 4));
-          const uint32_t xs[4] = {x4.x, x4.y, x4.z, x4.w};
           int hm[4] = {0, 0, 0, 0}, lm[4] = {0, 0, 0, 0};
 #pragma unroll
-          for (int j = 0; j < 4; ++j) {
-            const uint4 pa = *reinterpret_cast<const uint4*>(pw + 8 * j);
-            const uint4 pb = *reinterpret_cast<const uint4*>(pw + 8 * j + 4);
-            const uint32_t b0 = xs[j] & 0x03030303u, b1 = xs[j] & 0x0C0C0C0Cu;
-            const uint32_t b2 = xs[j] & 0x30303030u, b3 = xs[j] & 0xC0C0C0C0u;
-            hm[0] = dp4a_us(b0, pa.x, hm[0]); lm[0] = dp4a_uu(b0, pa.y, lm[0]);
-            hm[1] = dp4a_us(b1, pa.z, hm[1]); lm[1] = dp4a_uu(b1, pa.w, lm[1]);
-            hm[2] = dp4a_us(b2, pb.x, hm[2]); lm[2] = dp4a_uu(b2, pb.y, lm[2]);
-            hm[3] = dp4a_us(b3, pb.z, hm[3]); lm[3] = dp4a_uu(b3, pb.w, lm[3]);
+          for (int sb = 0; sb < C::UT; ++sb) {
+            const uint4 x4 = *reinterpret_cast<const uint4*>(st + sb * C::SUB + 2 * C::A_TILE +
+                                                             (2 * r + 1) * C::R_TILE + p2_ch * (kTile / 4));
+            const uint32_t xs[4] = {x4.x, x4.y, x4.z, x4.w};
+#pragma unroll
+            for (int j = 0; j < 4; ++j) {
+              const int jw = sb * 4 + j;
+              const uint4 pa = *reinterpret_cast<const uint4*>(pw + 8 * jw);
+              const uint4 pb = *reinterpret_cast<const uint4*>(pw + 8 * jw + 4);
+              const uint32_t b0 = xs[j] & 0x03030303u, b1 = xs[j] & 0x0C0C0C0Cu;
+              const uint32_t b2 = xs[j] & 0x30303030u, b3 = xs[j] & 0xC0C0C0C0u;
+              hm[0] = dp4a_us(b0, pa.x, hm[0]); lm[0] = dp4a_uu(b0, pa.y, lm[0]);
+              hm[1] = dp4a_us(b1, pa.z, hm[1]); lm[1] = dp4a_uu(b1, pa.w, lm[1]);
+              hm[2] = dp4a_us(b2, pb.x, hm[2]); lm[2] = dp4a_uu(b2, pb.y, lm[2]);
+              hm[3] = dp4a_us(b3, pb.z, hm[3]); lm[3] = dp4a_uu(b3, pb.w, lm[3]);
+            }
           }
           const int t = shl(shl(hm[0], 8) + lm[0], 6) + shl(shl(hm[1], 8) + lm[1], 4) +
                         shl(shl(hm[2], 8) + lm[2], 2) + (shl(hm[3], 8) + lm[3]);   // 64 x sum
-          add += fmaf((float)t, tau_s[buf][item] * (1.f / 64.f), off_s[buf][item]);
+          add = fmaf((float)t, tau_s[buf][item] * (1.f / 64.f), add);
         }
       }
       acc = fmaf(acc, alpha, add);
     }
-    // no barrier here: the next tile's writes go to the other parity buffers, and its
+    // no barrier here: the next unit's writes go to the other parity buffers, and its
     // stage is refilled only after the next B1
   }
 
   if (aborted) {
     // let the copies still in flight land before the CTA exits (each wait bounded)
     if (tid == 0)
-      for (long long v = fail_u; v < u1 && v < fail_u + STAGES; ++v)
+      for (int v = fail_u; v < u1 && v < fail_u + STAGES; ++v)
         (void)mbar_wait_bounded(&full_bar[(v - u0) % STAGES], (uint32_t)(((v - u0) / STAGES) & 1));
     __syncthreads();
     return;
