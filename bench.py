@@ -295,9 +295,10 @@ def run_rq(args, w):
         step(s.cuda_stream)
     torch.cuda.synchronize()
 
-    # warm-up
-    for _ in range(args.warmup):
-        graph.replay()
+    # warm-up (replay() launches on the current stream: make it s, where the events are)
+    with torch.cuda.stream(s):
+        for _ in range(args.warmup):
+            graph.replay()
     torch.cuda.synchronize()
     # timed region
     e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
@@ -305,10 +306,11 @@ def run_rq(args, w):
         if world > 1:
             torch.distributed.barrier()
         torch.cuda.synchronize()
-        e0.record(s)
-        for _ in range(args.steps):
-            graph.replay()
-        e1.record(s)
+        with torch.cuda.stream(s):
+            e0.record(s)
+            for _ in range(args.steps):
+                graph.replay()
+            e1.record(s)
         torch.cuda.synchronize()
         if world > 1:
             torch.distributed.barrier()
@@ -409,14 +411,15 @@ def bench_bf16(args, w, dev, gen, scale):
     graph = torch.cuda.CUDAGraph()
     with torch.cuda.graph(graph, stream=s):
         step(s.cuda_stream)
-    for _ in range(args.warmup):
-        graph.replay()
-    torch.cuda.synchronize()
     e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
-    e0.record(s)
-    for _ in range(args.steps):
-        graph.replay()
-    e1.record(s)
+    with torch.cuda.stream(s):
+        for _ in range(args.warmup):
+            graph.replay()
+        torch.cuda.synchronize()
+        e0.record(s)
+        for _ in range(args.steps):
+            graph.replay()
+        e1.record(s)
     torch.cuda.synchronize()
     ms = e0.elapsed_time(e1) / args.steps
     byts = ncalls * B * H * (N * 2 * d * 2 + 3 * d * 2 + d * 4)
@@ -434,8 +437,9 @@ def bench_e2e(args, graph, s, q_all, temp_all, out_all, B):
     q_h = q_all.cpu().pin_memory()
     t_h = temp_all.cpu().pin_memory()
     o_h = torch.empty(out_all.shape, dtype=out_all.dtype).pin_memory()
-    for _ in range(args.warmup):
-        graph.replay()
+    with torch.cuda.stream(s):
+        for _ in range(args.warmup):
+            graph.replay()
     torch.cuda.synchronize()
     t0 = time.perf_counter()
     e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)

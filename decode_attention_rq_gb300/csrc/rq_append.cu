@@ -14,9 +14,9 @@
 // match the exact-arithmetic reading for a given rotated residual.  The
 // rotation itself (d x d per vector) runs in float32 FMA.
 //
-// Grid: x = block of 4-position quads of one row, y = row * H + head, z = K/V.
-// A CTA owns whole aligned quads of positions, so the channel-major V bytes
-// it writes (2 or 4 positions per byte) are touched by no other CTA.
+// Grid: x = aligned block of 16 positions of one row, y = row * H + head,
+// z = K/V.  A channel-major V word holds 8 (INT4) or 16 (INT2) aligned
+// positions, so the words a CTA rewrites are touched by no other CTA.
 #include <cuda_fp8.h>
 
 #include "rq_internal.cuh"
@@ -25,8 +25,7 @@ namespace rq {
 namespace {
 
 constexpr int kThreads = 128;      // one thread per channel (d <= 128)
-constexpr int kQuadsPerCta = 4;    // 16 positions per CTA
-constexpr int kTok = 4 * kQuadsPerCta;
+constexpr int kTok = 16;           // positions per CTA (an aligned block)
 
 __device__ __forceinline__ uint8_t f32_to_e4m3(float x) {
   return (uint8_t)__nv_cvt_float_to_fp8(x, __NV_SATFINITE, __NV_E4M3);
@@ -136,23 +135,26 @@ __device__ void write_plane(const AppendArgs& a, uint8_t* plane, int64_t tile_by
       row[tid] = (uint8_t)byte;
     }
   } else {
-    // channel-major rows: thread = channel, one byte per `per_byte` positions
+    // channel-major rows: thread = channel; a 32-bit word holds tpw aligned positions,
+    // position q of the word in byte q % 4 at bit field q / 4
     if (tid < d) {
       const int row_bytes = kTile / per_byte;
-      for (int t0 = 0; t0 < kTok; t0 += per_byte) {
+      const int tpw = 4 * per_byte;
+      const uint32_t fmask = (1u << bits) - 1u;
+      for (int t0 = 0; t0 < kTok; t0 += tpw) {
         bool any = false;
-        for (int m = 0; m < per_byte; ++m) any |= valid[t0 + m];
+        for (int q = 0; q < tpw; ++q) any |= valid[t0 + q];
         if (!any) continue;
-        int pos0 = p0 + t0;   // aligned to per_byte (p0 is quad-aligned)
-        uint8_t* byte_ptr = plane + (int64_t)(pos0 / kTile) * tile_bytes + tid * row_bytes +
-                            (pos0 % kTile) / per_byte;
-        uint32_t byte = *byte_ptr;
-        for (int m = 0; m < per_byte; ++m) {
-          if (!valid[t0 + m]) continue;
-          uint32_t mask = ((1u << bits) - 1u) << (bits * m);
-          byte = (byte & ~mask) | ((uint32_t)codes[t0 + m][tid] << (bits * m));
+        const int pos0 = p0 + t0;   // word-aligned: p0 is a multiple of kTok
+        uint32_t* wp = reinterpret_cast<uint32_t*>(plane + (int64_t)(pos0 / kTile) * tile_bytes +
+                                                   tid * row_bytes + (pos0 % kTile) / per_byte);
+        uint32_t word = *wp;
+        for (int q = 0; q < tpw; ++q) {
+          if (!valid[t0 + q]) continue;
+          const int sh = 8 * (q & 3) + bits * (q >> 2);
+          word = (word & ~(fmask << sh)) | ((uint32_t)codes[t0 + q][tid] << sh);
         }
-        *byte_ptr = (uint8_t)byte;
+        *wp = word;
       }
     }
   }
@@ -217,10 +219,9 @@ __global__ void __launch_bounds__(kThreads) append_kernel(AppendArgs a) {
     if (blockIdx.x == 0 && h == 0 && kvi == 0 && tid == 0 && a.status) atomicExch(&a.status[1], 1);
     return;
   }
-  const int q_first = start / 4, q_last = (start + a.n - 1) / 4;
-  const int q0 = q_first + blockIdx.x * kQuadsPerCta;
-  if (q0 > q_last) return;
-  const int p0 = q0 * 4;
+  const int blk = start / kTok + blockIdx.x;
+  if (blk > (start + a.n - 1) / kTok) return;
+  const int p0 = blk * kTok;
   if (tid < kTok) {
     int pos = p0 + tid;
     valid_s[tid] = pos >= start && pos < start + a.n;
@@ -232,9 +233,12 @@ __global__ void __launch_bounds__(kThreads) append_kernel(AppendArgs a) {
   __syncthreads();
 
   uint8_t* region = a.base + a.g.region_offset(a.layer, a.group, b, h);
-  // every valid slot in the first quad: rotate 4 slots instead of 16
-  bool few = true;
-  for (int t = 4; t < kTok; ++t) few = few && !valid_s[t];
+  // all valid slots inside one aligned quad (a short append): rotate 4 slots, not 16
+  int t_lo = kTok, t_hi = 0;
+  for (int t = 0; t < kTok; ++t)
+    if (valid_s[t]) { t_lo = min(t_lo, t); t_hi = t; }
+  const int t4 = t_lo & ~3;   // t_lo < kTok: the block holds at least one appended position
+  const bool few = t_hi < t4 + 4;
   const bool act = tid < d;
 
   // ---- anchor: loop P-1, 4-bit (slots outside the appended range are skipped) ----
@@ -292,7 +296,7 @@ __global__ void __launch_bounds__(kThreads) append_kernel(AppendArgs a) {
     __syncthreads();
     // rotation u = R e, thread = output channel, sequential FMA over k
     if (act) {
-      if (few) rotate_rows<4>(a.R, d, tid, x_s, u_s);
+      if (few) rotate_rows<4>(a.R, d, tid, x_s + t4, u_s + t4);
       else rotate_rows<kTok>(a.R, d, tid, x_s, u_s);
     }
     __syncthreads();
@@ -350,9 +354,8 @@ cudaError_t launch_append(const rq_cache& c, int layer, int group, int batch,
   a.group = group;
   a.batch = batch;
   a.n = n_tokens;
-  // quads touched by n tokens starting anywhere: at most (n + 3) / 4 + 1
-  int quads = (n_tokens + 3) / 4 + 1;
-  dim3 grid((quads + kQuadsPerCta - 1) / kQuadsPerCta, batch * c.geom.H, 2);
+  // aligned 16-position blocks touched by n tokens starting anywhere: at most ceil(n/16) + 1
+  dim3 grid((n_tokens + kTok - 1) / kTok + 1, batch * c.geom.H, 2);
   append_kernel<<<grid, kThreads, 0, stream>>>(a);
   return cudaGetLastError();
 }

@@ -116,12 +116,10 @@ struct Cfg {
   static constexpr int STAGE = UT * SUB;
   static constexpr int STAGES = NRES >= 2 ? 2 : 3;
   static constexpr int PPT = UTOK * NGP / kThreads;               // (token, group) pairs per thread
-  static constexpr int TPL = UTOK / 32;                           // tokens per lane in the weight pass
   static constexpr int AW = GS / 8;              // 32-bit words of INT4 codes per (token, group)
   static constexpr int RW = GS / 16;             // 32-bit words of INT2 codes per (token, group)
   static constexpr int NITEM = NG * (1 + NRES);  // (kind, group) value-weight items per unit
-  static constexpr int IPW = (NITEM + kThreads / 32 - 1) / (kThreads / 32);   // items per warp
-  static constexpr int PACK = UTOK / 2;          // dp4a operand words per item and unit
+  static constexpr int WQ = 2 * UTOK + 16;       // weight bytes per item: hi by token, lo by token, pad
   static constexpr int SMEM = STAGES * STAGE;
 };
 
@@ -129,7 +127,7 @@ template <int D, int GS, int NRES>
 __global__ void __launch_bounds__(kThreads, kCtasPerSm) decode_kernel(DecodeArgs a) {
   using C = Cfg<D, GS, NRES>;
   constexpr int NG = C::NG, NGP = C::NGP, AW = C::AW, RW = C::RW, STAGES = C::STAGES;
-  constexpr int NITEM = C::NITEM, UTOK = C::UTOK, TPL = C::TPL, IPW = C::IPW, PACK = C::PACK;
+  constexpr int NITEM = C::NITEM, UTOK = C::UTOK, PPT = C::PPT, WQ = C::WQ;
   extern __shared__ __align__(128) uint8_t smem[];
   __shared__ uint64_t full_bar[STAGES];
   __shared__ int pre_s[kMaxRows + 1];
@@ -137,12 +135,14 @@ __global__ void __launch_bounds__(kThreads, kCtasPerSm) decode_kernel(DecodeArgs
   __shared__ int sl_s[kMaxRows];
   __shared__ __align__(16) float q_s[D];
   __shared__ __align__(16) float qr_s[D];
-  // per-unit scratch, double-buffered by unit parity
-  __shared__ float s_s[2][UTOK];                   // token scores (base-2 logits)
+  // per-unit scratch; the first two are double-buffered by unit parity
   __shared__ float red_s[2][kThreads / 32];        // per-warp score maxima
-  __shared__ float tau_s[2][NITEM];
-  // dp4a operands of the value weights (see the weight pass for the word order)
-  __shared__ __align__(16) uint32_t pack_s[2][NITEM][PACK];
+  __shared__ uint32_t tmax_s[2][NITEM];            // max |value weight| per item, float bits
+  // value weights of the unit in 16-bit fixed point, per item: the hi bytes indexed by token,
+  // then the lo bytes.  V rows put four consecutive tokens of a channel in the bytes of a
+  // masked code word, so one 32-bit load here is the matching dp4a operand.
+  __shared__ __align__(16) uint8_t wq_s[NITEM][WQ];
+  __shared__ float wsum_s[kThreads / 32][NITEM + 1];   // per-warp partials of off_s
   __shared__ float off_s[NITEM + 1];               // per-segment offset sums; [NITEM] = softmax sum
   __shared__ float mrg_s[8];
   __shared__ float rt_s[D];
@@ -232,6 +232,7 @@ __global__ void __launch_bounds__(kThreads, kCtasPerSm) decode_kernel(DecodeArgs
     for (int s = 0; s < STAGES; ++s) mbar_init(&full_bar[s], 1);
     fence_mbar_init();
   }
+  for (int i = tid; i < 2 * NITEM; i += kThreads) (&tmax_s[0][0])[i] = 0u;
   __syncthreads();
   if (tid == 0)
     for (int s = 0; s < STAGES && u0 + s < u1; ++s) issue(s);
@@ -246,10 +247,10 @@ __global__ void __launch_bounds__(kThreads, kCtasPerSm) decode_kernel(DecodeArgs
   float sig_a = 0.f, sig_r = 0.f, qsum = 0.f, qrsum = 0.f;
   float acc = 0.f;          // phase-2 accumulator: (channel, anchor|residual)
   float m_run = -INFINITY;
-  float off_part[IPW];      // lane partials of the offset sums of this warp's items
-  float l_part = 0.f;       // lane partial of the softmax denominator (warp 0)
+  float off_part[1 + NRES]; // partial offset sums of this thread's group: anchor, residual planes
+  float l_part = 0.f;       // partial softmax denominator (threads of group 0)
 #pragma unroll
-  for (int j = 0; j < IPW; ++j) off_part[j] = 0.f;
+  for (int j = 0; j <= NRES; ++j) off_part[j] = 0.f;
   int cur_bh = -1;
   bool aborted = false;
   int fail_u = 0;
@@ -259,18 +260,25 @@ __global__ void __launch_bounds__(kThreads, kCtasPerSm) decode_kernel(DecodeArgs
   const bool p2_active = tid < (NRES > 0 ? 2 * D : D);
 
   auto flush = [&](int bh) {
-    // finish the segment's lane partials: offset sums per item and the denominator
+    // finish the segment's partials: offset sums per item and the softmax denominator,
+    // per warp, then over the warps in a fixed order (repeated calls give equal bits)
 #pragma unroll
-    for (int j = 0; j < IPW; ++j) {
-      const int item = warp + j * (kThreads / 32);
+    for (int j = 0; j <= NRES; ++j) {
       float x = off_part[j];
-      for (int off = 16; off > 0; off >>= 1) x += __shfl_xor_sync(0xffffffffu, x, off);
-      if (item < NITEM && lane == 0) off_s[item] = x;
+      for (int off = NGP; off < 32; off <<= 1) x += __shfl_xor_sync(0xffffffffu, x, off);
+      if (lane < NGP && g_ok) wsum_s[warp][j * NG + gi1] = x;
     }
-    if (warp == 0) {
+    {
       float x = l_part;
       for (int off = 16; off > 0; off >>= 1) x += __shfl_xor_sync(0xffffffffu, x, off);
-      if (lane == 0) off_s[NITEM] = x;
+      if (lane == 0) wsum_s[warp][NITEM] = x;
+    }
+    __syncthreads();
+    for (int i = tid; i <= NITEM; i += kThreads) {
+      float x = 0.f;
+#pragma unroll
+      for (int w = 0; w < kThreads / 32; ++w) x += wsum_s[w][i];
+      off_s[i] = x;
     }
     __syncthreads();
     // write this CTA's partial for bh, then the last CTA merges
@@ -431,7 +439,7 @@ __global__ void __launch_bounds__(kThreads, kCtasPerSm) decode_kernel(DecodeArgs
     m_run = -INFINITY;
     l_part = 0.f;
 #pragma unroll
-    for (int j = 0; j < IPW; ++j) off_part[j] = 0.f;
+    for (int j = 0; j <= NRES; ++j) off_part[j] = 0.f;
     acc = 0.f;
     cur_bh = bh;
     __syncthreads();   // q_s / qr_s may be rewritten by the next merge only after all packs are read
@@ -452,8 +460,9 @@ __global__ void __launch_bounds__(kThreads, kCtasPerSm) decode_kernel(DecodeArgs
 
     // ---- phase 1: score of each token; a token's NGP groups sit in adjacent lanes ----
     float wmax = -INFINITY;
+    float sc[PPT];            // scores of this thread's tokens (every lane of a token has it)
 #pragma unroll
-    for (int pp = 0; pp < C::PPT; ++pp) {
+    for (int pp = 0; pp < PPT; ++pp) {
       const int tok = (tid + pp * kThreads) / NGP;
       const uint8_t* sub = st + (tok >> 6) * C::SUB;   // layout tile of this token
       const int row = tok & (kTile - 1);
@@ -519,12 +528,12 @@ __global__ void __launch_bounds__(kThreads, kCtasPerSm) decode_kernel(DecodeArgs
 #pragma unroll
       for (int off = 1; off < NGP; off <<= 1) score += __shfl_xor_sync(0xffffffffu, score, off);
       if (tok >= n_valid) score = -INFINITY;
-      if (gi1 == 0) s_s[buf][tok] = score;
+      sc[pp] = score;
       wmax = fmaxf(wmax, score);
     }
     for (int off = 16; off > 0; off >>= 1) wmax = fmaxf(wmax, __shfl_xor_sync(0xffffffffu, wmax, off));
     if (lane == 0) red_s[buf][warp] = wmax;
-    if (__syncthreads_or(aborted)) {                   // B1: scores of the unit are in s_s
+    if (__syncthreads_or(aborted)) {                   // B1: per-warp score maxima are in red_s
       fail_u = u;
       aborted = true;
       if (tid == 0) atomicExch(&a.status[0], 1);
@@ -540,96 +549,72 @@ __global__ void __launch_bounds__(kThreads, kCtasPerSm) decode_kernel(DecodeArgs
     const float alpha = exp2f(m_run - m_new);   // 0 on the first unit (m_run = -inf)
     m_run = m_new;
 
-    // ---- value weights: warp w takes items w, w+8, ... (item = (kind, group)) ----
-    // lane holds tokens lane + 32k; p and the coefficient products per token
-    float pt[TPL];
+    // the maxima of the other parity were last read before B1: clear them for the next unit
+    if (tid < NITEM) tmax_s[buf ^ 1][tid] = 0u;
+
+    // ---- value weights of this thread's (token, group) pairs: p * coefficients * scale,
+    //      and the offset terms p * coefficients * offset summed on the fly ----
+    float wv[PPT][1 + NRES];
 #pragma unroll
-    for (int k = 0; k < TPL; ++k) pt[k] = exp2f(s_s[buf][lane + 32 * k] - m_new);   // 0 if masked
-    if (warp == 0) {
-      float ps = 0.f;
+    for (int j = 0; j <= NRES; ++j) off_part[j] *= alpha;
 #pragma unroll
-      for (int k = 0; k < TPL; ++k) ps += pt[k];
-      l_part = fmaf(l_part, alpha, ps);
-    }
+    for (int pp = 0; pp < PPT; ++pp) {
+      const int tok = (tid + pp * kThreads) / NGP;
+      const float pt = exp2f(sc[pp] - m_new);          // 0 for masked tokens
+      if (gi1 == 0) l_part = fmaf(l_part, pp == 0 ? alpha : 1.f, pt);
 #pragma unroll
-    for (int j = 0; j < IPW; ++j) {
-      const int item = warp + j * (kThreads / 32);
-      if (item >= NITEM) break;
-      const int r = item / NG, gi = item % NG;      // r = 0 anchor, r >= 1 residual plane r-1
-      float wv[TPL];
-      float osum = 0.f, mx = 0.f;
-#pragma unroll
-      for (int k = 0; k < TPL; ++k) {
-        const int tok = lane + 32 * k;
+      for (int j = 0; j <= NRES; ++j) wv[pp][j] = 0.f;
+      if (g_ok && tok < n_valid) {
         const uint8_t* sub = st + (tok >> 6) * C::SUB;
         const int row = tok & (kTile - 1);
-        float w = 0.f, o = 0.f;
-        if (tok < n_valid) {
-          float cprod = 1.f;   // product of the coefficients of the planes before this one
-          const int upto = r == 0 ? NRES : r - 1;
+        float cprod = pt;   // p times the coefficients of the planes before the current one
 #pragma unroll
-          for (int q = 0; q < NRES; ++q)
-            if (q < upto)
-              cprod *= bf16_bits_to_f32(*reinterpret_cast<const uint16_t*>(
-                  sub + 2 * C::A_TILE + (2 * q + 1) * C::R_TILE + C::R_CODES + C::META + row * 2));
-          const uint8_t* mp = r == 0 ? sub + C::A_TILE + C::A_CODES
-                                     : sub + 2 * C::A_TILE + (2 * (r - 1) + 1) * C::R_TILE + C::R_CODES;
-          const float2 mv = meta2(mp + row * NG * 2 + gi * 2);
-          const float pc = pt[k] * cprod;
-          w = pc * mv.x;
-          o = pc * mv.y;
+        for (int r = 0; r < NRES; ++r) {
+          const uint8_t* RV = sub + 2 * C::A_TILE + (2 * r + 1) * C::R_TILE;
+          const float2 mv = meta2(RV + C::R_CODES + row * NG * 2 + gi1 * 2);
+          wv[pp][1 + r] = cprod * mv.x;
+          off_part[1 + r] = fmaf(cprod, mv.y, off_part[1 + r]);
+          cprod *= bf16_bits_to_f32(*reinterpret_cast<const uint16_t*>(RV + C::R_CODES + C::META + row * 2));
         }
-        wv[k] = w;
-        osum += o;
-        mx = fmaxf(mx, fabsf(w));
+        const float2 ma = meta2(sub + C::A_TILE + C::A_CODES + row * NG * 2 + gi1 * 2);
+        wv[pp][0] = cprod * ma.x;
+        off_part[0] = fmaf(cprod, ma.y, off_part[0]);
       }
-      off_part[j] = fmaf(off_part[j], alpha, osum);
-      // |w| >= 0 compares like its bit pattern: one warp-wide integer max
-      mx = __uint_as_float(__reduce_max_sync(0xffffffffu, __float_as_uint(mx)));
-      const float inv = mx > 0.f ? kFix / mx : 0.f;
-      // two tokens' 16-bit fixed-point values per word: pv[h] = token lane+64h | token lane+64h+32 << 16
-      uint32_t pv[TPL / 2];
-#pragma unroll
-      for (int h = 0; h < TPL / 2; ++h)
-        pv[h] = ((uint32_t)to_fix(wv[2 * h], inv) & 0xFFFFu) | ((uint32_t)to_fix(wv[2 * h + 1], inv) << 16);
-      // each lane builds PACK/32 operand words; word idx covers tokens inside one 64-token half
-#pragma unroll
-      for (int h = 0; h < TPL / 2; ++h) {
-        const int idx = lane + 32 * h;
-        uint32_t word = 0;
-        if (r == 0) {
-          // anchor: idx = word w (0..15) x kind k: tokens 8w + 2i + (k >> 1), hi (k even) / lo byte
-          const int w8 = idx >> 2, k = idx & 3;
-#pragma unroll
-          for (int i = 0; i < 4; ++i) {
-            const int tk = 8 * w8 + 2 * i + (k >> 1);
-            const uint32_t x = __shfl_sync(0xffffffffu, pv[h], tk & 31);
-            const int v = (int)(int16_t)(x >> (16 * ((tk >> 5) & 1)));
-            word |= ((k & 1) ? fix_lo(v) : fix_hi(v)) << (8 * i);
-          }
-        } else {
-          // residual: idx = word j (0..7) x mask m (4) x part: tokens 16j + 4i + m
-          const int j8 = idx >> 3, m = (idx >> 1) & 3, part = idx & 1;
-#pragma unroll
-          for (int i = 0; i < 4; ++i) {
-            const int tk = 16 * j8 + 4 * i + m;
-            const uint32_t x = __shfl_sync(0xffffffffu, pv[h], tk & 31);
-            const int v = (int)(int16_t)(x >> (16 * ((tk >> 5) & 1)));
-            word |= (part ? fix_lo(v) : fix_hi(v)) << (8 * i);
-          }
-        }
-        pack_s[buf][item][idx] = word;
-      }
-      if (lane == 0) tau_s[buf][item] = mx / kFix;
     }
-    __syncthreads();                                   // B2: weight operands are in pack_s
+    // per-item max |w|: lanes of one group, then one shared atomic per warp and item
+    // (|w| >= 0 orders like its bit pattern)
+#pragma unroll
+    for (int j = 0; j <= NRES; ++j) {
+      float mx = 0.f;
+#pragma unroll
+      for (int pp = 0; pp < PPT; ++pp) mx = fmaxf(mx, fabsf(wv[pp][j]));
+      for (int off = NGP; off < 32; off <<= 1) mx = fmaxf(mx, __shfl_xor_sync(0xffffffffu, mx, off));
+      if (lane < NGP && g_ok) atomicMax(&tmax_s[buf][j * NG + gi1], __float_as_uint(mx));
+    }
+    __syncthreads();                                   // B2: per-item maxima are final
+    if (g_ok) {
+#pragma unroll
+      for (int j = 0; j <= NRES; ++j) {
+        const float mx = __uint_as_float(tmax_s[buf][j * NG + gi1]);
+        const float inv = mx > 0.f ? kFix / mx : 0.f;
+        uint8_t* wq = wq_s[j * NG + gi1];
+#pragma unroll
+        for (int pp = 0; pp < PPT; ++pp) {
+          const int tok = (tid + pp * kThreads) / NGP;
+          const int v = to_fix(wv[pp][j], inv);
+          wq[tok] = (uint8_t)fix_hi(v);
+          wq[UTOK + tok] = (uint8_t)fix_lo(v);
+        }
+      }
+    }
+    __syncthreads();                                   // B3: weight operands are in wq_s
 
     // ---- phase 2: value accumulation, thread = (channel, anchor | residual) ----
     if (p2_active) {
       const int gi = p2_ch / GS;
       float add = 0.f;
       if (p2_anchor) {
-        const uint32_t* pw = pack_s[buf][gi];
+        const uint8_t* wq = wq_s[gi];
         int eh = 0, el = 0, oh = 0, ol = 0;
 #pragma unroll
         for (int sb = 0; sb < C::UT; ++sb) {
@@ -639,24 +624,31 @@ __global__ void __launch_bounds__(kThreads, kCtasPerSm) decode_kernel(DecodeArgs
             const uint4 x4 = row[h2];
             const uint32_t xs[4] = {x4.x, x4.y, x4.z, x4.w};
 #pragma unroll
-            for (int q4 = 0; q4 < 4; ++q4) {
-              const int w = sb * 8 + h2 * 4 + q4;
-              const uint4 pk = *reinterpret_cast<const uint4*>(pw + 4 * w);
-              const uint32_t lo4 = xs[q4] & 0x0F0F0F0Fu, hi4 = xs[q4] & 0xF0F0F0F0u;
-              eh = dp4a_us(lo4, pk.x, eh);
-              el = dp4a_uu(lo4, pk.y, el);
-              oh = dp4a_us(hi4, pk.z, oh);
-              ol = dp4a_uu(hi4, pk.w, ol);
+            for (int q2 = 0; q2 < 2; ++q2) {
+              // code words w, w+1 hold tokens 8w .. 8w+15; the low nibbles of word w are
+              // tokens 8w .. 8w+3, the high nibbles 8w+4 .. 8w+7
+              const int w = sb * 8 + h2 * 4 + q2 * 2;
+              const uint4 wh = *reinterpret_cast<const uint4*>(wq + 8 * w);
+              const uint4 wl = *reinterpret_cast<const uint4*>(wq + UTOK + 8 * w);
+              const uint32_t a0 = xs[2 * q2], a1 = xs[2 * q2 + 1];
+              eh = dp4a_us(a0 & 0x0F0F0F0Fu, wh.x, eh);
+              el = dp4a_uu(a0 & 0x0F0F0F0Fu, wl.x, el);
+              oh = dp4a_us(a0 & 0xF0F0F0F0u, wh.y, oh);
+              ol = dp4a_uu(a0 & 0xF0F0F0F0u, wl.y, ol);
+              eh = dp4a_us(a1 & 0x0F0F0F0Fu, wh.z, eh);
+              el = dp4a_uu(a1 & 0x0F0F0F0Fu, wl.z, el);
+              oh = dp4a_us(a1 & 0xF0F0F0F0u, wh.w, oh);
+              ol = dp4a_uu(a1 & 0xF0F0F0F0u, wl.w, ol);
             }
           }
         }
         const int t = shl(shl(eh, 8) + el, 4) + shl(oh, 8) + ol;        // 16 x sum(w_fix * code)
-        add = (float)t * (tau_s[buf][gi] * (1.f / 16.f));
+        add = (float)t * (__uint_as_float(tmax_s[buf][gi]) * (1.f / (16.f * kFix)));
       } else {
 #pragma unroll
         for (int r = 0; r < NRES; ++r) {
           const int item = (1 + r) * NG + gi;
-          const uint32_t* pw = pack_s[buf][item];
+          const uint8_t* wq = wq_s[item];
           int hm[4] = {0, 0, 0, 0}, lm[4] = {0, 0, 0, 0};
 #pragma unroll
           for (int sb = 0; sb < C::UT; ++sb) {
@@ -665,26 +657,27 @@ __global__ void __launch_bounds__(kThreads, kCtasPerSm) decode_kernel(DecodeArgs
             const uint32_t xs[4] = {x4.x, x4.y, x4.z, x4.w};
 #pragma unroll
             for (int j = 0; j < 4; ++j) {
-              const int jw = sb * 4 + j;
-              const uint4 pa = *reinterpret_cast<const uint4*>(pw + 8 * jw);
-              const uint4 pb = *reinterpret_cast<const uint4*>(pw + 8 * jw + 4);
+              // word j: mask 3 << 2m leaves tokens 16j + 4m .. 16j + 4m + 3
+              const int t0 = sb * kTile + 16 * j;
+              const uint4 wh = *reinterpret_cast<const uint4*>(wq + t0);
+              const uint4 wl = *reinterpret_cast<const uint4*>(wq + UTOK + t0);
               const uint32_t b0 = xs[j] & 0x03030303u, b1 = xs[j] & 0x0C0C0C0Cu;
               const uint32_t b2 = xs[j] & 0x30303030u, b3 = xs[j] & 0xC0C0C0C0u;
-              hm[0] = dp4a_us(b0, pa.x, hm[0]); lm[0] = dp4a_uu(b0, pa.y, lm[0]);
-              hm[1] = dp4a_us(b1, pa.z, hm[1]); lm[1] = dp4a_uu(b1, pa.w, lm[1]);
-              hm[2] = dp4a_us(b2, pb.x, hm[2]); lm[2] = dp4a_uu(b2, pb.y, lm[2]);
-              hm[3] = dp4a_us(b3, pb.z, hm[3]); lm[3] = dp4a_uu(b3, pb.w, lm[3]);
+              hm[0] = dp4a_us(b0, wh.x, hm[0]); lm[0] = dp4a_uu(b0, wl.x, lm[0]);
+              hm[1] = dp4a_us(b1, wh.y, hm[1]); lm[1] = dp4a_uu(b1, wl.y, lm[1]);
+              hm[2] = dp4a_us(b2, wh.z, hm[2]); lm[2] = dp4a_uu(b2, wl.z, lm[2]);
+              hm[3] = dp4a_us(b3, wh.w, hm[3]); lm[3] = dp4a_uu(b3, wl.w, lm[3]);
             }
           }
           const int t = shl(shl(hm[0], 8) + lm[0], 6) + shl(shl(hm[1], 8) + lm[1], 4) +
                         shl(shl(hm[2], 8) + lm[2], 2) + (shl(hm[3], 8) + lm[3]);   // 64 x sum
-          add = fmaf((float)t, tau_s[buf][item] * (1.f / 64.f), add);
+          add = fmaf((float)t, __uint_as_float(tmax_s[buf][item]) * (1.f / (64.f * kFix)), add);
         }
       }
       acc = fmaf(acc, alpha, add);
     }
-    // no barrier here: the next unit's writes go to the other parity buffers, and its
-    // stage is refilled only after the next B1
+    // no barrier here: the next unit writes wq_s only after its B2 and clears this
+    // parity's maxima only after its B1, and its stage is refilled after the next B1
   }
 
   if (aborted) {

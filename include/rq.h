@@ -38,8 +38,12 @@
  *   K codes are token-major: row r = the token's d codes;
  *     INT4 byte i = ch 2i (bits 0-3) | ch 2i+1 (bits 4-7);
  *     INT2 byte i = ch 4i+m in bits 2m..2m+1.
- *   V codes are channel-major: row ch = that channel's 64 token codes;
- *     INT4 byte i = token 2i | token 2i+1 << 4; INT2 byte i = token 4i+m in bits 2m.
+ *   V codes are channel-major: row ch = that channel's 64 token codes in
+ *     32-bit words; INT4 word w (tokens 8w..8w+7): byte i = token 8w+i
+ *     (bits 0-3) | token 8w+4+i (bits 4-7); INT2 word j (tokens 16j..16j+15):
+ *     byte i holds token 16j+4m+i in bits 2m..2m+1, m = 0..3.  Masking a word
+ *     with 0x0F0F0F0F, 0xF0F0F0F0 or 0x03030303 << 2m leaves four consecutive
+ *     tokens, one per byte.
  *   meta row r: for each channel group, the E4M3 scale byte then the E4M3
  *     offset byte.  c slot r: BF16, little-endian.
  *   Every tile and sub-block size is a multiple of 16 bytes.

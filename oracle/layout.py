@@ -19,8 +19,11 @@ Codes of K planes are token-major: row r (64 rows) holds the token's d
   codes, 4-bit: byte i = ch 2i (bits 0-3) | ch 2i+1 (bits 4-7);
   2-bit: byte i = ch 4i+m at bits 2m..2m+1, m = 0..3.
 Codes of V planes are channel-major: row ch (d rows) holds the 64 tokens'
-  codes of that channel, 4-bit: byte i = token 2i | token 2i+1 << 4;
-  2-bit: byte i = token 4i+m at bits 2m.
+  codes of that channel in 32-bit words; 4-bit: word w (8 tokens) has in byte
+  i token 8w+i (bits 0-3) and token 8w+4+i (bits 4-7); 2-bit: word j (16
+  tokens) has in byte i token 16j+4m+i at bits 2m..2m+1, m = 0..3.  (Masking
+  a word with 0x0F0F0F0F, 0xF0F0F0F0 or 0x03030303 << 2m leaves four
+  consecutive tokens, one per byte.)
 Meta: row r holds, for each group i, the E4M3 scale byte then the E4M3
   offset byte.  c: BF16 little-endian, slot r.
 Every tile size is a multiple of 16 bytes (64 rows), so every tile, and
@@ -109,8 +112,12 @@ def _code_addresses(geom: Geometry, plane_base: int, tile_bytes: int, pos: np.nd
     ch = np.arange(d)
     if channel_major:
         row_bytes = TILE // per_byte
-        addr = tile_base[:, None] + ch[None, :] * row_bytes + (r[:, None] // per_byte)
-        shift = (r[:, None] % per_byte) * bits + 0 * ch[None, :]
+        tok_per_word = 4 * per_byte                      # 8 (INT4) or 16 (INT2) tokens per word
+        word, q = np.divmod(r, tok_per_word)
+        byte_in_row = 4 * word + (q % 4)                 # token q of a word sits in byte q mod 4
+        slot = q // 4                                    # ... in nibble / 2-bit field q div 4
+        addr = tile_base[:, None] + ch[None, :] * row_bytes + byte_in_row[:, None]
+        shift = (slot * bits)[:, None] + 0 * ch[None, :]
     else:
         row_bytes = d // per_byte
         addr = tile_base[:, None] + r[:, None] * row_bytes + ch[None, :] // per_byte

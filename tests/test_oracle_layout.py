@@ -84,15 +84,41 @@ def test_code_positions_in_bytes():
     buf[:] = 0
     addr, sh = Lo._code_addresses(geom, 0, geom.a_tile, np.array([5]), 4, channel_major=True)
     Lo._write_codes(buf, addr, sh, codes4, 4)
-    # channel-major: channel 1's row is bytes 32..63, token 5 -> byte 2, high nibble
-    assert buf[32 + 2] == 12 << 4 and buf[0 + 2] == 3 << 4 and buf[5 * 32 + 2] == 7 << 4
+    # channel-major: channel 1's row is bytes 32..63; token 5 is token 5 of word 0:
+    # byte 5 mod 4 = 1, high nibble
+    assert buf[32 + 1] == 12 << 4 and buf[0 + 1] == 3 << 4 and buf[5 * 32 + 1] == 7 << 4
     buf[:] = 0
     codes2 = np.zeros((1, 128), dtype=np.uint8)
     codes2[0, 6] = 2
     base = geom.res_plane(0, 1)
     addr, sh = Lo._code_addresses(geom, base, geom.r_tile, np.array([7]), 2, channel_major=True)
     Lo._write_codes(buf, addr, sh, codes2, 2)
-    assert buf[base + 6 * 16 + 1] == 2 << 6      # token 7: byte 1, bits 6-7
+    assert buf[base + 6 * 16 + 3] == 2 << 2      # token 7 of word 0: byte 3, bits 2-3
+
+
+@pytest.mark.parametrize("bits", [4, 2])
+def test_channel_major_masks_give_consecutive_tokens(bits):
+    """The documented V word order: each byte mask of a 32-bit word leaves four
+    consecutive tokens of the channel, token t0+i in byte i."""
+    geom = Lo.Geometry(1, 2, 1, 1, 128, 32, 1, 64)
+    rng = np.random.default_rng(3)
+    codes = rng.integers(0, 1 << bits, size=(64, 128), dtype=np.uint8)
+    buf = np.zeros(geom.total_bytes, dtype=np.uint8)
+    tile = geom.a_tile if bits == 4 else geom.r_tile
+    base = geom.anchor_plane(1) if bits == 4 else geom.res_plane(0, 1)
+    addr, sh = Lo._code_addresses(geom, base, tile, np.arange(64), bits, channel_major=True)
+    Lo._write_codes(buf, addr, sh, codes, bits)
+    row_bytes = 64 * bits // 8
+    masks = [0x0F0F0F0F, 0xF0F0F0F0] if bits == 4 else [0x03030303 << (2 * m) for m in range(4)]
+    for ch in (0, 1, 77, 127):
+        words = buf[base + ch * row_bytes: base + (ch + 1) * row_bytes].view("<u4")
+        t0 = 0
+        for w in words:
+            for k, mk in enumerate(masks):
+                got = [((int(w) & mk) >> (8 * i + k * bits)) & ((1 << bits) - 1) for i in range(4)]
+                assert got == list(codes[t0:t0 + 4, ch]), (ch, t0)
+                t0 += 4
+        assert t0 == 64
 
 
 @pytest.mark.parametrize("chained", [False, True])
