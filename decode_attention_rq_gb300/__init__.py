@@ -16,6 +16,7 @@ __all__ = [
     "rq_cache_bytes", "rq_cache_create", "rq_cache_destroy", "rq_append",
     "rq_decode_workspace_bytes", "rq_decode_attention", "rq_bf16_workspace_bytes",
     "rq_decode_attention_bf16", "rq_status_string", "EXPORTED_SYMBOLS",
+    "rq_decode_attention_noalloc", "RQ_NOALLOC_WORKSPACE_BYTES",
 ]
 
 LIB_PATH = os.path.join(os.path.dirname(os.path.abspath(__file__)), "librq.so")
@@ -29,8 +30,11 @@ _STATUS_NAMES = {0: "RQ_OK", 1: "RQ_ERR_INVALID_ARG", 2: "RQ_ERR_ALIGNMENT", 3: 
 EXPORTED_SYMBOLS = (
     "rq_cache_bytes", "rq_cache_create", "rq_cache_destroy", "rq_append",
     "rq_decode_workspace_bytes", "rq_decode_attention", "rq_bf16_workspace_bytes",
-    "rq_decode_attention_bf16", "rq_status_string",
+    "rq_decode_attention_bf16", "rq_status_string", "rq_decode_attention_noalloc",
 )
+
+# size of the workspace built into the library for rq_decode_attention_noalloc (rq.h)
+RQ_NOALLOC_WORKSPACE_BYTES = 2 * 1024 * 1024
 
 
 class RqError(RuntimeError):
@@ -63,6 +67,8 @@ lib.rq_decode_workspace_bytes.argtypes = [_cfgp, _i32]
 lib.rq_decode_workspace_bytes.restype = _sz
 lib.rq_decode_attention.argtypes = [_p, _i32, _i32, _i32, _i32, _p, _p, _p, _p, _f, _p, _p, _sz, _p]
 lib.rq_decode_attention.restype = ctypes.c_int
+lib.rq_decode_attention_noalloc.argtypes = [_p, _i32, _i32, _i32, _i32, _p, _p, _p, _p, _f, _p, _p, _p]
+lib.rq_decode_attention_noalloc.restype = ctypes.c_int
 lib.rq_bf16_workspace_bytes.argtypes = [_i32, _i32, _i32]
 lib.rq_bf16_workspace_bytes.restype = _sz
 lib.rq_decode_attention_bf16.argtypes = [_p, _p, _p, _p, _p, _p, _i32, _i32, _i32, _i32, _f, _p, _p, _sz, _p]
@@ -128,6 +134,16 @@ def rq_decode_attention(handle, layer, group, loop, batch, q, k_cur, v_cur, seq_
     _check("rq_decode_attention", lib.rq_decode_attention(
         handle, layer, group, loop, batch, _ptr(q), _ptr(k_cur), _ptr(v_cur), _ptr(seq_lens),
         softmax_scale, _ptr(out), _ptr(workspace), workspace_bytes, _stream(stream)))
+
+
+def rq_decode_attention_noalloc(handle, layer, group, loop, batch, q, k_cur, v_cur, seq_lens, softmax_scale,
+                                out, status=None, stream=None):
+    """rq_decode_attention without a caller workspace, for callers that cannot
+    allocate device memory: the scratch lives in a fixed array inside the library
+    (RQ_NOALLOC_WORKSPACE_BYTES).  Calls that overlap on the GPU race on it."""
+    _check("rq_decode_attention_noalloc", lib.rq_decode_attention_noalloc(
+        handle, layer, group, loop, batch, _ptr(q), _ptr(k_cur), _ptr(v_cur), _ptr(seq_lens),
+        softmax_scale, _ptr(out), _ptr(status), _stream(stream)))
 
 
 def rq_bf16_workspace_bytes(batch: int, num_heads: int, head_dim: int) -> int:

@@ -163,6 +163,39 @@ rq_status rq_decode_attention(rq_cache* cache, int32_t layer, int32_t group, int
                               const int32_t* seq_lens, float softmax_scale, float* out,
                               void* workspace, size_t workspace_bytes, void* stream);
 
+/* Size of the workspace built into the library for rq_decode_attention_noalloc
+ * (2 MiB of device memory, held on every device that loads the library until
+ * the process exits).  With 152 SMs and head_dim 128 it covers
+ * batch * num_heads up to about 1700 (row, head) pairs. */
+#define RQ_NOALLOC_WORKSPACE_BYTES (2u * 1024u * 1024u)
+
+/* rq_decode_attention for callers that cannot allocate device memory.
+ * The paper has no counterpart to this entry point.  Some callers are handed
+ * their buffers and may not allocate more: a plugin whose host application
+ * owns all device memory, a process under a memory budget fixed up front,
+ * or a path on which an allocation could block or fail.  This call takes
+ * the same arguments as rq_decode_attention, less the workspace, and
+ * performs no device allocation: its scratch (status word, merge counters,
+ * split-K partials) lives in one array of RQ_NOALLOC_WORKSPACE_BYTES inside
+ * the library.
+ *   status   device int32[4] or NULL: receives the call's status word (as
+ *            under rq_decode_workspace_bytes) on `stream` after the kernel.
+ * The first call on a device looks up the array's device address (once per
+ * device, with that device current); make that first call before any
+ * stream capture.  Each call clears the part of the array it uses on
+ * `stream` before its kernel, then runs the same kernel as
+ * rq_decode_attention.  All calls share the one array: calls that overlap
+ * on the GPU (other streams, other host threads) race and give wrong
+ * results, so serialize them.
+ * Errors: as rq_decode_attention; WORKSPACE when the call needs more than
+ * RQ_NOALLOC_WORKSPACE_BYTES (too many rows x heads for the built-in array;
+ * use rq_decode_attention with a workspace of rq_decode_workspace_bytes). */
+rq_status rq_decode_attention_noalloc(rq_cache* cache, int32_t layer, int32_t group,
+                                      int32_t loop, int32_t batch, const void* q,
+                                      const void* k_cur, const void* v_cur,
+                                      const int32_t* seq_lens, float softmax_scale, float* out,
+                                      int32_t* status, void* stream);
+
 /* Workspace (device bytes) for rq_decode_attention_bf16; same zero-once rule. */
 size_t rq_bf16_workspace_bytes(int32_t batch, int32_t num_heads, int32_t head_dim);
 
