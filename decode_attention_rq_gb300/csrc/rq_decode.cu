@@ -8,34 +8,39 @@
 // chained one reads every residual between the loop and the anchor.
 //
 // GB300 design
-//   * Work units are (row, head, 64-token tile).  A fixed grid of
+//   * Three kernels per call.  qprep_kernel (one CTA per (row, head)) applies
+//     R to the query and turns q and R q into the fixed-point packs the
+//     scoring uses.  decode_kernel streams the cache and writes one partial
+//     softmax state per (CTA, segment).  merge_kernel (one CTA per (row,
+//     head)) combines the partials, adds the current BF16 token, applies R^T
+//     once and writes the output.  decode_kernel and merge_kernel are
+//     launched as programmatic dependents of the kernel before them: their
+//     prologues (work split, first cache copies; R staged in shared memory)
+//     overlap that kernel, and each waits for it (griddepcontrol.wait) only
+//     before reading what it wrote.
+//   * Work units are (row, head, 128 tokens).  A fixed grid of
 //     num_SMs x kCtasPerSm CTAs takes equal contiguous ranges of the flattened
 //     unit list (ranges cross (row, head) boundaries), so every SM streams
 //     the same number of tiles whatever the batch and lengths.
-//   * A tile's plane slices (anchor K/V, the residual K/V planes this loop
+//   * A unit's plane slices (anchor K/V, the residual K/V planes this loop
 //     reads) are contiguous and 16-byte aligned: one thread issues 1-D TMA
 //     bulk copies into a shared-memory ring tracked by mbarriers (bounded
 //     waits); all other threads only compute.
 //   * Scores use the rotated query: q.(c a_hat + R^T r_hat) = c (q.a_hat) +
-//     (R q).r_hat.  R is applied to q once per (row, head) segment; the value
-//     side accumulates the anchor part and the rotated residual part apart,
-//     and R^T is applied once, at the merge.
+//     (R q).r_hat.  The value side accumulates the anchor part and the
+//     rotated residual part apart; R^T is applied once, in the merge.
 //   * Per group, q.x_hat = s * sum(q * code) + o * sum(q), and the value side
-//     keeps the offsets as one scalar per (tile, group): the work per code is
+//     keeps the offsets as one scalar per (unit, group): the work per code is
 //     one multiply-add against a small integer.
 //   * That multiply-add runs on the integer dot-product unit: the query (per
-//     group) and the softmax-times-scale weights (per tile and group) are
+//     group) and the softmax-times-scale weights (per unit and group) are
 //     taken to 16-bit fixed point as two int8 parts; dp4a sums 4 code x part
 //     products exactly.  Byte masks put the codes straight into dp4a operands:
 //     K rows are token-major (4 codes of one token per operand), V rows are
-//     channel-major (4 tokens of one channel per operand), so no shifts are
-//     needed.  The masks and the dot products run on separate pipes of the
-//     SM and overlap.
-//   * Online softmax in base 2 (scale * log2(e) folded into q).  Each CTA
-//     writes one partial (m, l, acc_anchor, acc_residual) per segment; the
-//     last CTA to finish a (row, head) -- an atomic counter, no spinning --
-//     merges the partials, adds the current BF16 token, applies R^T and
-//     writes the output.
+//     channel-major (4 consecutive tokens of one channel per operand), so no
+//     shifts are needed.  The masks and the dot products run on separate
+//     pipes of the SM and overlap.
+//   * Online softmax in base 2 (scale * log2(e) folded into q).
 #include <cuda_fp8.h>
 
 #include "rq_internal.cuh"
@@ -49,6 +54,10 @@ constexpr int kMaxRows = 256;          // batch rows one call may cover
 constexpr int kMaxRes = 3;             // residual planes one call may read (chained, 4 loops)
 constexpr float kLog2e = 1.4426950408889634f;
 constexpr float kFix = 32767.f;        // 16-bit fixed point: values in [-32767, 32767]
+constexpr int kPackWords = 36;         // query pack per (row, head, group): anchor 16, residual 16, 4 scalars
+constexpr int kPrepThreads = 256;
+constexpr int kMergeThreads = 256;
+constexpr int kMaxContrib = 1024;      // decode CTAs one merge can combine (the grid is smaller)
 
 struct DecodeArgs {
   Geom g;
@@ -60,8 +69,8 @@ struct DecodeArgs {
   const int32_t* seq_lens;
   float* out;
   int32_t* status;
-  int32_t* counters;     // [batch * H]
-  float* partials;       // [(C + batch*H)][pstride]
+  float* partials;       // [(C + batch*H)][pstride]: (m, l, acc_anchor[d], acc_residual[d])
+  uint32_t* packs;       // [batch*H][NG][kPackWords]
   int pstride;
   int layer, group, batch, res0;   // res0: first residual plane this loop reads
   float qscale;                    // softmax_scale * log2(e)
@@ -88,6 +97,14 @@ __device__ __forceinline__ int to_fix(float x, float inv) {
 __device__ __forceinline__ float2 meta2(const uint8_t* p) {   // (scale, offset)
   return e4m3x2_to_f32x2(*reinterpret_cast<const uint16_t*>(p));
 }
+// Programmatic dependent launch: let the next kernel of the stream start its
+// prologue; wait until the kernel before this one has finished and its writes
+// are visible (returns at once when launched without the dependency).
+__device__ __forceinline__ void pdl_launch_dependents() {
+  asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
+}
+__device__ __forceinline__ void pdl_wait() { asm volatile("griddepcontrol.wait;" ::: "memory"); }
+__device__ __forceinline__ int clamp_len(int n, int nmax) { return n < 0 ? 0 : (n > nmax ? nmax : n); }
 
 // Balanced split of U units over C CTAs: CTA c takes [start(c), start(c+1)) with
 // start(c) = c*q + min(c, rem), q = U / C, rem = U % C (32-bit arithmetic only).
@@ -123,6 +140,95 @@ struct Cfg {
   static constexpr int SMEM = STAGES * STAGE;
 };
 
+// Query packs of one (row, head): for each group, the 16-bit fixed-point query
+// as int8 (hi, lo) parts laid out as the dp4a operands of the scoring, their
+// scales and sums.  Words of pack (bh, group):
+//   [4w + k], w < GS/8        anchor word w: k = 0 even-channel hi, 1 even lo,
+//                             2 odd hi, 3 odd lo (channels 8w + 2i (+1), i = byte)
+//   [16 + 8w + 2m + p]        residual word w, 2-bit field m: p = 0 hi, 1 lo
+//                             (channels 16w + 4i + m, i = byte)
+//   [32..35]                  sig_a, sum(q), sig_r, sum(R q) of the group (float bits)
+template <int D, int GS, int NRES>
+__global__ void __launch_bounds__(kPrepThreads) qprep_kernel(DecodeArgs a) {
+  constexpr int NG = D / GS, NV = D / 8;   // NV: float4 loads per half row of R
+  __shared__ __align__(16) float q_s[D];
+  __shared__ float qr_s[D];
+  __shared__ __align__(16) uint32_t img_s[NG * kPackWords];   // the packs of this (row, head)
+  pdl_launch_dependents();
+  const int bh = blockIdx.x, tid = threadIdx.x;
+  // R rows first (they do not depend on q): two threads per row, all loads in flight
+  const int row = tid >> 1, half = tid & 1;
+  float4 rv[NRES > 0 ? NV : 1];
+  if (NRES > 0 && row < D) {
+    const float4* rp = reinterpret_cast<const float4*>(a.R + (size_t)row * D + half * (D / 2));
+#pragma unroll
+    for (int v = 0; v < NV; ++v) rv[v] = __ldg(rp + v);
+  }
+  if (tid < D) q_s[tid] = __bfloat162float(a.q[(size_t)bh * D + tid]) * a.qscale;
+  for (int i = tid; i < NG * kPackWords; i += kPrepThreads) img_s[i] = 0u;
+  __syncthreads();
+  if (NRES > 0) {   // (R q)[row]: the two halves of the row, then one sum
+    float qr = 0.f;
+    if (row < D) {
+      const float4* qp = reinterpret_cast<const float4*>(q_s + half * (D / 2));
+#pragma unroll
+      for (int v = 0; v < NV; ++v) {
+        const float4 x = qp[v];
+        qr = fmaf(rv[v].x, x.x, fmaf(rv[v].y, x.y, fmaf(rv[v].z, x.z, fmaf(rv[v].w, x.w, qr))));
+      }
+    }
+    qr += __shfl_xor_sync(0xffffffffu, qr, 1);
+    if (row < D && half == 0) qr_s[row] = qr;
+    __syncthreads();
+  }
+  // Each pack byte is written by the thread of its channel: thread k < D holds
+  // channel k of q and of R q.  A group's GS channels sit in GS consecutive lanes
+  // of one warp, so group maxima and sums are lane reductions.
+  uint8_t* img = reinterpret_cast<uint8_t*>(img_s);
+  if (tid < D) {
+    const int k = tid, gi = k / GS, j = k % GS;
+    const float x = q_s[k];
+    float mx = fabsf(x), s1 = x;
+#pragma unroll
+    for (int off = GS / 2; off > 0; off >>= 1) {
+      mx = fmaxf(mx, __shfl_xor_sync(0xffffffffu, mx, off));
+      s1 += __shfl_xor_sync(0xffffffffu, s1, off);
+    }
+    const int v = to_fix(x, mx > 0.f ? kFix / mx : 0.f);
+    const int w = j >> 3, i = (j & 7) >> 1, odd = j & 1;
+    uint8_t* wb = img + 4 * (gi * kPackWords + 4 * w + 2 * odd) + i;
+    wb[0] = (uint8_t)fix_hi(v);
+    wb[4] = (uint8_t)fix_lo(v);
+    if (j == 0) {
+      img_s[gi * kPackWords + 32] = __float_as_uint(mx / (kFix * 16.f));   // anchor sums carry 16
+      img_s[gi * kPackWords + 33] = __float_as_uint(s1);
+    }
+  }
+  if (NRES > 0 && tid < D) {
+    const int k = tid, gi = k / GS, j = k % GS;
+    const float x = qr_s[k];
+    float mr = fabsf(x), s2 = x;
+#pragma unroll
+    for (int off = GS / 2; off > 0; off >>= 1) {
+      mr = fmaxf(mr, __shfl_xor_sync(0xffffffffu, mr, off));
+      s2 += __shfl_xor_sync(0xffffffffu, s2, off);
+    }
+    const int v = to_fix(x, mr > 0.f ? kFix / mr : 0.f);
+    const int w = j >> 4, i = (j & 15) >> 2, m = j & 3;
+    uint8_t* wb = img + 4 * (gi * kPackWords + 16 + 8 * w + 2 * m) + i;
+    wb[0] = (uint8_t)fix_hi(v);
+    wb[4] = (uint8_t)fix_lo(v);
+    if (j == 0) {
+      img_s[gi * kPackWords + 34] = __float_as_uint(mr / (kFix * 64.f));   // residual sums carry 64
+      img_s[gi * kPackWords + 35] = __float_as_uint(s2);
+    }
+  }
+  __syncthreads();
+  uint4* dst = reinterpret_cast<uint4*>(a.packs + (size_t)bh * NG * kPackWords);
+  const uint4* src = reinterpret_cast<const uint4*>(img_s);
+  for (int i = tid; i < NG * kPackWords / 4; i += kPrepThreads) dst[i] = src[i];
+}
+
 template <int D, int GS, int NRES>
 __global__ void __launch_bounds__(kThreads, kCtasPerSm) decode_kernel(DecodeArgs a) {
   using C = Cfg<D, GS, NRES>;
@@ -133,8 +239,6 @@ __global__ void __launch_bounds__(kThreads, kCtasPerSm) decode_kernel(DecodeArgs
   __shared__ int pre_s[kMaxRows + 1];
   __shared__ int nt_s[kMaxRows + 1];        // work units (128-token) per row; then a sentinel
   __shared__ int sl_s[kMaxRows];
-  __shared__ __align__(16) float q_s[D];
-  __shared__ __align__(16) float qr_s[D];
   // per-unit scratch; the first two are double-buffered by unit parity
   __shared__ float red_s[2][kThreads / 32];        // per-warp score maxima
   __shared__ uint32_t tmax_s[2][NITEM];            // max |value weight| per item, float bits
@@ -144,19 +248,15 @@ __global__ void __launch_bounds__(kThreads, kCtasPerSm) decode_kernel(DecodeArgs
   __shared__ __align__(16) uint8_t wq_s[NITEM][WQ];
   __shared__ float wsum_s[kThreads / 32][NITEM + 1];   // per-warp partials of off_s
   __shared__ float off_s[NITEM + 1];               // per-segment offset sums; [NITEM] = softmax sum
-  __shared__ float mrg_s[8];
-  __shared__ float rt_s[D];
-  __shared__ float m_sh, l_sh;
-  __shared__ int flag_s;
 
+  pdl_launch_dependents();   // the merge kernel may start staging R
   const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
   const int H = a.g.H, B = a.batch;
   const int Cn = gridDim.x, cta = blockIdx.x;
 
   // ---- per-row unit counts and prefix over (row, head) ----
   for (int b = tid; b < B; b += kThreads) {
-    int n = a.seq_lens[b];
-    n = n < 0 ? 0 : (n > a.g.Nmax ? a.g.Nmax : n);
+    const int n = clamp_len(a.seq_lens[b], a.g.Nmax);
     sl_s[b] = n;
     nt_s[b] = (n + UTOK - 1) / UTOK;
   }
@@ -173,13 +273,7 @@ __global__ void __launch_bounds__(kThreads, kCtasPerSm) decode_kernel(DecodeArgs
   __syncthreads();
   const int U = pre_s[B];
 
-  // ---- (row, head) pairs with an empty cache: the output is the current V ----
-  for (int bh = cta; bh < B * H; bh += Cn) {
-    if (nt_s[bh / H] != 0) continue;
-    for (int k = tid; k < D; k += kThreads)
-      a.out[(size_t)bh * D + k] = __bfloat162float(a.v_cur[(size_t)bh * D + k]);
-  }
-  if (U == 0) return;
+  if (U == 0) return;   // every row empty: the merge kernel writes the current V
   const Split split{U / Cn, U % Cn};
   const int u0 = split.start(cta), u1 = split.start(cta + 1);
   if (u0 >= u1) return;
@@ -237,6 +331,7 @@ __global__ void __launch_bounds__(kThreads, kCtasPerSm) decode_kernel(DecodeArgs
   if (tid == 0)
     for (int s = 0; s < STAGES && u0 + s < u1; ++s) issue(s);
   Cursor cc = locate(u0);   // consumer cursor
+  pdl_wait();               // the query packs of qprep_kernel are complete
 
   // ---- per-thread state ----
   const int gi1 = tid % NGP;              // phase-1 group of this thread (same for every pair)
@@ -281,7 +376,7 @@ __global__ void __launch_bounds__(kThreads, kCtasPerSm) decode_kernel(DecodeArgs
       off_s[i] = x;
     }
     __syncthreads();
-    // write this CTA's partial for bh, then the last CTA merges
+    // this CTA's partial for bh; merge_kernel combines the partials
     float* part = a.partials + (size_t)(cta + bh) * a.pstride;
     if (tid == 0) {
       part[0] = m_run;
@@ -298,151 +393,39 @@ __global__ void __launch_bounds__(kThreads, kCtasPerSm) decode_kernel(DecodeArgs
       }
       part[2 + (p2_anchor ? 0 : D) + p2_ch] = v;
     }
-    __threadfence();
-    __syncthreads();
-    const int b = bh / H, h = bh % H;
-    const int s0 = pre_s[b] + h * nt_s[b];
-    const int s1 = s0 + nt_s[b];
-    // contributors: the CTAs owning units s0 .. s1-1 (every CTA in between owns at least
-    // one of them, as ranges are contiguous and cover every unit)
-    const int c_lo = split.owner(s0), c_hi = split.owner(s1 - 1);
-    if (tid == 0) {
-      int prev = atomicAdd(&a.counters[bh], 1);
-      flag_s = (prev == c_hi - c_lo);
-    }
-    __syncthreads();
-    if (!flag_s) return;
-    __threadfence();
-    // ---- merge (this CTA is the last one for bh) ----
-    float sc = 0.f;
-    for (int k = tid; k < D; k += kThreads) sc += q_s[k] * __bfloat162float(a.k_cur[(size_t)bh * D + k]);
-    for (int off = 16; off > 0; off >>= 1) sc += __shfl_xor_sync(0xffffffffu, sc, off);
-    if (lane == 0) mrg_s[warp] = sc;
-    __syncthreads();
-    if (tid == 0) {
-      float s_cur = 0.f;
-      for (int w = 0; w < kThreads / 32; ++w) s_cur += mrg_s[w];
-      float M = s_cur;
-      for (int c = c_lo; c <= c_hi; ++c) M = fmaxf(M, __ldcg(a.partials + (size_t)(c + bh) * a.pstride));
-      float L = exp2f(s_cur - M);
-      for (int c = c_lo; c <= c_hi; ++c) {
-        const float* pc2 = a.partials + (size_t)(c + bh) * a.pstride;
-        L += __ldcg(pc2 + 1) * exp2f(__ldcg(pc2) - M);
-      }
-      m_sh = M;
-      l_sh = L;
-      mrg_s[0] = s_cur;
-    }
-    __syncthreads();
-    const float M = m_sh, L = l_sh, s_cur = mrg_s[0];
-    if (tid < D) {
-      float va = 0.f, vr = 0.f;
-      for (int c = c_lo; c <= c_hi; ++c) {
-        const float* pc2 = a.partials + (size_t)(c + bh) * a.pstride;
-        float w = exp2f(__ldcg(pc2) - M);
-        va = fmaf(w, __ldcg(pc2 + 2 + tid), va);
-        if (NRES > 0) vr = fmaf(w, __ldcg(pc2 + 2 + D + tid), vr);
-      }
-      va = fmaf(exp2f(s_cur - M), __bfloat162float(a.v_cur[(size_t)bh * D + tid]), va);
-      if (NRES > 0) qr_s[tid] = vr;
-      q_s[tid] = va;
-    }
-    __syncthreads();
-    if (NRES > 0) {
-      // (R^T acc_r)[c]: thread = (column c, half of the rows); loads coalesced over c,
-      // issued 16 at a time
-      const int c = tid % D, hh = tid / D;
-      float t = 0.f;
-      if (tid < 2 * D) {
-        const float* rc = a.R + (size_t)hh * (D / 2) * D + c;
-        const float* ar = qr_s + hh * (D / 2);
-#pragma unroll 16
-        for (int k = 0; k < D / 2; ++k) t = fmaf(__ldg(rc + (size_t)k * D), ar[k], t);
-        if (hh == 1) rt_s[c] = t;
-      }
-      __syncthreads();
-      if (tid < D) a.out[(size_t)bh * D + c] = (q_s[c] + t + rt_s[c]) / L;
-    } else if (tid < D) {
-      a.out[(size_t)bh * D + tid] = q_s[tid] / L;
-    }
-    if (tid == 0) a.counters[bh] = 0;
-    __syncthreads();
   };
 
   auto begin_segment = [&](int bh) {
-    for (int k = tid; k < D; k += kThreads) q_s[k] = __bfloat162float(a.q[(size_t)bh * D + k]) * a.qscale;
-    __syncthreads();
-    if (NRES > 0) {
-      // q' = R q: two threads per row, each with all its row loads in flight at once
-      constexpr int NV = D / 8;                 // float4 loads per half row
-      const int i = tid >> 1, hh = tid & 1;
-      float t = 0.f;
-      if (i < D) {
-        const float4* rp = reinterpret_cast<const float4*>(a.R + (size_t)i * D + hh * (D / 2));
-        const float4* qp = reinterpret_cast<const float4*>(q_s + hh * (D / 2));
-        float4 rv[NV];
-#pragma unroll
-        for (int v = 0; v < NV; ++v) rv[v] = __ldg(rp + v);
-#pragma unroll
-        for (int v = 0; v < NV; ++v) {
-          const float4 qv = qp[v];
-          t = fmaf(rv[v].x, qv.x, fmaf(rv[v].y, qv.y, fmaf(rv[v].z, qv.z, fmaf(rv[v].w, qv.w, t))));
-        }
-      }
-      t += __shfl_xor_sync(0xffffffffu, t, 1);
-      if (i < D && hh == 0) qr_s[i] = t;
-      __syncthreads();
-    }
-    // fixed-point packs of this thread's phase-1 group
+    // this thread's group's query packs (written by qprep_kernel; read through L2)
     const int gq = g_ok ? gi1 : 0;
-    {
-      const float* qg = q_s + gq * GS;
-      float mx = 0.f, s1 = 0.f;
+    const uint4* pk = reinterpret_cast<const uint4*>(a.packs + ((size_t)bh * NG + gq) * kPackWords);
+    uint32_t w[kPackWords];
 #pragma unroll
-      for (int k = 0; k < GS; ++k) { mx = fmaxf(mx, fabsf(qg[k])); s1 += qg[k]; }
-      const float inv = mx > 0.f ? kFix / mx : 0.f;
-      sig_a = mx / (kFix * 16.f);              // anchor sums carry a factor 16
-      qsum = s1;
+    for (int i = 0; i < kPackWords / 4; ++i) {
+      const uint4 v = __ldcg(pk + i);
+      w[4 * i] = v.x; w[4 * i + 1] = v.y; w[4 * i + 2] = v.z; w[4 * i + 3] = v.w;
+    }
 #pragma unroll
-      for (int w = 0; w < AW; ++w) {
-        uint32_t eh = 0, el = 0, oh = 0, ol = 0;
+    for (int x = 0; x < AW; ++x)
 #pragma unroll
-        for (int i = 0; i < 4; ++i) {
-          int ve = to_fix(qg[8 * w + 2 * i], inv), vo = to_fix(qg[8 * w + 2 * i + 1], inv);
-          eh |= fix_hi(ve) << (8 * i); el |= fix_lo(ve) << (8 * i);
-          oh |= fix_hi(vo) << (8 * i); ol |= fix_lo(vo) << (8 * i);
-        }
-        qa[w][0] = eh; qa[w][1] = el; qa[w][2] = oh; qa[w][3] = ol;
+      for (int k = 0; k < 4; ++k) qa[x][k] = w[4 * x + k];
+#pragma unroll
+    for (int x = 0; x < RW; ++x)
+#pragma unroll
+      for (int m = 0; m < 4; ++m) {
+        qrp[x][m][0] = w[16 + 8 * x + 2 * m];
+        qrp[x][m][1] = w[16 + 8 * x + 2 * m + 1];
       }
-    }
-    if (NRES > 0) {
-      const float* rg = qr_s + gq * GS;
-      float mr = 0.f, s2 = 0.f;
-#pragma unroll
-      for (int k = 0; k < GS; ++k) { mr = fmaxf(mr, fabsf(rg[k])); s2 += rg[k]; }
-      const float invr = mr > 0.f ? kFix / mr : 0.f;
-      sig_r = mr / (kFix * 64.f);            // residual sums carry a factor 64
-      qrsum = s2;
-#pragma unroll
-      for (int w = 0; w < RW; ++w)
-#pragma unroll
-        for (int m = 0; m < 4; ++m) {
-          uint32_t hh = 0, ll = 0;
-#pragma unroll
-          for (int i = 0; i < 4; ++i) {
-            int v = to_fix(rg[16 * w + 4 * i + m], invr);
-            hh |= fix_hi(v) << (8 * i); ll |= fix_lo(v) << (8 * i);
-          }
-          qrp[w][m][0] = hh; qrp[w][m][1] = ll;
-        }
-    }
+    sig_a = __uint_as_float(w[32]);
+    qsum = __uint_as_float(w[33]);
+    sig_r = __uint_as_float(w[34]);
+    qrsum = __uint_as_float(w[35]);
     m_run = -INFINITY;
     l_part = 0.f;
 #pragma unroll
     for (int j = 0; j <= NRES; ++j) off_part[j] = 0.f;
     acc = 0.f;
     cur_bh = bh;
-    __syncthreads();   // q_s / qr_s may be rewritten by the next merge only after all packs are read
   };
 
   for (int u = u0; u < u1; ++u, advance(cc)) {
@@ -692,18 +675,159 @@ __global__ void __launch_bounds__(kThreads, kCtasPerSm) decode_kernel(DecodeArgs
   if (cur_bh >= 0) flush(cur_bh);
 }
 
+// Combines the partial softmax states of (row, head) blockIdx.x: the CTAs that
+// held its units are recomputed from seq_lens with the decode kernel's split.
+template <int D, int NRES>
+__global__ void __launch_bounds__(kMergeThreads) merge_kernel(DecodeArgs a, int Cn) {
+  extern __shared__ __align__(16) float R_s[];   // [D][D] when NRES > 0
+  __shared__ float w_s[kMaxContrib];
+  __shared__ float l_s[kMaxContrib];
+  __shared__ float va_s[D];
+  __shared__ float vr_s[D];
+  __shared__ float redf_s[kMergeThreads / 32];
+  __shared__ int redi_s[2][kMergeThreads / 32];
+  __shared__ float ml_s[2];
+  __shared__ uint64_t r_bar;
+  constexpr int UTOK = 2 * kTile;
+  const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
+  const int bh = blockIdx.x, H = a.g.H, B = a.batch, b = bh / H, h = bh - b * H;
+
+  // ---- before the wait: inputs the decode kernel does not write ----
+  if (NRES > 0 && tid == 0) {   // R -> shared memory, one bulk copy (R is 16-byte aligned)
+    mbar_init(&r_bar, 1);
+    fence_mbar_init();
+    mbar_arrive_expect_tx(&r_bar, (uint32_t)(D * D * sizeof(float)));
+    bulk_g2s(R_s, a.R, (uint32_t)(D * D * sizeof(float)), &r_bar);
+  }
+  // current token's score (base 2)
+  float sc = 0.f;
+  for (int k = tid; k < D; k += kMergeThreads)
+    sc += __bfloat162float(a.q[(size_t)bh * D + k]) * a.qscale *
+          __bfloat162float(a.k_cur[(size_t)bh * D + k]);
+  // units before this row and in total (same clamping and unit size as the decode kernel)
+  int before = 0, total = 0;
+  for (int r = tid; r < B; r += kMergeThreads) {
+    const int nt = (clamp_len(a.seq_lens[r], a.g.Nmax) + UTOK - 1) / UTOK;
+    total += H * nt;
+    if (r < b) before += H * nt;
+  }
+  for (int off = 16; off > 0; off >>= 1) {
+    sc += __shfl_xor_sync(0xffffffffu, sc, off);
+    before += __shfl_xor_sync(0xffffffffu, before, off);
+    total += __shfl_xor_sync(0xffffffffu, total, off);
+  }
+  if (lane == 0) { redf_s[warp] = sc; redi_s[0][warp] = before; redi_s[1][warp] = total; }
+  __syncthreads();
+  float s_cur = 0.f;
+  int pre = 0, U = 0;
+#pragma unroll
+  for (int w = 0; w < kMergeThreads / 32; ++w) { s_cur += redf_s[w]; pre += redi_s[0][w]; U += redi_s[1][w]; }
+  const int ntb = (clamp_len(a.seq_lens[b], a.g.Nmax) + UTOK - 1) / UTOK;
+  if (ntb == 0) {   // empty cache: attention over the current token alone
+    for (int k = tid; k < D; k += kMergeThreads)
+      a.out[(size_t)bh * D + k] = __bfloat162float(a.v_cur[(size_t)bh * D + k]);
+    if (NRES > 0) (void)mbar_wait_bounded(&r_bar, 0);   // the R copy lands before the CTA exits
+    return;
+  }
+  const Split split{U / Cn, U % Cn};
+  const int s0 = pre + h * ntb, s1 = s0 + ntb;
+  const int c_lo = split.owner(s0), c_hi = split.owner(s1 - 1);
+  const int nc = min(c_hi - c_lo + 1, kMaxContrib);
+
+  pdl_wait();   // every partial of the decode kernel is written and visible
+
+  if (warp == 0) {
+    // (m, l) of each contributor, read once: m parked in w_s, l in l_s
+    float M = s_cur;
+    for (int i = lane; i < nc; i += 32) {
+      const float2 ml = __ldcg(reinterpret_cast<const float2*>(a.partials + (size_t)(c_lo + i + bh) * a.pstride));
+      w_s[i] = ml.x;
+      l_s[i] = ml.y;
+      M = fmaxf(M, ml.x);
+    }
+    for (int off = 16; off > 0; off >>= 1) M = fmaxf(M, __shfl_xor_sync(0xffffffffu, M, off));
+    float L = 0.f;
+    for (int i = lane; i < nc; i += 32) {
+      const float w = exp2f(w_s[i] - M);
+      w_s[i] = w;
+      L = fmaf(w, l_s[i], L);
+    }
+    for (int off = 16; off > 0; off >>= 1) L += __shfl_xor_sync(0xffffffffu, L, off);
+    if (lane == 0) { ml_s[0] = M; ml_s[1] = L + exp2f(s_cur - M); }
+  }
+  __syncthreads();
+  const float M = ml_s[0], L = ml_s[1];
+  // thread = (channel, anchor | residual accumulator)
+  if (tid < (NRES > 0 ? 2 * D : D)) {
+    const float* pc = a.partials + (size_t)(c_lo + bh) * a.pstride + 2 + tid;
+    float v = 0.f;
+    int i = 0;
+    for (; i + 8 <= nc; i += 8) {   // eight loads in flight
+      float x[8];
+#pragma unroll
+      for (int k = 0; k < 8; ++k) x[k] = __ldcg(pc + (size_t)(i + k) * a.pstride);
+#pragma unroll
+      for (int k = 0; k < 8; ++k) v = fmaf(w_s[i + k], x[k], v);
+    }
+    for (; i < nc; ++i) v = fmaf(w_s[i], __ldcg(pc + (size_t)i * a.pstride), v);
+    if (tid < D) va_s[tid] = fmaf(exp2f(s_cur - M), __bfloat162float(a.v_cur[(size_t)bh * D + tid]), v);
+    else vr_s[tid - D] = v;
+  }
+  __syncthreads();
+  // R in shared memory (waited on by every thread; bounded, a timeout sets the status word)
+  if (NRES > 0 && !mbar_wait_bounded(&r_bar, 0)) {
+    if (tid == 0) atomicExch(&a.status[0], 1);
+    return;
+  }
+  if (tid < D) {
+    float o = va_s[tid];
+    if (NRES > 0) {   // + (R^T acc_r)[tid]
+      float t = 0.f;
+#pragma unroll 8
+      for (int k = 0; k < D; ++k) t = fmaf(R_s[k * D + tid], vr_s[k], t);
+      o += t;
+    }
+    a.out[(size_t)bh * D + tid] = o / L;
+  }
+}
+
+template <typename... Args>
+cudaError_t launch_dependent(void (*k)(Args...), dim3 grid, dim3 block, size_t smem,
+                             cudaStream_t stream, Args... args) {
+  cudaLaunchConfig_t cfg = {};
+  cfg.gridDim = grid;
+  cfg.blockDim = block;
+  cfg.dynamicSmemBytes = smem;
+  cfg.stream = stream;
+  cudaLaunchAttribute attr[1];
+  attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+  attr[0].val.programmaticStreamSerializationAllowed = 1;
+  cfg.attrs = attr;
+  cfg.numAttrs = 1;
+  return cudaLaunchKernelEx(&cfg, k, args...);
+}
+
 template <int D, int GS, int NRES>
 cudaError_t launch_t(const DecodeArgs& a, int grid, cudaStream_t stream) {
   using C = Cfg<D, GS, NRES>;
   auto k = decode_kernel<D, GS, NRES>;
+  auto km = merge_kernel<D, (NRES > 0 ? 1 : 0)>;
+  constexpr size_t merge_smem = NRES > 0 ? (size_t)D * D * sizeof(float) : 0;
   static bool attr_set = false;
   if (!attr_set) {
     cudaError_t e = cudaFuncSetAttribute(k, cudaFuncAttributeMaxDynamicSharedMemorySize, C::SMEM);
     if (e != cudaSuccess) return e;
+    e = cudaFuncSetAttribute(km, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)merge_smem);
+    if (e != cudaSuccess) return e;
     attr_set = true;
   }
-  k<<<grid, kThreads, C::SMEM, stream>>>(a);
-  return cudaGetLastError();
+  const int bhs = a.batch * a.g.H;
+  qprep_kernel<D, GS, NRES><<<bhs, kPrepThreads, 0, stream>>>(a);
+  cudaError_t e = cudaGetLastError();
+  if (e != cudaSuccess) return e;
+  e = launch_dependent(k, dim3(grid), dim3(kThreads), (size_t)C::SMEM, stream, a);
+  if (e != cudaSuccess) return e;
+  return launch_dependent(km, dim3(bhs), dim3(kMergeThreads), merge_smem, stream, a, grid);
 }
 
 template <int D, int GS>
@@ -723,11 +847,15 @@ int pstride_for(int d) { return ((2 + 2 * d) + 3) / 4 * 4; }
 
 int decode_max_chained_loops() { return kMaxRes + 1; }
 
+// Workspace: status word (256 B slot) | partials (C + batch*H) x pstride floats | query packs.
+static size_t partials_bytes(const Geom& g, int batch, int num_sms) {
+  const size_t C = (size_t)num_sms * kCtasPerSm, bh = (size_t)batch * g.H;
+  return ((C + bh) * pstride_for(g.d) * sizeof(float) + 255) / 256 * 256;
+}
+
 size_t decode_workspace_bytes(const Geom& g, int batch, int num_sms) {
-  size_t C = (size_t)num_sms * kCtasPerSm;
-  size_t bh = (size_t)batch * g.H;
-  size_t counters = (bh * 4 + 255) / 256 * 256;
-  return 256 + counters + (C + bh) * pstride_for(g.d) * sizeof(float);
+  const size_t bh = (size_t)batch * g.H;
+  return 256 + partials_bytes(g, batch, num_sms) + bh * g.ng * kPackWords * sizeof(uint32_t);
 }
 
 cudaError_t launch_decode(const rq_cache& c, int layer, int group, int loop, int batch,
@@ -750,9 +878,8 @@ cudaError_t launch_decode(const rq_cache& c, int layer, int group, int loop, int
   a.out = out;
   uint8_t* ws = static_cast<uint8_t*>(workspace);
   a.status = reinterpret_cast<int32_t*>(ws);
-  a.counters = reinterpret_cast<int32_t*>(ws + 256);
-  size_t bh = (size_t)batch * c.geom.H;
-  a.partials = reinterpret_cast<float*>(ws + 256 + (bh * 4 + 255) / 256 * 256);
+  a.partials = reinterpret_cast<float*>(ws + 256);
+  a.packs = reinterpret_cast<uint32_t*>(ws + 256 + partials_bytes(c.geom, batch, c.num_sms));
   a.pstride = pstride_for(c.geom.d);
   a.layer = layer;
   a.group = group;
@@ -760,6 +887,7 @@ cudaError_t launch_decode(const rq_cache& c, int layer, int group, int loop, int
   a.res0 = loop;
   a.qscale = scale * kLog2e;
   const int grid = c.num_sms * kCtasPerSm;
+  if (grid > kMaxContrib) return cudaErrorNotSupported;   // merge_kernel's contributor table
   const int d = c.geom.d, gs = c.geom.g;
   if (d == 128 && gs == 32) return launch_d<128, 32>(a, grid, nres, stream);
   if (d == 128 && gs == 16) return launch_d<128, 16>(a, grid, nres, stream);

@@ -6,8 +6,8 @@
 // plugins whose host application owns all device memory, code that runs
 // under a fixed memory budget reserved up front, or code on a path where an
 // allocation could block or fail.  Such a caller still passes the inputs and
-// the output; the split-K workspace (status word, per-(row, head) merge
-// counters, per-CTA partial softmax states) lives in one file-scope device
+// the output; the split-K workspace (status word, per-CTA partial softmax
+// states, query packs) lives in one file-scope device
 // array of RQ_NOALLOC_WORKSPACE_BYTES.  Every device on which this library is
 // loaded holds that array until the process exits.
 //
@@ -18,8 +18,8 @@
 // on the first call made with that device current, and passed to the kernel.
 //
 // Every call shares the array and finds in it what the last call left.  A
-// call clears the part it uses (the counters and the status word must start
-// at zero) on its own stream before launching, so calls that overlap on the
+// call clears the part it uses (the status word must start at zero) on its
+// own stream before launching, so calls that overlap on the
 // GPU -- two streams, or two threads -- race on the array and give wrong
 // results: serialize them.
 #include <mutex>
@@ -80,8 +80,8 @@ extern "C" rq_status rq_decode_attention_noalloc(rq_cache* cache, int32_t layer,
   void* ws = nullptr;
   if (noalloc_workspace(&ws) != cudaSuccess) return RQ_ERR_CUDA;
   cudaStream_t st = static_cast<cudaStream_t>(stream);
-  // the status word and the merge counters must start at zero; clearing the whole
-  // extent this call uses also drops whatever an earlier, aborted call left behind
+  // the status word must start at zero; clearing the whole extent this call uses
+  // also drops whatever an earlier, aborted call left behind
   if (cudaMemsetAsync(ws, 0, need, st) != cudaSuccess) return RQ_ERR_CUDA;
   cudaError_t e = launch_decode(*cache, layer, group, loop, batch,
                                 static_cast<const __nv_bfloat16*>(q),

@@ -135,7 +135,7 @@ rq_status rq_append(rq_cache* cache, int32_t layer, int32_t group, int32_t batch
 
 /* Workspace (device bytes) one rq_decode_attention call needs for `batch` rows
  * on the current device.  The workspace must be zero-filled once before its
- * first use; every call leaves its counters at zero again.  Its first 16 bytes
+ * first use (the status word must start at zero).  Its first 16 bytes
  * are the status word (int32[4]): [0] != 0 after a device-side wait timed out,
  * [1] != 0 after an append skipped a row that would overflow. */
 size_t rq_decode_workspace_bytes(const rq_config* cfg, int32_t batch);
@@ -152,7 +152,8 @@ size_t rq_decode_workspace_bytes(const rq_config* cfg, int32_t batch);
  *   out            device float32 [batch][H][d]
  *   workspace      device, >= rq_decode_workspace_bytes(cfg, batch), zeroed once
  * Split-K over the sequence: each CTA of a balanced grid streams its range of
- * tiles; the last CTA to finish a (row, head) merges the partial softmax
+ * tiles into one partial softmax state per (CTA, row, head); a merge kernel
+ * then combines the partial softmax
  * states, adds the current token and applies R^T once.
  * Chained mode reads the anchor and every residual plane from this loop to
  * the anchor; decode supports it for loops_per_group <= 4 (UNSUPPORTED beyond).
@@ -165,8 +166,8 @@ rq_status rq_decode_attention(rq_cache* cache, int32_t layer, int32_t group, int
 
 /* Size of the workspace built into the library for rq_decode_attention_noalloc
  * (2 MiB of device memory, held on every device that loads the library until
- * the process exits).  With 152 SMs and head_dim 128 it covers
- * batch * num_heads up to about 1700 (row, head) pairs. */
+ * the process exits).  With 152 SMs, head_dim 128 and group size 32 it
+ * covers batch * num_heads up to about 1100 (row, head) pairs. */
 #define RQ_NOALLOC_WORKSPACE_BYTES (2u * 1024u * 1024u)
 
 /* rq_decode_attention for callers that cannot allocate device memory.
@@ -175,8 +176,8 @@ rq_status rq_decode_attention(rq_cache* cache, int32_t layer, int32_t group, int
  * owns all device memory, a process under a memory budget fixed up front,
  * or a path on which an allocation could block or fail.  This call takes
  * the same arguments as rq_decode_attention, less the workspace, and
- * performs no device allocation: its scratch (status word, merge counters,
- * split-K partials) lives in one array of RQ_NOALLOC_WORKSPACE_BYTES inside
+ * performs no device allocation: its scratch (status word, split-K
+ * partials, query packs) lives in one array of RQ_NOALLOC_WORKSPACE_BYTES inside
  * the library.
  *   status   device int32[4] or NULL: receives the call's status word (as
  *            under rq_decode_workspace_bytes) on `stream` after the kernel.
