@@ -219,11 +219,14 @@ def main():
     ap.add_argument("--no-e2e", action="store_true")
     ap.add_argument("--ref-budget", type=float, default=2.0)
     ap.add_argument("--quiet", action="store_true")
+    ap.add_argument("--layers", type=int, default=None,
+                    help="fewer layers than the workload (a small case for profiler captures)")
     args = ap.parse_args()
     w = synth.WORKLOADS[args.workload]
-    if args.batch or args.group_size:
+    if args.batch or args.group_size or args.layers:
         import dataclasses
-        w = dataclasses.replace(w, batch=args.batch or w.batch, group_size=args.group_size or w.group_size)
+        w = dataclasses.replace(w, batch=args.batch or w.batch, group_size=args.group_size or w.group_size,
+                                num_layers=args.layers or w.num_layers)
     if args.impl == "reference":
         run_reference(args, w)
         return
@@ -284,7 +287,7 @@ def run_rq(args, w):
             if lp == P - 1:
                 rq.rq_append(handle, layer, grp, B, t, seq, 1, status, stream)
 
-    launches_per_step = ncalls + L * G
+    launches_per_step = 3 * ncalls + L * G   # a decode call is qprep + decode + merge kernels
     s = torch.cuda.Stream(device=dev)
     torch.cuda.synchronize()
     with torch.cuda.stream(s):
@@ -324,7 +327,7 @@ def run_rq(args, w):
     if st.any():
         raise RuntimeError(f"device status word reports an error: {st.tolist()}")
 
-    # per-launch duration of the dominant kernel (decode split-K), CUDA events on its stream
+    # duration of one decode call (its three kernels; decode_kernel dominates), CUDA events on its stream
     dur = []
     ev = [torch.cuda.Event(enable_timing=True) for _ in range(2 * ncalls)]
     with torch.cuda.stream(s):
@@ -364,7 +367,7 @@ def run_rq(args, w):
         "effective_gbps": step_gbs, "frac_of_hbm_peak": step_gbs / peak,
         "roofline": {"bound": "hbm", "achieved": achieved, "peak": peak, "unit": "GB/s",
                      "frac": achieved / peak, "traffic": traffic,
-                     "kernel": "rq decode split-K (decode_kernel)",
+                     "kernel": "rq_decode_attention call (qprep_kernel + decode_kernel + merge_kernel)",
                      "peak_source": f"MEASURED_PEAKS.json hbm_gbs ({peak_kind})",
                      "avg_launch_ms": avg_launch_ms, "bytes_per_launch": per_launch_bytes},
         "gpu_launches": launches_per_step * args.steps,

@@ -15,8 +15,12 @@
 // rotation itself (d x d per vector) runs in float32 FMA.
 //
 // Grid: x = aligned block of 16 positions of one row, y = row * H + head,
-// z = K/V.  A channel-major V word holds 8 (INT4) or 16 (INT2) aligned
-// positions, so the words a CTA rewrites are touched by no other CTA.
+// z = K/V (and, for short appends in shared mode, the residual loop: the
+// loops are coded independently against the anchor, so each CTA takes one
+// and requantizes the anchor as its reference; only loop 0's CTA writes the
+// anchor plane).  A channel-major V word holds 8 (INT4) or 16 (INT2)
+// aligned positions, so the words a CTA rewrites are touched by no other CTA
+// that writes the same plane.
 #include <cuda_fp8.h>
 
 #include "rq_internal.cuh"
@@ -177,16 +181,21 @@ __device__ void write_plane(const AppendArgs& a, uint8_t* plane, int64_t tile_by
 }
 
 // u[t][i] = sum_k R[i][k] e[t][k] for the first NT token slots; thread = output
-// channel i; the sum runs k = 0..d-1 as a chain of float32 fused multiply-adds.
-template <int NT>
-__device__ __forceinline__ void rotate_rows(const float* R, int d, int i, const float (*e)[128],
+// channel i; the sum runs k = 0..D-1 as a chain of float32 fused multiply-adds.
+// The row of R is loaded first, all of it in flight.
+template <int NT, int D>
+__device__ __forceinline__ void rotate_rows(const float* R, int i, const float (*e)[128],
                                             float (*u)[128]) {
   float acc[NT];
 #pragma unroll
   for (int t = 0; t < NT; ++t) acc[t] = 0.f;
-  const float4* Rrow = reinterpret_cast<const float4*>(R + (size_t)i * d);
-  for (int k4 = 0; k4 < d / 4; ++k4) {
-    float4 r = __ldg(Rrow + k4);
+  const float4* Rrow = reinterpret_cast<const float4*>(R + (size_t)i * D);
+  float4 rr[D / 4];
+#pragma unroll
+  for (int k4 = 0; k4 < D / 4; ++k4) rr[k4] = __ldg(Rrow + k4);
+#pragma unroll
+  for (int k4 = 0; k4 < D / 4; ++k4) {
+    const float4 r = rr[k4];
 #pragma unroll
     for (int t = 0; t < NT; ++t) {
       float4 x = *reinterpret_cast<const float4*>(&e[t][4 * k4]);
@@ -200,9 +209,13 @@ __device__ __forceinline__ void rotate_rows(const float* R, int d, int i, const 
   for (int t = 0; t < NT; ++t) u[t][i] = acc[t];
 }
 
+template <int D>
 __global__ void __launch_bounds__(kThreads) append_kernel(AppendArgs a) {
-  const int d = a.g.d, gs = a.g.g, P = a.g.P, tid = threadIdx.x;
-  const int b = blockIdx.y / a.g.H, h = blockIdx.y % a.g.H, kvi = blockIdx.z;
+  constexpr int d = D;
+  const int gs = a.g.g, P = a.g.P, tid = threadIdx.x;
+  const int b = blockIdx.y / a.g.H, h = blockIdx.y % a.g.H;
+  const int kvi = blockIdx.z & 1, jz = blockIdx.z >> 1;
+  const bool split = gridDim.z > 2;   // this CTA codes residual loop jz only
   const bool chained = a.g.mode == RQ_MODE_CHAINED;
 
   __shared__ float ref_s[kTok][128];     // anchor_hat (shared) or rebuilt loop l+1 (chained)
@@ -216,7 +229,7 @@ __global__ void __launch_bounds__(kThreads) append_kernel(AppendArgs a) {
 
   const int start = a.seq_lens[b];
   if (start < 0 || start + a.n > a.g.Nmax) {
-    if (blockIdx.x == 0 && h == 0 && kvi == 0 && tid == 0 && a.status) atomicExch(&a.status[1], 1);
+    if (blockIdx.x == 0 && h == 0 && blockIdx.z == 0 && tid == 0 && a.status) atomicExch(&a.status[1], 1);
     return;
   }
   const int blk = start / kTok + blockIdx.x;
@@ -240,6 +253,9 @@ __global__ void __launch_bounds__(kThreads) append_kernel(AppendArgs a) {
   const int t4 = t_lo & ~3;   // t_lo < kTok: the block holds at least one appended position
   const bool few = t_hi < t4 + 4;
   const bool act = tid < d;
+  if (split && act)   // this CTA's loop, loaded together with the anchor below
+    for (int t = 0; t < kTok; ++t)
+      x_s[t][tid] = valid_s[t] ? load_x(a, jz, kvi, b, h, p0 + t - start, tid) : 0.f;
 
   // ---- anchor: loop P-1, 4-bit (slots outside the appended range are skipped) ----
   for (int t = 0; t < kTok; ++t) {
@@ -255,13 +271,15 @@ __global__ void __launch_bounds__(kThreads) append_kernel(AppendArgs a) {
     }
   }
   __syncthreads();
-  write_plane(a, region + a.g.anchor_plane(kvi), a.g.a_tile, a.g.a_codes, 4, kvi == 1, p0, valid_s,
-              codes_s, meta_s, nullptr);
+  if (!split || jz == 0)
+    write_plane(a, region + a.g.anchor_plane(kvi), a.g.a_tile, a.g.a_codes, 4, kvi == 1, p0, valid_s,
+                codes_s, meta_s, nullptr);
   __syncthreads();
 
   // ---- earlier loops: shared mode any order; chained from P-2 down ----
   for (int j = P - 2; j >= 0; --j) {
-    if (act)
+    if (split && j != jz) continue;   // uniform over the CTA
+    if (act && !split)
       for (int t = 0; t < kTok; ++t)
         x_s[t][tid] = valid_s[t] ? load_x(a, j, kvi, b, h, p0 + t - start, tid) : 0.f;
     __syncthreads();
@@ -296,8 +314,8 @@ __global__ void __launch_bounds__(kThreads) append_kernel(AppendArgs a) {
     __syncthreads();
     // rotation u = R e, thread = output channel, sequential FMA over k
     if (act) {
-      if (few) rotate_rows<4>(a.R, d, tid, x_s + t4, u_s + t4);
-      else rotate_rows<kTok>(a.R, d, tid, x_s, u_s);
+      if (few) rotate_rows<4, D>(a.R, tid, x_s + t4, u_s + t4);
+      else rotate_rows<kTok, D>(a.R, tid, x_s, u_s);
     }
     __syncthreads();
     // 2-bit quantization of u
@@ -354,9 +372,13 @@ cudaError_t launch_append(const rq_cache& c, int layer, int group, int batch,
   a.group = group;
   a.batch = batch;
   a.n = n_tokens;
-  // aligned 16-position blocks touched by n tokens starting anywhere: at most ceil(n/16) + 1
-  dim3 grid((n_tokens + kTok - 1) / kTok + 1, batch * c.geom.H, 2);
-  append_kernel<<<grid, kThreads, 0, stream>>>(a);
+  // aligned 16-position blocks touched by n tokens starting anywhere: at most ceil(n/16) + 1;
+  // a short append in shared mode takes one CTA per (K/V, residual loop)
+  const bool split = c.geom.mode == RQ_MODE_SHARED && c.geom.P > 1 && n_tokens <= kTok;
+  dim3 grid((n_tokens + kTok - 1) / kTok + 1, batch * c.geom.H, split ? 2 * (c.geom.P - 1) : 2);
+  if (c.geom.d == 128) append_kernel<128><<<grid, kThreads, 0, stream>>>(a);
+  else if (c.geom.d == 96) append_kernel<96><<<grid, kThreads, 0, stream>>>(a);
+  else return cudaErrorNotSupported;
   return cudaGetLastError();
 }
 

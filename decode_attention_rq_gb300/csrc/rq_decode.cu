@@ -19,7 +19,7 @@
 //     overlap that kernel, and each waits for it (griddepcontrol.wait) only
 //     before reading what it wrote.
 //   * Work units are (row, head, 128 tokens).  A fixed grid of
-//     num_SMs x kCtasPerSm CTAs takes equal contiguous ranges of the flattened
+//     num_SMs x (CTAs resident per SM) takes equal contiguous ranges of the flattened
 //     unit list (ranges cross (row, head) boundaries), so every SM streams
 //     the same number of tiles whatever the batch and lengths.
 //   * A unit's plane slices (anchor K/V, the residual K/V planes this loop
@@ -49,7 +49,7 @@ namespace rq {
 namespace {
 
 constexpr int kThreads = 256;
-constexpr int kCtasPerSm = 2;
+constexpr int kMaxCtasPerSm = 3;     // the workspace holds partials for this many CTAs per SM
 constexpr int kMaxRows = 256;          // batch rows one call may cover
 constexpr int kMaxRes = 3;             // residual planes one call may read (chained, 4 loops)
 constexpr float kLog2e = 1.4426950408889634f;
@@ -131,7 +131,10 @@ struct Cfg {
   static constexpr int UT = 2;                                    // layout tiles per work unit
   static constexpr int UTOK = UT * kTile;                         // tokens per work unit
   static constexpr int STAGE = UT * SUB;
-  static constexpr int STAGES = NRES >= 2 ? 2 : 3;
+  static constexpr int STAGES = 2;
+  // CTAs per SM: three (24 warps) while the registers allow it; the chained
+  // variants with more residual planes keep two
+  static constexpr int MINB = NRES <= 1 ? 3 : 2;
   static constexpr int PPT = UTOK * NGP / kThreads;               // (token, group) pairs per thread
   static constexpr int AW = GS / 8;              // 32-bit words of INT4 codes per (token, group)
   static constexpr int RW = GS / 16;             // 32-bit words of INT2 codes per (token, group)
@@ -154,9 +157,9 @@ __global__ void __launch_bounds__(kPrepThreads) qprep_kernel(DecodeArgs a) {
   __shared__ __align__(16) float q_s[D];
   __shared__ float qr_s[D];
   __shared__ __align__(16) uint32_t img_s[NG * kPackWords];   // the packs of this (row, head)
-  pdl_launch_dependents();
   const int bh = blockIdx.x, tid = threadIdx.x;
-  // R rows first (they do not depend on q): two threads per row, all loads in flight
+  // R rows first (R stays unchanged while the cache is used): two threads per row,
+  // all loads in flight, before waiting for the kernel ahead of this one
   const int row = tid >> 1, half = tid & 1;
   float4 rv[NRES > 0 ? NV : 1];
   if (NRES > 0 && row < D) {
@@ -164,6 +167,13 @@ __global__ void __launch_bounds__(kPrepThreads) qprep_kernel(DecodeArgs a) {
 #pragma unroll
     for (int v = 0; v < NV; ++v) rv[v] = __ldg(rp + v);
   }
+  // Launched as a programmatic dependent of whatever precedes the call on the
+  // stream: everything else read here (q) or written (the packs, which the
+  // previous call's decode kernel may still read) waits for that kernel.  The
+  // decode kernel is released only after this wait, so its own early reads
+  // (seq_lens, the cache) also follow it.
+  pdl_wait();
+  pdl_launch_dependents();
   if (tid < D) q_s[tid] = __bfloat162float(a.q[(size_t)bh * D + tid]) * a.qscale;
   for (int i = tid; i < NG * kPackWords; i += kPrepThreads) img_s[i] = 0u;
   __syncthreads();
@@ -230,7 +240,7 @@ __global__ void __launch_bounds__(kPrepThreads) qprep_kernel(DecodeArgs a) {
 }
 
 template <int D, int GS, int NRES>
-__global__ void __launch_bounds__(kThreads, kCtasPerSm) decode_kernel(DecodeArgs a) {
+__global__ void __launch_bounds__(kThreads, (Cfg<D, GS, NRES>::MINB)) decode_kernel(DecodeArgs a) {
   using C = Cfg<D, GS, NRES>;
   constexpr int NG = C::NG, NGP = C::NGP, AW = C::AW, RW = C::RW, STAGES = C::STAGES;
   constexpr int NITEM = C::NITEM, UTOK = C::UTOK, PPT = C::PPT, WQ = C::WQ;
@@ -299,6 +309,7 @@ __global__ void __launch_bounds__(kThreads, kCtasPerSm) decode_kernel(DecodeArgs
     }
   };
   Cursor pc = locate(u0);   // producer cursor (thread 0 only)
+  const uint64_t pol = l2_evict_first_policy();   // the cache is read once per call
   auto issue = [&](int stage) {
     const uint8_t* region = a.base + a.g.region_offset(a.layer, a.group, pc.b, pc.h);
     const int t0 = pc.t * C::UT;
@@ -309,14 +320,16 @@ __global__ void __launch_bounds__(kThreads, kCtasPerSm) decode_kernel(DecodeArgs
     for (int k = 0; k < ntile; ++k) {
       uint8_t* d = dst + k * C::SUB;
       const int64_t tile = t0 + k;
-      bulk_g2s(d, region + a.g.anchor_plane(0) + tile * C::A_TILE, C::A_TILE, &full_bar[stage]);
-      bulk_g2s(d + C::A_TILE, region + a.g.anchor_plane(1) + tile * C::A_TILE, C::A_TILE, &full_bar[stage]);
+      bulk_g2s_hint(d, region + a.g.anchor_plane(0) + tile * C::A_TILE, C::A_TILE, &full_bar[stage], pol);
+      bulk_g2s_hint(d + C::A_TILE, region + a.g.anchor_plane(1) + tile * C::A_TILE, C::A_TILE, &full_bar[stage],
+                    pol);
 #pragma unroll
       for (int r = 0; r < NRES; ++r) {
         uint8_t* d0 = d + 2 * C::A_TILE + 2 * r * C::R_TILE;
-        bulk_g2s(d0, region + a.g.res_plane(a.res0 + r, 0) + tile * C::R_TILE, C::R_TILE, &full_bar[stage]);
-        bulk_g2s(d0 + C::R_TILE, region + a.g.res_plane(a.res0 + r, 1) + tile * C::R_TILE, C::R_TILE,
-                 &full_bar[stage]);
+        bulk_g2s_hint(d0, region + a.g.res_plane(a.res0 + r, 0) + tile * C::R_TILE, C::R_TILE, &full_bar[stage],
+                      pol);
+        bulk_g2s_hint(d0 + C::R_TILE, region + a.g.res_plane(a.res0 + r, 1) + tile * C::R_TILE, C::R_TILE,
+                      &full_bar[stage], pol);
       }
     }
     advance(pc);
@@ -684,11 +697,13 @@ __global__ void __launch_bounds__(kMergeThreads) merge_kernel(DecodeArgs a, int 
   __shared__ float l_s[kMaxContrib];
   __shared__ float va_s[D];
   __shared__ float vr_s[D];
+  __shared__ float rt_s[D];
   __shared__ float redf_s[kMergeThreads / 32];
   __shared__ int redi_s[2][kMergeThreads / 32];
   __shared__ float ml_s[2];
   __shared__ uint64_t r_bar;
   constexpr int UTOK = 2 * kTile;
+  pdl_launch_dependents();   // the next call's prep may start loading R; it waits for this kernel
   const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
   const int bh = blockIdx.x, H = a.g.H, B = a.batch, b = bh / H, h = bh - b * H;
 
@@ -736,6 +751,14 @@ __global__ void __launch_bounds__(kMergeThreads) merge_kernel(DecodeArgs a, int 
 
   pdl_wait();   // every partial of the decode kernel is written and visible
 
+  // this thread's element of the first contributors' accumulators, loaded while
+  // warp 0 reads the (m, l) pairs
+  constexpr int PF = 8;
+  const bool acc_thread = tid < (NRES > 0 ? 2 * D : D);
+  const float* pc = a.partials + (size_t)(c_lo + bh) * a.pstride + 2 + tid;
+  float xa[PF];
+#pragma unroll
+  for (int k = 0; k < PF; ++k) xa[k] = (acc_thread && k < nc) ? __ldcg(pc + (size_t)k * a.pstride) : 0.f;
   if (warp == 0) {
     // (m, l) of each contributor, read once: m parked in w_s, l in l_s
     float M = s_cur;
@@ -758,37 +781,44 @@ __global__ void __launch_bounds__(kMergeThreads) merge_kernel(DecodeArgs a, int 
   __syncthreads();
   const float M = ml_s[0], L = ml_s[1];
   // thread = (channel, anchor | residual accumulator)
-  if (tid < (NRES > 0 ? 2 * D : D)) {
-    const float* pc = a.partials + (size_t)(c_lo + bh) * a.pstride + 2 + tid;
+  if (acc_thread) {
     float v = 0.f;
-    int i = 0;
-    for (; i + 8 <= nc; i += 8) {   // eight loads in flight
-      float x[8];
 #pragma unroll
-      for (int k = 0; k < 8; ++k) x[k] = __ldcg(pc + (size_t)(i + k) * a.pstride);
-#pragma unroll
-      for (int k = 0; k < 8; ++k) v = fmaf(w_s[i + k], x[k], v);
-    }
-    for (; i < nc; ++i) v = fmaf(w_s[i], __ldcg(pc + (size_t)i * a.pstride), v);
+    for (int k = 0; k < PF; ++k)
+      if (k < nc) v = fmaf(w_s[k], xa[k], v);
+    for (int i = PF; i < nc; ++i) v = fmaf(w_s[i], __ldcg(pc + (size_t)i * a.pstride), v);
     if (tid < D) va_s[tid] = fmaf(exp2f(s_cur - M), __bfloat162float(a.v_cur[(size_t)bh * D + tid]), v);
     else vr_s[tid - D] = v;
   }
   __syncthreads();
-  // R in shared memory (waited on by every thread; bounded, a timeout sets the status word)
-  if (NRES > 0 && !mbar_wait_bounded(&r_bar, 0)) {
-    if (tid == 0) atomicExch(&a.status[0], 1);
-    return;
-  }
-  if (tid < D) {
-    float o = va_s[tid];
-    if (NRES > 0) {   // + (R^T acc_r)[tid]
-      float t = 0.f;
-#pragma unroll 8
-      for (int k = 0; k < D; ++k) t = fmaf(R_s[k * D + tid], vr_s[k], t);
-      o += t;
+  float o = 0.f;
+  if (NRES > 0) {
+    // R in shared memory (bounded wait; a timeout sets the status word, decided for the CTA)
+    const bool ok = mbar_wait_bounded(&r_bar, 0);
+    if (__syncthreads_or(!ok)) {
+      if (tid == 0) atomicExch(&a.status[0], 1);
+      return;
     }
-    a.out[(size_t)bh * D + tid] = o / L;
+    // (R^T acc_r)[c]: thread = (column c, half of the rows), four accumulator chains
+    if (tid < 2 * D) {
+      const int c = tid % D, hh = tid / D;
+      const float* rc = R_s + (size_t)hh * (D / 2) * D + c;
+      const float* vr = vr_s + hh * (D / 2);
+      float t0 = 0.f, t1 = 0.f, t2 = 0.f, t3 = 0.f;
+#pragma unroll 4
+      for (int k = 0; k < D / 2; k += 4) {
+        t0 = fmaf(rc[(k + 0) * D], vr[k + 0], t0);
+        t1 = fmaf(rc[(k + 1) * D], vr[k + 1], t1);
+        t2 = fmaf(rc[(k + 2) * D], vr[k + 2], t2);
+        t3 = fmaf(rc[(k + 3) * D], vr[k + 3], t3);
+      }
+      o = (t0 + t1) + (t2 + t3);
+      if (hh == 1) rt_s[c] = o;
+    }
+    __syncthreads();
+    if (tid < D) o += rt_s[tid];
   }
+  if (tid < D) a.out[(size_t)bh * D + tid] = (va_s[tid] + o) / L;
 }
 
 template <typename... Args>
@@ -808,22 +838,27 @@ cudaError_t launch_dependent(void (*k)(Args...), dim3 grid, dim3 block, size_t s
 }
 
 template <int D, int GS, int NRES>
-cudaError_t launch_t(const DecodeArgs& a, int grid, cudaStream_t stream) {
+cudaError_t launch_t(const DecodeArgs& a, int num_sms, cudaStream_t stream) {
   using C = Cfg<D, GS, NRES>;
   auto k = decode_kernel<D, GS, NRES>;
   auto km = merge_kernel<D, (NRES > 0 ? 1 : 0)>;
   constexpr size_t merge_smem = NRES > 0 ? (size_t)D * D * sizeof(float) : 0;
-  static bool attr_set = false;
-  if (!attr_set) {
+  static int per_sm = 0;   // resident decode CTAs per SM (registers and shared memory)
+  if (per_sm == 0) {
     cudaError_t e = cudaFuncSetAttribute(k, cudaFuncAttributeMaxDynamicSharedMemorySize, C::SMEM);
     if (e != cudaSuccess) return e;
     e = cudaFuncSetAttribute(km, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)merge_smem);
     if (e != cudaSuccess) return e;
-    attr_set = true;
+    int occ = 0;
+    e = cudaOccupancyMaxActiveBlocksPerMultiprocessor(&occ, k, kThreads, C::SMEM);
+    if (e != cudaSuccess) return e;
+    if (occ < 1) return cudaErrorNotSupported;
+    per_sm = occ < C::MINB ? occ : C::MINB;
   }
+  const int grid = num_sms * per_sm;
+  if (grid > kMaxContrib) return cudaErrorNotSupported;   // merge_kernel's contributor table
   const int bhs = a.batch * a.g.H;
-  qprep_kernel<D, GS, NRES><<<bhs, kPrepThreads, 0, stream>>>(a);
-  cudaError_t e = cudaGetLastError();
+  cudaError_t e = launch_dependent(qprep_kernel<D, GS, NRES>, dim3(bhs), dim3(kPrepThreads), 0, stream, a);
   if (e != cudaSuccess) return e;
   e = launch_dependent(k, dim3(grid), dim3(kThreads), (size_t)C::SMEM, stream, a);
   if (e != cudaSuccess) return e;
@@ -831,12 +866,12 @@ cudaError_t launch_t(const DecodeArgs& a, int grid, cudaStream_t stream) {
 }
 
 template <int D, int GS>
-cudaError_t launch_d(const DecodeArgs& a, int grid, int nres, cudaStream_t stream) {
+cudaError_t launch_d(const DecodeArgs& a, int num_sms, int nres, cudaStream_t stream) {
   switch (nres) {
-    case 0: return launch_t<D, GS, 0>(a, grid, stream);
-    case 1: return launch_t<D, GS, 1>(a, grid, stream);
-    case 2: return launch_t<D, GS, 2>(a, grid, stream);
-    case 3: return launch_t<D, GS, 3>(a, grid, stream);
+    case 0: return launch_t<D, GS, 0>(a, num_sms, stream);
+    case 1: return launch_t<D, GS, 1>(a, num_sms, stream);
+    case 2: return launch_t<D, GS, 2>(a, num_sms, stream);
+    case 3: return launch_t<D, GS, 3>(a, num_sms, stream);
   }
   return cudaErrorNotSupported;
 }
@@ -849,7 +884,7 @@ int decode_max_chained_loops() { return kMaxRes + 1; }
 
 // Workspace: status word (256 B slot) | partials (C + batch*H) x pstride floats | query packs.
 static size_t partials_bytes(const Geom& g, int batch, int num_sms) {
-  const size_t C = (size_t)num_sms * kCtasPerSm, bh = (size_t)batch * g.H;
+  const size_t C = (size_t)num_sms * kMaxCtasPerSm, bh = (size_t)batch * g.H;
   return ((C + bh) * pstride_for(g.d) * sizeof(float) + 255) / 256 * 256;
 }
 
@@ -886,13 +921,11 @@ cudaError_t launch_decode(const rq_cache& c, int layer, int group, int loop, int
   a.batch = batch;
   a.res0 = loop;
   a.qscale = scale * kLog2e;
-  const int grid = c.num_sms * kCtasPerSm;
-  if (grid > kMaxContrib) return cudaErrorNotSupported;   // merge_kernel's contributor table
-  const int d = c.geom.d, gs = c.geom.g;
-  if (d == 128 && gs == 32) return launch_d<128, 32>(a, grid, nres, stream);
-  if (d == 128 && gs == 16) return launch_d<128, 16>(a, grid, nres, stream);
-  if (d == 96 && gs == 32) return launch_d<96, 32>(a, grid, nres, stream);
-  if (d == 96 && gs == 16) return launch_d<96, 16>(a, grid, nres, stream);
+  const int d = c.geom.d, gs = c.geom.g, n = c.num_sms;
+  if (d == 128 && gs == 32) return launch_d<128, 32>(a, n, nres, stream);
+  if (d == 128 && gs == 16) return launch_d<128, 16>(a, n, nres, stream);
+  if (d == 96 && gs == 32) return launch_d<96, 32>(a, n, nres, stream);
+  if (d == 96 && gs == 16) return launch_d<96, 16>(a, n, nres, stream);
   return cudaErrorNotSupported;
 }
 
