@@ -153,19 +153,24 @@ struct Cfg {
 //   [32..35]                  sig_a, sum(q), sig_r, sum(R q) of the group (float bits)
 template <int D, int GS, int NRES>
 __global__ void __launch_bounds__(kPrepThreads) qprep_kernel(DecodeArgs a) {
-  constexpr int NG = D / GS, NV = D / 8;   // NV: float4 loads per half row of R
+  constexpr int NG = D / GS;
+  constexpr int RPW = 16;                  // rows of R per warp (D / 8 <= 16; the rest padded)
   __shared__ __align__(16) float q_s[D];
   __shared__ float qr_s[D];
   __shared__ __align__(16) uint32_t img_s[NG * kPackWords];   // the packs of this (row, head)
   const int bh = blockIdx.x, tid = threadIdx.x;
-  // R rows first (R stays unchanged while the cache is used): two threads per row,
-  // all loads in flight, before waiting for the kernel ahead of this one
-  const int row = tid >> 1, half = tid & 1;
-  float4 rv[NRES > 0 ? NV : 1];
-  if (NRES > 0 && row < D) {
-    const float4* rp = reinterpret_cast<const float4*>(a.R + (size_t)row * D + half * (D / 2));
+  // R first (R stays unchanged while the cache is used), before waiting for the
+  // kernel ahead of this one.  Warp w holds rows w, w+8, ...; lane l columns
+  // 4l..4l+3, so each warp-wide load reads one contiguous row.
+  const int lane = tid & 31, warp = tid >> 5;
+  float4 rv[NRES > 0 ? RPW : 1];
+  if (NRES > 0) {
 #pragma unroll
-    for (int v = 0; v < NV; ++v) rv[v] = __ldg(rp + v);
+    for (int v = 0; v < RPW; ++v) {
+      const int row = warp + 8 * v;
+      rv[v] = (row < D && lane < D / 4) ? __ldg(reinterpret_cast<const float4*>(a.R + (size_t)row * D) + lane)
+                                        : make_float4(0.f, 0.f, 0.f, 0.f);
+    }
   }
   // Launched as a programmatic dependent of whatever precedes the call on the
   // stream: everything else read here (q) or written (the packs, which the
@@ -177,18 +182,27 @@ __global__ void __launch_bounds__(kPrepThreads) qprep_kernel(DecodeArgs a) {
   if (tid < D) q_s[tid] = __bfloat162float(a.q[(size_t)bh * D + tid]) * a.qscale;
   for (int i = tid; i < NG * kPackWords; i += kPrepThreads) img_s[i] = 0u;
   __syncthreads();
-  if (NRES > 0) {   // (R q)[row]: the two halves of the row, then one sum
-    float qr = 0.f;
-    if (row < D) {
-      const float4* qp = reinterpret_cast<const float4*>(q_s + half * (D / 2));
+  if (NRES > 0) {   // (R q)[row] for the warp's rows: lane partials, then a reduce-scatter
+    const float4 x = lane < D / 4 ? reinterpret_cast<const float4*>(q_s)[lane] : make_float4(0.f, 0.f, 0.f, 0.f);
+    float pv[RPW];
 #pragma unroll
-      for (int v = 0; v < NV; ++v) {
-        const float4 x = qp[v];
-        qr = fmaf(rv[v].x, x.x, fmaf(rv[v].y, x.y, fmaf(rv[v].z, x.z, fmaf(rv[v].w, x.w, qr))));
+    for (int v = 0; v < RPW; ++v) pv[v] = fmaf(rv[v].x, x.x, fmaf(rv[v].y, x.y, fmaf(rv[v].z, x.z, rv[v].w * x.w)));
+    // after the step with offset o, each lane keeps the half of its values whose
+    // index bit matches its lane bit, summed with the partner's: 16 -> 8 -> 4 -> 2 -> 1
+#pragma unroll
+    for (int o = 16, n = RPW / 2; n >= 1; o >>= 1, n >>= 1) {
+      const bool up = (lane & o) != 0;
+#pragma unroll
+      for (int i = 0; i < n; ++i) {
+        const float send = up ? pv[i] : pv[i + n];
+        const float keep = up ? pv[i + n] : pv[i];
+        pv[i] = keep + __shfl_xor_sync(0xffffffffu, send, o);
       }
     }
-    qr += __shfl_xor_sync(0xffffffffu, qr, 1);
-    if (row < D && half == 0) qr_s[row] = qr;
+    pv[0] += __shfl_xor_sync(0xffffffffu, pv[0], 1);
+    // lanes 2v and 2v+1 now hold the sum for the warp's row index v
+    const int row = warp + 8 * (lane >> 1);
+    if ((lane & 1) == 0 && row < D) qr_s[row] = pv[0];
     __syncthreads();
   }
   // Each pack byte is written by the thread of its channel: thread k < D holds
