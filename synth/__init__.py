@@ -34,7 +34,7 @@ from typing import Optional, Sequence
 import numpy as np
 
 __all__ = [
-    "Workload", "WORKLOADS", "rotation", "looped_kv", "queries",
+    "Workload", "WORKLOADS", "rotation", "looped_kv", "looped_kv_slice", "queries",
     "to_bf16_f64", "looped_kv_torch", "queries_torch",
 ]
 
@@ -119,6 +119,17 @@ def _kv_f32(rng: np.random.Generator, w: Workload, batch: int, ntok: int) -> np.
             alpha = w.alphas[i]
             out[i] = np.float32(alpha) * base + np.float32(w.noise) * rng.standard_normal(shape, dtype=np.float32)
     return out
+
+
+def looped_kv_slice(seed: int, w: Workload, ntok: int, layer: int, group: int, b: int, h: int):
+    """KV of one (layer, group, batch row, head), drawn from its own stream (seeded by
+    the tuple), so a single slice of a full-size cache can be regenerated alone.
+
+    Returns (bf16 tensor [P, 2, ntok, d], float64 copy of the same values)."""
+    rng = np.random.default_rng(np.random.SeedSequence([seed, layer, group, b, h]))
+    one = dataclasses.replace(w, num_heads=1)
+    t, f = to_bf16_f64(_kv_f32(rng, one, 1, ntok))
+    return t[:, :, 0, 0], f[:, :, 0, 0]
 
 
 def to_bf16_f64(x: np.ndarray):
