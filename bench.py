@@ -169,6 +169,24 @@ def cpu_baseline(w: synth.Workload, batch: int, ctx: int, budget_s: float = 15.0
                       f"{smp.row_calls_per_step(batch)} row-calls per step"}
 
 
+def reduce_max_over_ranks(x: float, device=None) -> float:
+    """Largest x over the ranks of the default process group (x itself without one):
+    the job's time is its slowest rank's."""
+    import torch
+    import torch.distributed as dist
+    if not (dist.is_available() and dist.is_initialized()) or dist.get_world_size() == 1:
+        return x
+    t = torch.tensor([x], dtype=torch.float64, device=device)
+    dist.all_reduce(t, op=dist.ReduceOp.MAX)
+    return float(t.item())
+
+
+def job_throughput(world: int, batch: int, ms_step: float) -> float:
+    """Whole-job tokens/s: each of `world` replicas decodes `batch` rows per step, and the
+    step lasts `ms_step` milliseconds (the slowest rank's)."""
+    return world * batch / (ms_step / 1e3)
+
+
 def run_reference(args, w):
     rank = int(os.environ.get("RANK", "0"))
     if rank != 0:
@@ -317,11 +335,7 @@ def run_rq(args, w):
         torch.cuda.synchronize()
         if world > 1:
             torch.distributed.barrier()
-    ms_total = e0.elapsed_time(e1)
-    if world > 1:
-        t = torch.tensor([ms_total], device=dev)
-        torch.distributed.all_reduce(t, op=torch.distributed.ReduceOp.MAX)
-        ms_total = float(t.item())
+    ms_total = reduce_max_over_ranks(e0.elapsed_time(e1), dev)
     ms_step = ms_total / args.steps
     st = status.cpu().numpy()
     if st.any():
@@ -359,7 +373,7 @@ def run_rq(args, w):
             traffic = None
 
     step_gbs = byts["step"] / (ms_step / 1e3) / 1e9
-    value = world * B / (ms_step / 1e3)
+    value = job_throughput(world, B, ms_step)
     line = {
         "metric": METRIC, "value": value, "unit": "tokens/s", "n_gpus": world, "steps": args.steps,
         "warmup": args.warmup, "ms_per_step": ms_step, "higher_is_better": True, "scaling": "weak",
