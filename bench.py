@@ -342,7 +342,7 @@ def run_rq(args, w):
         raise RuntimeError(f"device status word reports an error: {st.tolist()}")
 
     # duration of one decode call (its three kernels; decode_kernel dominates), CUDA events on its stream
-    dur = []
+    dur_res, dur_anchor = [], []
     ev = [torch.cuda.Event(enable_timing=True) for _ in range(2 * ncalls)]
     with torch.cuda.stream(s):
         for r in range(3):
@@ -356,12 +356,16 @@ def run_rq(args, w):
                 i += 1
             torch.cuda.synchronize()
             if r > 0:
-                dur += [ev[2 * k].elapsed_time(ev[2 * k + 1]) for k in range(ncalls)]
+                for k, (lp, _, _) in enumerate(order):
+                    (dur_anchor if lp == P - 1 else dur_res).append(ev[2 * k].elapsed_time(ev[2 * k + 1]))
     byts = algorithmic_bytes_per_step(w, B, N)
-    per_launch_bytes = ((P - 1) * byts["call_res"] + byts["call_anchor"]) / P
-    avg_launch_ms = statistics.mean(dur)
+    # the dominant launch: a residual-loop call (anchor + one residual plane, shared mode)
+    per_launch_bytes = byts["call_res"]
+    avg_launch_ms = statistics.mean(dur_res)
     peak, peak_kind = _peaks()
     achieved = per_launch_bytes / (avg_launch_ms / 1e3) / 1e9
+    anchor_ms = statistics.mean(dur_anchor)
+    anchor_gbs = byts["call_anchor"] / (anchor_ms / 1e3) / 1e9
     traffic = None
     tp = os.path.join(ROOT, "profiles", "traffic_per_launch.json")
     if os.path.exists(tp):
@@ -377,13 +381,16 @@ def run_rq(args, w):
     line = {
         "metric": METRIC, "value": value, "unit": "tokens/s", "n_gpus": world, "steps": args.steps,
         "warmup": args.warmup, "ms_per_step": ms_step, "higher_is_better": True, "scaling": "weak",
-        "vs_baseline": None, "dtype": "fp32", "data": "synthetic", "config": _config(w),
+        "vs_baseline": None, "dtype": "int32/fp32", "data": "synthetic", "config": _config(w),
         "effective_gbps": step_gbs, "frac_of_hbm_peak": step_gbs / peak,
         "roofline": {"bound": "hbm", "achieved": achieved, "peak": peak, "unit": "GB/s",
                      "frac": achieved / peak, "traffic": traffic,
-                     "kernel": "rq_decode_attention call (qprep_kernel + decode_kernel + merge_kernel)",
+                     "kernel": "rq_decode_attention, residual-loop call (qprep_kernel + "
+                               "decode_kernel<d, g, 1> + merge_kernel)",
                      "peak_source": f"MEASURED_PEAKS.json hbm_gbs ({peak_kind})",
-                     "avg_launch_ms": avg_launch_ms, "bytes_per_launch": per_launch_bytes},
+                     "avg_launch_ms": avg_launch_ms, "bytes_per_launch": per_launch_bytes,
+                     "anchor_loop_call": {"avg_ms": anchor_ms, "bytes": byts["call_anchor"],
+                                          "achieved": anchor_gbs, "frac": anchor_gbs / peak}},
         "gpu_launches": launches_per_step * args.steps,
         "clocks": clk.summary(),
         "prefill_s": prefill_s,
