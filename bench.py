@@ -79,7 +79,7 @@ class ClockSampler:
              "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
         try:
             self.proc = subprocess.Popen(["nvidia-smi", "-i", str(self.gpu), f"--query-gpu={q}",
-                                          "--format=csv,noheader,nounits", "-lms", "200"],
+                                          "--format=csv,noheader,nounits", "-lms", "50"],
                                          stdout=subprocess.PIPE, stderr=subprocess.DEVNULL, text=True)
             self.t = threading.Thread(target=self._read, daemon=True)
             self.t.start()
@@ -191,18 +191,19 @@ def run_reference(args, w):
     rank = int(os.environ.get("RANK", "0"))
     if rank != 0:
         return
+    budget = args.ref_budget or max(0.2, min(2.0, 150.0 / (args.steps + args.warmup)))
     smp = OracleSample(w, w.context)
     per_step = smp.row_calls_per_step(w.batch)
     times, total_n, total_s = [], 0, 0.0
     for i in range(args.warmup + args.steps):
-        n, el = smp.run(args.ref_budget)
+        n, el = smp.run(budget)
         if i >= args.warmup:
             times.append(el / n * per_step)
             total_n += n
             total_s += el
     ms = 1000 * statistics.mean(times)
     val = w.batch / (ms / 1000)
-    sample = (f"each step: about {args.ref_budget:.0f} s of (row, head) attention calls at {w.context} tokens "
+    sample = (f"each step: about {budget:.2f} s of (row, head) attention calls at {w.context} tokens "
               f"(float64 NumPy rebuild from the cache bytes + softmax), extrapolated to {per_step} row-calls; "
               f"{total_n} row-calls in {total_s:.1f} s over the timed steps")
     line = {"metric": METRIC, "value": val, "unit": "tokens/s", "impl": "reference", "n_gpus": args.gpus,
@@ -226,7 +227,7 @@ def _config(w):
 def main():
     ap = argparse.ArgumentParser()
     ap.add_argument("--gpus", type=int, default=1)
-    ap.add_argument("--steps", type=int, default=20)
+    ap.add_argument("--steps", type=int, default=100)
     ap.add_argument("--warmup", type=int, default=5)
     ap.add_argument("--impl", default="rq", choices=["rq", "reference"])
     ap.add_argument("--workload", default="ouro8k", choices=sorted(synth.WORKLOADS))
@@ -235,7 +236,8 @@ def main():
     ap.add_argument("--no-bf16", action="store_true", help="skip the BF16 comparator")
     ap.add_argument("--no-cpu", action="store_true", help="skip the CPU-oracle baseline")
     ap.add_argument("--no-e2e", action="store_true")
-    ap.add_argument("--ref-budget", type=float, default=2.0)
+    ap.add_argument("--ref-budget", type=float, default=None,
+                    help="seconds of oracle work per reference step (default: about 150 s per run)")
     ap.add_argument("--quiet", action="store_true")
     ap.add_argument("--layers", type=int, default=None,
                     help="fewer layers than the workload (a small case for profiler captures)")
