@@ -9,10 +9,13 @@
 // code = exact nearest grid point, ties to even.
 //
 // Precision: every decision that fixes a stored byte (min/max, the E4M3
-// roundings, the nearest code, the BF16 coefficient) is taken exactly -- the
-// scalar steps run in float64 where float32 could round -- so stored bytes
-// match the exact-arithmetic reading for a given rotated residual.  The
-// rotation itself (d x d per vector) runs in float32 FMA.
+// roundings, the nearest code, the BF16 coefficient) is taken exactly, so
+// stored bytes match the exact-arithmetic reading for a given rotated
+// residual.  Each decision is first taken in float32 together with a bound
+// on its rounding error; only when the bound does not rule out the other
+// side of a rounding boundary is it retaken in float64 (FP64 throughput is a
+// small fraction of FP32 on this GPU).  The rotation itself (d x d per
+// vector) runs in float32 FMA.
 //
 // Grid: x = aligned block of 16 positions of one row, y = row * H + head,
 // z = K/V (and, for short appends in shared mode, the residual loop: the
@@ -75,6 +78,35 @@ __device__ int nearest_code(float v, float o, float s, int qmax) {
   return min(max(k, 0), qmax);
 }
 
+// e4m3_nearest_ratio for D = hi - lo: a float32 estimate decides unless it lies
+// within its error bound (relative 2^-22: one rounding in hi - lo, one in the
+// division) of a midpoint between two E4M3 values; then the exact routine.
+__device__ uint8_t e4m3_ratio(float hi, float lo, int qmax) {
+  const float est = __fdiv_rn(hi - lo, (float)qmax);
+  const int c0 = f32_to_e4m3(est);                       // est >= 0: codes 0 .. 0x7E
+  const float v0 = e4m3_to_f32((uint8_t)c0);
+  const float vlo = c0 > 0 ? e4m3_to_f32((uint8_t)(c0 - 1)) : -INFINITY;
+  const float vhi = c0 < 0x7E ? e4m3_to_f32((uint8_t)(c0 + 1)) : INFINITY;
+  const float tol = est * 0x1p-20f;
+  // midpoints of neighbouring E4M3 values are exact in float32 (few significant bits)
+  if (est > 0.5f * (vlo + v0) + tol && est < 0.5f * (v0 + vhi) - tol) return (uint8_t)c0;
+  return e4m3_nearest_ratio((double)hi - (double)lo, qmax);
+}
+
+// nearest_code with a float32 first pass: (v - o) / s is within |x| 2^-22 of
+// the exact quotient, so a fractional part far enough from 1/2 decides.
+__device__ int nearest_code_fast(float v, float o, float s, int qmax) {
+  if (!(s > 0.f)) return 0;
+  const float x = __fdiv_rn(v - o, s);
+  const float kf = rintf(x);
+  const float tol = fmaxf(0x1p-14f, fabsf(x) * 0x1p-20f);
+  if (fabsf(x - kf) < 0.5f - tol) {
+    const float kc = fminf(fmaxf(kf, 0.f), (float)qmax);
+    return (int)kc;
+  }
+  return nearest_code(v, o, s, qmax);
+}
+
 // Group quantizer for one element per lane; the g lanes of a group are
 // consecutive lanes of one warp (g = 16 or 32).  Returns the code; writes
 // the dequantized value and (on every lane) the scale/offset bytes.
@@ -86,9 +118,9 @@ __device__ int quantize_lane(float v, bool active, int g, int qmax, uint8_t* s_b
     hi = fmaxf(hi, __shfl_xor_sync(0xffffffffu, hi, off, g));
   }
   uint8_t ob = f32_to_e4m3(lo);
-  uint8_t sb = e4m3_nearest_ratio((double)hi - (double)lo, qmax);
+  uint8_t sb = e4m3_ratio(hi, lo, qmax);
   float o = e4m3_to_f32(ob), s = e4m3_to_f32(sb);
-  int code = nearest_code(v, o, s, qmax);
+  int code = nearest_code_fast(v, o, s, qmax);
   *s_byte = sb;
   *o_byte = ob;
   *vhat = fmaf(s, (float)code, o);                  // exact (few significant bits)
@@ -283,25 +315,54 @@ __global__ void __launch_bounds__(kThreads) append_kernel(AppendArgs a) {
       for (int t = 0; t < kTok; ++t)
         x_s[t][tid] = valid_s[t] ? load_x(a, j, kvi, b, h, p0 + t - start, tid) : 0.f;
     __syncthreads();
-    // least-squares coefficient per token (float64: the products are exact
-    // and their sums exact for data of moderate dynamic range)
+    // least-squares coefficient per token, rounded to BF16 from the value of the
+    // float64 sums (exact products; sums exact for data of moderate dynamic
+    // range).  float32 sums with an error bound decide when both ends of the
+    // bound round to the same BF16 value; otherwise the float64 sums do.
     {
       const int warp = tid / 32, lane = tid % 32;
       for (int t = warp; t < kTok; t += kThreads / 32) {
         if (!valid_s[t]) continue;   // same for every lane of the warp
-        double num = 0.0, den = 0.0;
+        float num = 0.f, den = 0.f, mag = 0.f;
         for (int k = lane; k < d; k += 32) {
-          double y = ref_s[t][k], x = x_s[t][k];
-          num = fma(x, y, num);
-          den = fma(y, y, den);
+          const float y = ref_s[t][k], x = x_s[t][k];
+          num = fmaf(x, y, num);
+          den = fmaf(y, y, den);
+          mag = fmaf(fabsf(x), fabsf(y), mag);
         }
         for (int off = 16; off > 0; off >>= 1) {
           num += __shfl_xor_sync(0xffffffffu, num, off);
           den += __shfl_xor_sync(0xffffffffu, den, off);
+          mag += __shfl_xor_sync(0xffffffffu, mag, off);
+        }
+        // every lane holds the same sums: the branch below is uniform over the warp
+        bool decided = false;
+        uint16_t bits = 0;
+        if (den > 0.f) {
+          // at most 4 + 5 roundings per term (< 2^-20 relative to the sums of magnitudes)
+          const float c = __fdiv_rn(num, den);
+          const float err = (mag + fabsf(c) * den) * 0x1p-20f / den + fabsf(c) * 0x1p-22f;
+          const __nv_bfloat16 lo = __float2bfloat16_rn(c - err), hi = __float2bfloat16_rn(c + err);
+          const uint16_t blo = *reinterpret_cast<const uint16_t*>(&lo);
+          const uint16_t bhi = *reinterpret_cast<const uint16_t*>(&hi);
+          if (blo == bhi) { bits = blo; decided = true; }
+        } else {
+          decided = true;   // c = 0
+        }
+        if (!decided) {
+          double num64 = 0.0, den64 = 0.0;
+          for (int k = lane; k < d; k += 32) {
+            double y = ref_s[t][k], x = x_s[t][k];
+            num64 = fma(x, y, num64);
+            den64 = fma(y, y, den64);
+          }
+          for (int off = 16; off > 0; off >>= 1) {
+            num64 += __shfl_xor_sync(0xffffffffu, num64, off);
+            den64 += __shfl_xor_sync(0xffffffffu, den64, off);
+          }
+          bits = f64_to_bf16_bits(den64 > 0.0 ? num64 / den64 : 0.0);
         }
         if (lane == 0) {
-          double c = den > 0.0 ? num / den : 0.0;
-          uint16_t bits = f64_to_bf16_bits(c);
           c_s[t] = bits;
           cb_s[t] = bf16_bits_to_f32(bits);
         }
