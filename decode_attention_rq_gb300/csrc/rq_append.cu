@@ -259,6 +259,10 @@ __global__ void __launch_bounds__(kThreads) append_kernel(AppendArgs a) {
   __shared__ float cb_s[kTok];
   __shared__ bool valid_s[kTok];
 
+  // launched as a programmatic dependent: seq_lens and kv may come from the kernel
+  // ahead of this one; the next kernel is released once they are visible
+  pdl_wait();
+  pdl_launch_dependents();
   const int start = a.seq_lens[b];
   if (start < 0 || start + a.n > a.g.Nmax) {
     if (blockIdx.x == 0 && h == 0 && blockIdx.z == 0 && tid == 0 && a.status) atomicExch(&a.status[1], 1);
@@ -437,10 +441,9 @@ cudaError_t launch_append(const rq_cache& c, int layer, int group, int batch,
   // a short append in shared mode takes one CTA per (K/V, residual loop)
   const bool split = c.geom.mode == RQ_MODE_SHARED && c.geom.P > 1 && n_tokens <= kTok;
   dim3 grid((n_tokens + kTok - 1) / kTok + 1, batch * c.geom.H, split ? 2 * (c.geom.P - 1) : 2);
-  if (c.geom.d == 128) append_kernel<128><<<grid, kThreads, 0, stream>>>(a);
-  else if (c.geom.d == 96) append_kernel<96><<<grid, kThreads, 0, stream>>>(a);
-  else return cudaErrorNotSupported;
-  return cudaGetLastError();
+  if (c.geom.d == 128) return launch_dependent(append_kernel<128>, grid, dim3(kThreads), 0, stream, a);
+  if (c.geom.d == 96) return launch_dependent(append_kernel<96>, grid, dim3(kThreads), 0, stream, a);
+  return cudaErrorNotSupported;
 }
 
 }  // namespace rq

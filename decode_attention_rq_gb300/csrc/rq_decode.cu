@@ -97,13 +97,6 @@ __device__ __forceinline__ int to_fix(float x, float inv) {
 __device__ __forceinline__ float2 meta2(const uint8_t* p) {   // (scale, offset)
   return e4m3x2_to_f32x2(*reinterpret_cast<const uint16_t*>(p));
 }
-// Programmatic dependent launch: let the next kernel of the stream start its
-// prologue; wait until the kernel before this one has finished and its writes
-// are visible (returns at once when launched without the dependency).
-__device__ __forceinline__ void pdl_launch_dependents() {
-  asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
-}
-__device__ __forceinline__ void pdl_wait() { asm volatile("griddepcontrol.wait;" ::: "memory"); }
 __device__ __forceinline__ int clamp_len(int n, int nmax) { return n < 0 ? 0 : (n > nmax ? nmax : n); }
 
 // Balanced split of U units over C CTAs: CTA c takes [start(c), start(c+1)) with
@@ -297,10 +290,12 @@ __global__ void __launch_bounds__(kThreads, (Cfg<D, GS, NRES>::MINB)) decode_ker
   __syncthreads();
   const int U = pre_s[B];
 
-  if (U == 0) return;   // every row empty: the merge kernel writes the current V
+  // Every CTA waits for the kernel ahead of it before exiting, early exits
+  // included, so that this kernel's completion implies the prep kernel's.
+  if (U == 0) { pdl_wait(); return; }   // every row empty: the merge kernel writes the current V
   const Split split{U / Cn, U % Cn};
   const int u0 = split.start(cta), u1 = split.start(cta + 1);
-  if (u0 >= u1) return;
+  if (u0 >= u1) { pdl_wait(); return; }
 
   // unit cursor (row, head, unit), advanced without divisions
   struct Cursor { int b, h, t; };
@@ -756,6 +751,7 @@ __global__ void __launch_bounds__(kMergeThreads) merge_kernel(DecodeArgs a, int 
     for (int k = tid; k < D; k += kMergeThreads)
       a.out[(size_t)bh * D + k] = __bfloat162float(a.v_cur[(size_t)bh * D + k]);
     if (NRES > 0) (void)mbar_wait_bounded(&r_bar, 0);   // the R copy lands before the CTA exits
+    pdl_wait();   // completion of this kernel implies the decode kernel's
     return;
   }
   const Split split{U / Cn, U % Cn};
@@ -833,22 +829,6 @@ __global__ void __launch_bounds__(kMergeThreads) merge_kernel(DecodeArgs a, int 
     if (tid < D) o += rt_s[tid];
   }
   if (tid < D) a.out[(size_t)bh * D + tid] = (va_s[tid] + o) / L;
-}
-
-template <typename... Args>
-cudaError_t launch_dependent(void (*k)(Args...), dim3 grid, dim3 block, size_t smem,
-                             cudaStream_t stream, Args... args) {
-  cudaLaunchConfig_t cfg = {};
-  cfg.gridDim = grid;
-  cfg.blockDim = block;
-  cfg.dynamicSmemBytes = smem;
-  cfg.stream = stream;
-  cudaLaunchAttribute attr[1];
-  attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
-  attr[0].val.programmaticStreamSerializationAllowed = 1;
-  cfg.attrs = attr;
-  cfg.numAttrs = 1;
-  return cudaLaunchKernelEx(&cfg, k, args...);
 }
 
 template <int D, int GS, int NRES>

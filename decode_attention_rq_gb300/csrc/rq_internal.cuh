@@ -155,6 +155,32 @@ __device__ __forceinline__ float2 e4m3x2_to_f32x2(uint16_t v) {
   __half2 hh = *reinterpret_cast<__half2*>(&h2);
   return __half22float2(hh);
 }
+// Programmatic dependent launch: let the next kernel of the stream start its
+// prologue; wait until the kernel before this one has finished and its writes
+// are visible (returns at once when launched without the dependency).
+__device__ __forceinline__ void pdl_launch_dependents() {
+  asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
+}
+__device__ __forceinline__ void pdl_wait() { asm volatile("griddepcontrol.wait;" ::: "memory"); }
 #endif
+
+// Launch with programmatic stream serialization: the kernel may start before the
+// previous kernel on the stream finishes and must call pdl_wait() before it reads
+// anything that kernel (or earlier work) produced.
+template <typename... Args>
+cudaError_t launch_dependent(void (*k)(Args...), dim3 grid, dim3 block, size_t smem,
+                             cudaStream_t stream, Args... args) {
+  cudaLaunchConfig_t cfg = {};
+  cfg.gridDim = grid;
+  cfg.blockDim = block;
+  cfg.dynamicSmemBytes = smem;
+  cfg.stream = stream;
+  cudaLaunchAttribute attr[1];
+  attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+  attr[0].val.programmaticStreamSerializationAllowed = 1;
+  cfg.attrs = attr;
+  cfg.numAttrs = 1;
+  return cudaLaunchKernelEx(&cfg, k, args...);
+}
 
 }  // namespace rq
