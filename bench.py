@@ -49,20 +49,27 @@ def _algo_bytes_per_token_call(w: synth.Workload, has_res: bool, chained_planes:
     return 2 * (anchor + (res * chained_planes if has_res else 0))
 
 
-def algorithmic_bytes_per_step(w: synth.Workload, batch: int, ctx: int) -> dict:
+def algorithmic_bytes_per_step(w: synth.Workload, batch: int, ctx: int, chained: bool = False) -> dict:
     """Bytes the step must move at minimum: every attention call reads its
     planes for all cached tokens, plus the current token, q and out; each
-    append writes one token's records."""
+    append writes one token's records.  Shared anchor: loop l < P-1 reads the
+    anchor and its own residual plane; chained: the anchor and the residual
+    planes of loops l .. P-2."""
     P, L, H, d = w.loops_per_group, w.num_layers, w.num_heads, w.head_dim
     rows = batch * H
-    per_call_res = _algo_bytes_per_token_call(w, True) * ctx * rows
-    per_call_anchor = _algo_bytes_per_token_call(w, False) * ctx * rows
     small = rows * (3 * d * 2 + d * 4)                      # q, k_cur, v_cur (bf16) + out (fp32)
-    calls = (P - 1) * (per_call_res + small) + (per_call_anchor + small)
+    per_loop = []
+    for lp in range(P):
+        planes = 0 if lp == P - 1 else (P - 1 - lp if chained else 1)
+        per_loop.append(_algo_bytes_per_token_call(w, planes > 0, max(planes, 1)) * ctx * rows + small)
+    per_call_res = per_loop[0] - small if P > 1 else 0
+    per_call_anchor = per_loop[P - 1] - small
+    calls = sum(per_loop)
     ng = d // w.group_size
     append = rows * 2 * ((d // 2 + 2 * ng) + (P - 1) * (d // 4 + 2 * ng + 2)) + rows * P * 2 * d * 2
     total = L * w.num_groups * (calls + append)
-    return {"step": total, "call_res": per_call_res + small, "call_anchor": per_call_anchor + small}
+    return {"step": total, "call_res": per_call_res + small, "call_anchor": per_call_anchor + small,
+            "per_loop": per_loop}
 
 
 class ClockSampler:
@@ -209,17 +216,18 @@ def run_reference(args, w):
     line = {"metric": METRIC, "value": val, "unit": "tokens/s", "impl": "reference", "n_gpus": args.gpus,
             "steps": args.steps, "warmup": args.warmup, "ms_per_step": ms, "higher_is_better": True,
             "scaling": "weak", "vs_baseline": None, "dtype": "f64", "data": "synthetic",
-            "config": _config(w),
+            "config": _config(w, args.chained),
             "cpu_baseline": {"value": val, "unit": "tokens/s", "cores": len(os.sched_getaffinity(0)),
                              "kind": "oracle", "sample": sample},
             "e2e": {"value": val, "unit": "tokens/s", "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0}}
     print(json.dumps(line))
 
 
-def _config(w):
+def _config(w, chained=False):
     return {"workload": f"{w.name}: {w.num_layers} layers x {w.loops_per_group} loops x {w.num_groups} groups, "
                         f"{w.num_heads} KV heads x {w.head_dim}, batch {w.batch}, {w.context}-token context, "
-                        f"INT4 anchor + INT2 residuals, group {w.group_size}, shared anchor",
+                        f"INT4 anchor + INT2 residuals, group {w.group_size}, "
+                        f"{'chained' if chained else 'shared'} anchor",
             "global_batch": w.batch, "seq_len": w.context, "parallelism": "replicas",
             "l2": "inputs larger than L2 (every step streams the whole compressed cache)"}
 
@@ -239,6 +247,7 @@ def main():
     ap.add_argument("--ref-budget", type=float, default=None,
                     help="seconds of oracle work per reference step (default: about 150 s per run)")
     ap.add_argument("--quiet", action="store_true")
+    ap.add_argument("--chained", action="store_true", help="chained anchors (loop l coded against loop l+1)")
     ap.add_argument("--layers", type=int, default=None,
                     help="fewer layers than the workload (a small case for profiler captures)")
     args = ap.parse_args()
@@ -270,7 +279,7 @@ def run_rq(args, w):
     gen = torch.Generator(device=dev)
     gen.manual_seed(1234 + rank)
     R32 = torch.from_numpy(synth.rotation(d).astype(np.float32)).to(dev)
-    cfg = rq.rq_config(L, P, G, H, d, g, B, N + 64, rq.RQ_MODE_SHARED)
+    cfg = rq.rq_config(L, P, G, H, d, g, B, N + 64, rq.RQ_MODE_CHAINED if args.chained else rq.RQ_MODE_SHARED)
     nbytes = rq.rq_cache_bytes(cfg)
     cache_buf = torch.empty(nbytes, dtype=torch.uint8, device=dev)
     handle = rq.rq_cache_create(cfg, cache_buf, nbytes, R32)
@@ -344,7 +353,8 @@ def run_rq(args, w):
         raise RuntimeError(f"device status word reports an error: {st.tolist()}")
 
     # duration of one decode call (its three kernels; decode_kernel dominates), CUDA events on its stream
-    dur_res, dur_anchor = [], []
+    byts = algorithmic_bytes_per_step(w, B, N, args.chained)
+    dur_res, dur_anchor, bytes_res = [], [], 0
     ev = [torch.cuda.Event(enable_timing=True) for _ in range(2 * ncalls)]
     with torch.cuda.stream(s):
         for r in range(3):
@@ -360,9 +370,11 @@ def run_rq(args, w):
             if r > 0:
                 for k, (lp, _, _) in enumerate(order):
                     (dur_anchor if lp == P - 1 else dur_res).append(ev[2 * k].elapsed_time(ev[2 * k + 1]))
-    byts = algorithmic_bytes_per_step(w, B, N)
-    # the dominant launch: a residual-loop call (anchor + one residual plane, shared mode)
-    per_launch_bytes = byts["call_res"]
+                    if lp < P - 1:
+                        bytes_res += byts["per_loop"][lp]
+    # the dominant launch: a residual-loop call (shared: anchor + one residual plane;
+    # chained: anchor + the planes down to the loop), bytes and time summed over those calls
+    per_launch_bytes = bytes_res / len(dur_res)
     avg_launch_ms = statistics.mean(dur_res)
     peak, peak_kind = _peaks()
     achieved = per_launch_bytes / (avg_launch_ms / 1e3) / 1e9
@@ -373,7 +385,8 @@ def run_rq(args, w):
     if os.path.exists(tp):
         try:
             tj = json.load(open(tp))
-            if tj.get("workload") == w.name and tj.get("kernel_source_hash") == _kernel_hash():
+            if (tj.get("workload") == w.name and tj.get("batch") == B and tj.get("group_size") == g
+                    and not args.chained and tj.get("kernel_source_hash") == _kernel_hash()):
                 traffic = tj.get("bytes_per_launch")
         except Exception:
             traffic = None
@@ -383,7 +396,7 @@ def run_rq(args, w):
     line = {
         "metric": METRIC, "value": value, "unit": "tokens/s", "n_gpus": world, "steps": args.steps,
         "warmup": args.warmup, "ms_per_step": ms_step, "higher_is_better": True, "scaling": "weak",
-        "vs_baseline": None, "dtype": "int32/fp32", "data": "synthetic", "config": _config(w),
+        "vs_baseline": None, "dtype": "int32/fp32", "data": "synthetic", "config": _config(w, args.chained),
         "effective_gbps": step_gbs, "frac_of_hbm_peak": step_gbs / peak,
         "roofline": {"bound": "hbm", "achieved": achieved, "peak": peak, "unit": "GB/s",
                      "frac": achieved / peak, "traffic": traffic,
@@ -417,7 +430,11 @@ def bench_bf16(args, w, dev, gen, scale):
     import decode_attention_rq_gb300 as rq
     L, P, G, H, d, B, N = w.num_layers, w.loops_per_group, w.num_groups, w.num_heads, w.head_dim, w.batch, w.context
     ncalls = L * G * P
-    kv = torch.empty((ncalls, 2, B, H, N, d), dtype=torch.bfloat16, device=dev)
+    # distinct K/V per call up to a memory budget; beyond it calls cycle over the buffers
+    # (each call streams far more than the L2 holds, so reuse across calls hits DRAM)
+    per_call = 2 * B * H * N * d * 2
+    nbuf = max(2, min(ncalls, int(48e9 // per_call)))
+    kv = torch.empty((nbuf, 2, B, H, N, d), dtype=torch.bfloat16, device=dev)
     kv.normal_(generator=gen)
     q = torch.randn((ncalls, B, H, d), generator=gen, device=dev).to(torch.bfloat16)
     cur = torch.randn((ncalls, 2, B, H, d), generator=gen, device=dev).to(torch.bfloat16)
@@ -429,7 +446,7 @@ def bench_bf16(args, w, dev, gen, scale):
 
     def step(st):
         for i in range(ncalls):
-            rq.rq_decode_attention_bf16(kv[i, 0], kv[i, 1], cur[i, 0], cur[i, 1], q[i], seq, B, H, d, N, scale,
+            rq.rq_decode_attention_bf16(kv[i % nbuf, 0], kv[i % nbuf, 1], cur[i, 0], cur[i, 1], q[i], seq, B, H, d, N, scale,
                                         out, ws, ws_bytes, st)
     with torch.cuda.stream(s):
         step(s.cuda_stream)
