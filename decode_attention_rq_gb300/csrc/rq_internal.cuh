@@ -14,7 +14,7 @@ namespace rq {
 constexpr int kTile = 64;            // token slots per tile (layout constant, see rq.h)
 constexpr int kAnchorBits = 4;
 constexpr int kResBits = 2;
-constexpr int kMaxLoops = 8;
+constexpr int kMaxLoops = 16;      // loops per anchor group (Huginn-shaped groups of up to 16)
 constexpr int kStatusWords = 4;      // int32 status word at the start of a workspace
 constexpr unsigned long long kWaitNs = 2000000000ull;  // give up an mbarrier wait after 2 s
 

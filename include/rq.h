@@ -23,7 +23,7 @@
  *     RQ_ERR_CUDA.  Faults inside a kernel surface on a later CUDA call.
  *   - Device pointers must be 16-byte aligned (RQ_ERR_ALIGNMENT).
  *   - Supported shapes: head_dim in {96, 128}; group_size in {16, 32} dividing
- *     head_dim; loops_per_group in [1, 8].  Others: RQ_ERR_UNSUPPORTED.
+ *     head_dim; loops_per_group in [1, 16].  Others: RQ_ERR_UNSUPPORTED.
  *
  * ---------------------------------------------------------------------------
  * Cache byte layout (this library's format; the pages fix the record

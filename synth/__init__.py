@@ -34,7 +34,7 @@ from typing import Optional, Sequence
 import numpy as np
 
 __all__ = [
-    "Workload", "WORKLOADS", "rotation", "looped_kv", "looped_kv_slice", "queries",
+    "Workload", "WORKLOADS", "rotation", "group_alphas", "looped_kv", "looped_kv_slice", "queries",
     "to_bf16_f64", "looped_kv_torch", "queries_torch",
 ]
 
@@ -69,6 +69,11 @@ class Workload:
 OURO_ALPHAS = (0.7, 0.85, 0.95)
 HUGINN_ALPHAS = (0.7, 0.85, 0.95, 1.0)
 
+
+def group_alphas(p: int) -> tuple:
+    """Loop similarity to the base for groups of p loops: 0.7 rising evenly to 1.0."""
+    return tuple(0.7 + 0.3 * i / (p - 1) for i in range(p)) if p > 1 else (1.0,)
+
 WORKLOADS = {
     # one layer, 4 loops, batch 1, 2 heads, width 128, 256 tokens
     "toy": Workload("toy", 1, 4, 1, 2, 128, 32, 1, 256, OURO_ALPHAS, True),
@@ -79,6 +84,10 @@ WORKLOADS = {
     "ouro16k_b4": Workload("ouro16k_b4", 24, 4, 1, 16, 128, 32, 4, 16384, OURO_ALPHAS, True),
     # Huginn-3.5B shape: 4-layer block, 32 loops as 8 groups of 4, 55 heads of width 96
     "huginn": Workload("huginn", 4, 4, 8, 55, 96, 32, 2, 4096, HUGINN_ALPHAS, False),
+    # the same 32 loops as 4 groups of 8 and as 2 groups of 16 loops per anchor (the
+    # larger groups the arXiv summary mentions from the appendix)
+    "huginn_g8": Workload("huginn_g8", 4, 8, 4, 55, 96, 32, 2, 4096, group_alphas(8), False),
+    "huginn_g16": Workload("huginn_g16", 4, 16, 2, 55, 96, 32, 2, 4096, group_alphas(16), False),
 }
 
 

@@ -29,7 +29,7 @@ class Case:
 
     def workload(self, anchor_is_base=True):
         alphas = synth.OURO_ALPHAS if self.P == 4 and anchor_is_base else tuple(
-            [0.7, 0.85, 0.95, 1.0, 0.9, 0.8, 0.75, 0.7][: self.P])
+            [0.7, 0.85, 0.95, 1.0, 0.9, 0.8, 0.75, 0.7][: self.P] if self.P <= 8 else synth.group_alphas(self.P))
         return synth.Workload("case", self.L, self.P, self.G, self.H, self.d, self.g, self.B, self.Nmax,
                               alphas, anchor_is_base)
 

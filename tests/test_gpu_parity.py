@@ -302,6 +302,45 @@ def test_chained_append_bitexact():
     assert np.array_equal(gbuf, obuf), f"{int((gbuf != obuf).sum())} cache bytes differ"
 
 
+@pytest.mark.parametrize("P,d", [(8, 128), (16, 96)])
+def test_large_loop_groups_shared(P, d):
+    """Groups of 8 and 16 loops per anchor (shared anchor): every byte matches the
+    oracle's, and loops across the group decode within tolerance (each residual
+    loop reads the anchor and its own plane, whatever the group length)."""
+    import decode_attention_rq_gb300 as rq
+    case = Case(L=1, P=P, G=2, H=2, d=d, g=32, B=2, Nmax=200, seed=12 + P)
+    gpu, geom, obuf, R, _ = _build_both(case, chunks=[170, 1], anchor_is_base=False)
+    gbuf = gpu.bytes_host()
+    assert np.array_equal(gbuf, obuf), f"{int((gbuf != obuf).sum())} cache bytes differ"
+    seq = np.array([171, 90])
+    scale = 1 / math.sqrt(d)
+    worst = 0.0
+    for group in (0, 1):
+        for loop in (0, P // 2, P - 2, P - 1):
+            qb, q, kcb, kc, vcb, vc = _queries(case, 40 + group, loop)
+            out = gpu.decode(0, group, loop, qb, kcb, vcb, seq, scale).cpu().numpy()
+            ref = oracle.decode_attention(obuf, geom, R, 0, group, loop, q, kc, vc, seq, scale)
+            err = float(np.abs(out - ref).max())
+            worst = max(worst, err)
+            assert err <= ATOL, f"P={P} group {group} loop {loop}: max abs err {err:.3e}"
+    assert int(gpu.status.cpu()[0]) == 0
+    print(f"P={P}: worst max-abs error {worst:.3e}; cache bytes equal")
+
+
+def test_large_chained_group_appends_and_decode_limit():
+    """Chained groups of 8 loops: appends (each loop coded against the rebuilt next
+    one) match byte for byte; decode supports chained groups of up to 4 loops and
+    refuses longer ones with UNSUPPORTED."""
+    import decode_attention_rq_gb300 as rq
+    case = Case(L=1, P=8, G=1, H=2, d=128, g=32, B=1, Nmax=128, seed=21, chained=True)
+    gpu, geom, obuf, R, _ = _build_both(case, chunks=[100], anchor_is_base=False)
+    assert np.array_equal(gpu.bytes_host(), obuf)
+    qb, q, kcb, kc, vcb, vc = _queries(case, 50, 0)
+    with pytest.raises(rq.RqError) as e:
+        gpu.decode(0, 0, 0, qb, kcb, vcb, np.array([100]), 0.1)
+    assert e.value.status == 6   # RQ_ERR_UNSUPPORTED
+
+
 def test_huginn_groups_and_layers():
     """Several loop groups and layers: regions do not overlap, each group decodes right."""
     case = Case(L=2, P=4, G=3, H=3, d=96, g=32, B=2, Nmax=192, seed=10)

@@ -54,13 +54,14 @@ def test_cache_bytes_matches_storage_accounting(rq):
     assert n == 24 * 4 * 16 * 8192 * 396
     geom = oracle.Geometry(24, 4, 1, 16, 128, 32, 4, 8192)
     assert n == geom.total_bytes
-    for d, g, P, G, N in [(96, 32, 4, 8, 4096), (128, 16, 4, 1, 1000), (96, 16, 2, 3, 77), (128, 32, 1, 1, 64)]:
+    for d, g, P, G, N in [(96, 32, 4, 8, 4096), (128, 16, 4, 1, 1000), (96, 16, 2, 3, 77), (128, 32, 1, 1, 64),
+                          (96, 32, 8, 4, 4096), (96, 32, 16, 2, 4096), (128, 16, 16, 1, 300)]:
         cfg = _cfg(rq, head_dim=d, group_size=g, loops_per_group=P, num_groups=G, max_seq_len=N)
         assert rq.rq_cache_bytes(cfg) == oracle.Geometry(24, P, G, 16, d, g, 4, N).total_bytes
 
 
 @pytest.mark.parametrize("kw", [dict(head_dim=64), dict(group_size=8), dict(head_dim=96, group_size=64),
-                                dict(loops_per_group=0), dict(loops_per_group=9), dict(mode=2),
+                                dict(loops_per_group=0), dict(loops_per_group=17), dict(mode=2),
                                 dict(num_heads=0), dict(max_seq_len=0)])
 def test_unsupported_shapes(rq, kw):
     cfg = _cfg(rq, **kw)

@@ -34,6 +34,19 @@ def test_storage_other_shapes():
     assert Lo.bits_per_element(96, 32, 4)["total"] == 4.5 + 3 * (2 + 0.5 + 16 / 96)
 
 
+@pytest.mark.parametrize("P", [8, 16])
+def test_storage_of_larger_loop_groups(P):
+    """Groups of 8 or 16 loops per anchor (the appendix variant): one INT4 anchor and
+    P-1 INT2 residuals.  Closed form from the record sizes at d=128, g=32: anchor
+    4 + 16/32 bits, each residual 2 + 16/32 + 16/128 bits per element."""
+    acc = Lo.bits_per_element(128, 32, P)
+    assert acc["total"] == pytest.approx(4.5 + (P - 1) * 2.625)
+    assert acc["reduction"] == pytest.approx(1 - (4.5 + (P - 1) * 2.625) / (16 * P))
+    geom = Lo.Geometry(1, P, 1, 1, 128, 32, 1, 64)
+    # one tile of 64 tokens, K and V: bytes = 64 tokens x 128 channels x bits / 8
+    assert geom.region == 2 * 64 * 128 * acc["total"] / 8
+
+
 @pytest.mark.parametrize("d,g,per_token", [(128, 32, 396), (128, 16, 2 * 80 + 6 * 50), (96, 32, 2 * 54 + 6 * 32)])
 def test_geometry_bytes_match_the_accounting(d, g, per_token):
     geom = Lo.Geometry(1, 4, 1, 1, d, g, 1, 640)
