@@ -306,18 +306,31 @@ def run_rq(args, w):
 
     order = [(lp, layer, grp) for grp in range(G) for lp in range(P) for layer in range(L)]
 
-    def step(stream):
-        i = 0
+    s = torch.cuda.Stream(device=dev)
+    # Each layer's append follows its last-loop attention call on a second stream: it
+    # writes only the new token's slot (which no attention call of the step reads; the
+    # channel-major words it rewrites keep the other tokens' fields), so it overlaps
+    # the next attention calls.  The step joins it before ending.
+    s_app = torch.cuda.Stream(device=dev)
+    ev_after = [torch.cuda.Event() for _ in range(L * G)]
+    ev_join = torch.cuda.Event()
+
+    def step(stream=None):
+        i = k = 0
         for (lp, layer, grp) in order:
             t = temp_all[layer * G + grp]
             rq.rq_decode_attention(handle, layer, grp, lp, B, q_all[i], t[lp, 0, :, :, 0], t[lp, 1, :, :, 0], seq,
-                                   scale, out_all[i], ws, ws_bytes, stream)
+                                   scale, out_all[i], ws, ws_bytes, s.cuda_stream)
             i += 1
             if lp == P - 1:
-                rq.rq_append(handle, layer, grp, B, t, seq, 1, status, stream)
+                ev_after[k].record(s)
+                s_app.wait_event(ev_after[k])
+                rq.rq_append(handle, layer, grp, B, t, seq, 1, status, s_app.cuda_stream)
+                k += 1
+        ev_join.record(s_app)
+        s.wait_event(ev_join)
 
     launches_per_step = 3 * ncalls + L * G   # a decode call is qprep + decode + merge kernels
-    s = torch.cuda.Stream(device=dev)
     torch.cuda.synchronize()
     with torch.cuda.stream(s):
         step(s.cuda_stream)   # eager once (also sets kernel attributes before capture)
