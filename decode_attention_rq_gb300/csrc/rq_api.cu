@@ -14,7 +14,7 @@ bool make_geom(const rq_config& c, Geom* g) {
   if (c.head_dim != 96 && c.head_dim != 128) return false;
   if (c.group_size != 16 && c.group_size != 32) return false;
   if (c.head_dim % c.group_size) return false;
-  if (c.mode != RQ_MODE_SHARED && c.mode != RQ_MODE_CHAINED) return false;
+  if (c.mode & ~(RQ_MODE_CHAINED | RQ_MODE_NORM_RATIO)) return false;
   g->L = c.num_layers;
   g->P = c.loops_per_group;
   g->G = c.num_groups;
@@ -119,7 +119,7 @@ rq_status rq_decode_attention(rq_cache* cache, int32_t layer, int32_t group, int
       batch <= 0)
     return RQ_ERR_INVALID_ARG;
   if (batch > g.Bmax) return RQ_ERR_CAPACITY;
-  if (g.mode == RQ_MODE_CHAINED && g.P > decode_max_chained_loops()) return RQ_ERR_UNSUPPORTED;
+  if ((g.mode & RQ_MODE_CHAINED) && g.P > decode_max_chained_loops()) return RQ_ERR_UNSUPPORTED;
   if (workspace_bytes < decode_workspace_bytes(g, batch, cache->num_sms)) return RQ_ERR_WORKSPACE;
   if (!aligned16(q) || !aligned16(k_cur) || !aligned16(v_cur) || !aligned16(seq_lens) ||
       !aligned16(out) || !aligned16(workspace))

@@ -248,7 +248,8 @@ __global__ void __launch_bounds__(kThreads) append_kernel(AppendArgs a) {
   const int b = blockIdx.y / a.g.H, h = blockIdx.y % a.g.H;
   const int kvi = blockIdx.z & 1, jz = blockIdx.z >> 1;
   const bool split = gridDim.z > 2;   // this CTA codes residual loop jz only
-  const bool chained = a.g.mode == RQ_MODE_CHAINED;
+  const bool chained = (a.g.mode & RQ_MODE_CHAINED) != 0;
+  const bool norm_ratio = (a.g.mode & RQ_MODE_NORM_RATIO) != 0;
 
   __shared__ float ref_s[kTok][128];     // anchor_hat (shared) or rebuilt loop l+1 (chained)
   __shared__ float x_s[kTok][128];       // current loop, then its residual
@@ -319,18 +320,19 @@ __global__ void __launch_bounds__(kThreads) append_kernel(AppendArgs a) {
       for (int t = 0; t < kTok; ++t)
         x_s[t][tid] = valid_s[t] ? load_x(a, j, kvi, b, h, p0 + t - start, tid) : 0.f;
     __syncthreads();
-    // least-squares coefficient per token, rounded to BF16 from the value of the
-    // float64 sums (exact products; sums exact for data of moderate dynamic
-    // range).  float32 sums with an error bound decide when both ends of the
+    // coefficient per token -- least squares <x, y> / <y, y>, or in norm-ratio mode
+    // sqrt(<x, x> / <y, y>) -- rounded to BF16 from the value of the float64 sums
+    // (exact products; sums exact for data of moderate dynamic range).  float32 sums with an error bound decide when both ends of the
     // bound round to the same BF16 value; otherwise the float64 sums do.
     {
       const int warp = tid / 32, lane = tid % 32;
       for (int t = warp; t < kTok; t += kThreads / 32) {
         if (!valid_s[t]) continue;   // same for every lane of the warp
+        // least squares: num = <x, y>, mag = sum |x y|; norm ratio: num = <x, x>
         float num = 0.f, den = 0.f, mag = 0.f;
         for (int k = lane; k < d; k += 32) {
           const float y = ref_s[t][k], x = x_s[t][k];
-          num = fmaf(x, y, num);
+          num = fmaf(x, norm_ratio ? x : y, num);
           den = fmaf(y, y, den);
           mag = fmaf(fabsf(x), fabsf(y), mag);
         }
@@ -344,8 +346,11 @@ __global__ void __launch_bounds__(kThreads) append_kernel(AppendArgs a) {
         uint16_t bits = 0;
         if (den > 0.f) {
           // at most 4 + 5 roundings per term (< 2^-20 relative to the sums of magnitudes)
-          const float c = __fdiv_rn(num, den);
-          const float err = (mag + fabsf(c) * den) * 0x1p-20f / den + fabsf(c) * 0x1p-22f;
+          // norm ratio: sums of squares carry at most 2^-20 relative error each, so the
+          // square root of their quotient is within 2^-19 (with its own rounding)
+          const float c = norm_ratio ? sqrtf(__fdiv_rn(num, den)) : __fdiv_rn(num, den);
+          const float err = norm_ratio ? c * 0x1p-19f
+                                       : (mag + fabsf(c) * den) * 0x1p-20f / den + fabsf(c) * 0x1p-22f;
           const __nv_bfloat16 lo = __float2bfloat16_rn(c - err), hi = __float2bfloat16_rn(c + err);
           const uint16_t blo = *reinterpret_cast<const uint16_t*>(&lo);
           const uint16_t bhi = *reinterpret_cast<const uint16_t*>(&hi);
@@ -357,14 +362,15 @@ __global__ void __launch_bounds__(kThreads) append_kernel(AppendArgs a) {
           double num64 = 0.0, den64 = 0.0;
           for (int k = lane; k < d; k += 32) {
             double y = ref_s[t][k], x = x_s[t][k];
-            num64 = fma(x, y, num64);
+            num64 = fma(x, norm_ratio ? x : y, num64);
             den64 = fma(y, y, den64);
           }
           for (int off = 16; off > 0; off >>= 1) {
             num64 += __shfl_xor_sync(0xffffffffu, num64, off);
             den64 += __shfl_xor_sync(0xffffffffu, den64, off);
           }
-          bits = f64_to_bf16_bits(den64 > 0.0 ? num64 / den64 : 0.0);
+          const double q64 = den64 > 0.0 ? num64 / den64 : 0.0;
+          bits = f64_to_bf16_bits(norm_ratio ? sqrt(q64) : q64);
         }
         if (lane == 0) {
           c_s[t] = bits;
@@ -439,7 +445,7 @@ cudaError_t launch_append(const rq_cache& c, int layer, int group, int batch,
   a.n = n_tokens;
   // aligned 16-position blocks touched by n tokens starting anywhere: at most ceil(n/16) + 1;
   // a short append in shared mode takes one CTA per (K/V, residual loop)
-  const bool split = c.geom.mode == RQ_MODE_SHARED && c.geom.P > 1 && n_tokens <= kTok;
+  const bool split = !(c.geom.mode & RQ_MODE_CHAINED) && c.geom.P > 1 && n_tokens <= kTok;
   dim3 grid((n_tokens + kTok - 1) / kTok + 1, batch * c.geom.H, split ? 2 * (c.geom.P - 1) : 2);
   if (c.geom.d == 128) return launch_dependent(append_kernel<128>, grid, dim3(kThreads), 0, stream, a);
   if (c.geom.d == 96) return launch_dependent(append_kernel<96>, grid, dim3(kThreads), 0, stream, a);

@@ -893,7 +893,7 @@ cudaError_t launch_decode(const rq_cache& c, int layer, int group, int loop, int
                           float* out, void* workspace, cudaStream_t stream) {
   if (batch > kMaxRows) return cudaErrorInvalidValue;
   const int P = c.geom.P;
-  const bool chained = c.geom.mode == RQ_MODE_CHAINED;
+  const bool chained = (c.geom.mode & RQ_MODE_CHAINED) != 0;
   const int nres = loop == P - 1 ? 0 : (chained ? P - 1 - loop : 1);
   if (nres > kMaxRes) return cudaErrorNotSupported;
   DecodeArgs a;

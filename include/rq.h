@@ -77,7 +77,11 @@ typedef enum rq_status {
 
 typedef enum rq_mode {
   RQ_MODE_SHARED = 0,   /* every earlier loop coded against the anchor: 2 plane reads per loop */
-  RQ_MODE_CHAINED = 1   /* loop l coded against the rebuilt loop l+1: reads grow with distance */
+  RQ_MODE_CHAINED = 1,  /* loop l coded against the rebuilt loop l+1: reads grow with distance */
+  RQ_MODE_NORM_RATIO = 2 /* flag, OR'd with one of the above: the stored coefficient is the
+                            norm ratio ||kv_l|| / ||ref|| (the scaling the arXiv summary lists
+                            beside least squares among its appendix comparisons) instead of
+                            the least-squares <kv_l, ref> / <ref, ref>; decode is unchanged */
 } rq_mode;
 
 /* Shape of one cache.  The anchor is 4-bit and residuals 2-bit (fixed). */
@@ -90,7 +94,7 @@ typedef struct rq_config {
   int32_t group_size;       /* g: 16 or 32 channels per quantization group */
   int32_t max_batch;        /* rows of the cache */
   int32_t max_seq_len;      /* token capacity per (layer, group, row, head) */
-  int32_t mode;             /* rq_mode */
+  int32_t mode;             /* rq_mode: SHARED or CHAINED, optionally | NORM_RATIO */
 } rq_config;
 
 typedef struct rq_cache rq_cache;   /* opaque host-side handle; holds no device memory */

@@ -31,12 +31,13 @@ __all__ = ["formats", "method", "layout", "Geometry", "TILE", "quantize", "dequa
 
 
 def append(buf: np.ndarray, geom: Geometry, R: np.ndarray, layer: int, group: int,
-           kv: np.ndarray, start, chained: bool = False, precision: str = "f32") -> dict:
+           kv: np.ndarray, start, chained: bool = False, precision: str = "f32",
+           scaling: str = "ls") -> dict:
     """Compress the P loops of n new tokens and write them at positions start[b].. .
 
     kv: float64 [P, 2, B, H, n, d] (exact BF16 values), anchor = last loop.
     Returns the compress_group result (codes, metadata, reconstructions)."""
-    comp = compress_group(kv, R, geom.group_size, chained=chained, precision=precision)
+    comp = compress_group(kv, R, geom.group_size, chained=chained, precision=precision, scaling=scaling)
     pack_group(buf, geom, layer, group, comp, np.asarray(start, dtype=np.int64))
     return comp
 

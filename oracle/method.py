@@ -132,7 +132,18 @@ def rotate_back_f32(R: np.ndarray, r: np.ndarray) -> np.ndarray:
     return acc
 
 
-def compress_group(x: np.ndarray, R: np.ndarray, g: int, chained: bool = False, precision: str = "f32"):
+def norm_ratio_coefficient(x: np.ndarray, y: np.ndarray) -> np.ndarray:
+    """c = ||x|| / ||y|| over the last axis, 0 where ||y|| == 0.  The scaling the
+    arXiv summary lists beside least squares among the appendix comparisons
+    (ablation paragraph); the pages give no formula, so this takes the plain
+    ratio of L2 norms, computed as sqrt(sum x^2 / sum y^2)."""
+    num = np.sum(x * x, axis=-1)
+    den = np.sum(y * y, axis=-1)
+    return np.where(den > 0, np.sqrt(num / np.where(den > 0, den, 1.0)), 0.0)
+
+
+def compress_group(x: np.ndarray, R: np.ndarray, g: int, chained: bool = False, precision: str = "f32",
+                   scaling: str = "ls"):
     """Compress the P loops of one loop group.
 
     x: float64 [P, ..., d], loop index first, the last loop is the anchor
@@ -140,6 +151,7 @@ def compress_group(x: np.ndarray, R: np.ndarray, g: int, chained: bool = False, 
     R: [d, d], the fixed rotation as the device receives it (binary32 values).
     precision: "f32" (the residual and rotation as the device computes them,
        see the module docstring) or "f64".
+    scaling: "ls" (least-squares coefficient, the method's) or "norm" (norm ratio).
     Returns a dict with
       anchor: (codes, scale_b, offset_b)
       res[j] for j in 0..P-2: (codes, scale_b, offset_b, c_bf16_bits)
@@ -158,7 +170,7 @@ def compress_group(x: np.ndarray, R: np.ndarray, g: int, chained: bool = False, 
     enc_ref = a_hat                                   # the encoder's reference (chained: rebuilt loop)
     for j in range(P - 2, -1, -1):
         ref = enc_ref if chained else a_hat
-        c = ls_coefficient(x[j], ref)
+        c = ls_coefficient(x[j], ref) if scaling == "ls" else norm_ratio_coefficient(x[j], ref)
         c_bits = bf16_encode(c)
         cb = bf16_decode(c_bits)[..., None]
         if precision == "f32":

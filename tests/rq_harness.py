@@ -26,6 +26,7 @@ class Case:
     Nmax: int = 256
     chained: bool = False
     seed: int = 0
+    scaling: str = "ls"      # "ls" (least squares) or "norm" (norm ratio)
 
     def workload(self, anchor_is_base=True):
         alphas = synth.OURO_ALPHAS if self.P == 4 and anchor_is_base else tuple(
@@ -49,7 +50,8 @@ class GpuCache:
         self.case = case
         self.device = device
         self.cfg = rq.rq_config(case.L, case.P, case.G, case.H, case.d, case.g, case.B, case.Nmax,
-                                rq.RQ_MODE_CHAINED if case.chained else rq.RQ_MODE_SHARED)
+                                (rq.RQ_MODE_CHAINED if case.chained else rq.RQ_MODE_SHARED)
+                                | (rq.RQ_MODE_NORM_RATIO if case.scaling == "norm" else 0))
         self.nbytes = rq.rq_cache_bytes(self.cfg)
         assert self.nbytes > 0
         self.buf = torch.zeros(self.nbytes, dtype=torch.uint8, device=device)

@@ -97,7 +97,8 @@ def _build_both(case: Case, chunks, seq_start=None, anchor_is_base=True):
             for ci, n in enumerate(chunks):
                 kv_bf16, kv = kv_for(case, seed * 1000 + layer * 100 + group * 10 + ci, n, anchor_is_base)
                 gpu.append(layer, group, kv_bf16, pos)
-                comp = oracle.append(obuf, geom, R, layer, group, kv, pos, chained=case.chained)
+                comp = oracle.append(obuf, geom, R, layer, group, kv, pos, chained=case.chained,
+                                     scaling=case.scaling)
                 if layer == 0 and group == 0:
                     for j in range(case.P - 1):
                         us[j] = comp["u"][j] if us[j] is None else np.concatenate([us[j], comp["u"][j]], axis=-2)
@@ -339,6 +340,24 @@ def test_large_chained_group_appends_and_decode_limit():
     with pytest.raises(rq.RqError) as e:
         gpu.decode(0, 0, 0, qb, kcb, vcb, np.array([100]), 0.1)
     assert e.value.status == 6   # RQ_ERR_UNSUPPORTED
+
+
+@pytest.mark.parametrize("chained", [False, True])
+def test_norm_ratio_scaling(chained):
+    """Norm-ratio coefficient (||x|| / ||ref||, the appendix alternative to least
+    squares): every cache byte equals the oracle's, and decode (unchanged: it uses
+    the stored coefficient) stays within tolerance."""
+    case = Case(L=1, P=4, G=1, H=3, d=128, g=32, B=2, Nmax=256, seed=31, chained=chained, scaling="norm")
+    gpu, geom, obuf, R, _ = _build_both(case, chunks=[200, 1])
+    gbuf = gpu.bytes_host()
+    assert np.array_equal(gbuf, obuf), f"{int((gbuf != obuf).sum())} cache bytes differ"
+    seq = np.array([201, 150])
+    for loop in range(4):
+        qb, q, kcb, kc, vcb, vc = _queries(case, 60, loop)
+        out = gpu.decode(0, 0, loop, qb, kcb, vcb, seq, 1 / math.sqrt(128)).cpu().numpy()
+        ref = oracle.decode_attention(obuf, geom, R, 0, 0, loop, q, kc, vc, seq, 1 / math.sqrt(128),
+                                      chained=chained)
+        assert np.abs(out - ref).max() <= ATOL
 
 
 def test_huginn_groups_and_layers():

@@ -61,7 +61,7 @@ def test_cache_bytes_matches_storage_accounting(rq):
 
 
 @pytest.mark.parametrize("kw", [dict(head_dim=64), dict(group_size=8), dict(head_dim=96, group_size=64),
-                                dict(loops_per_group=0), dict(loops_per_group=17), dict(mode=2),
+                                dict(loops_per_group=0), dict(loops_per_group=17), dict(mode=4),
                                 dict(num_heads=0), dict(max_seq_len=0)])
 def test_unsupported_shapes(rq, kw):
     cfg = _cfg(rq, **kw)

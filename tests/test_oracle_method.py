@@ -187,6 +187,43 @@ def test_reconstruction_error_is_the_residual_quantization_error(chained):
         assert rel < 0.5 * rel_direct
 
 
+def test_norm_ratio_coefficient():
+    """Norm ratio ||x|| / ||y||: exact for x = lambda * y (lambda a power of two),
+    equal to a separately computed norm quotient, 0 for a zero reference."""
+    rng = np.random.default_rng(5)
+    y = rng.standard_normal((3, 128)).astype(np.float32).astype(np.float64)
+    for lam in (0.5, -2.0, 4.0):      # powers of two scale every rounded sum exactly
+        c = M.norm_ratio_coefficient(lam * y, y)
+        assert np.all(c == abs(lam))
+    for lam in (0.75, -1.5, 3.0):
+        c = M.norm_ratio_coefficient(lam * y, y)
+        assert np.allclose(c, abs(lam), rtol=1e-15, atol=0)
+    x = rng.standard_normal((3, 128))
+    c = M.norm_ratio_coefficient(x, y)
+    want = np.linalg.norm(x, axis=-1) / np.linalg.norm(y, axis=-1)
+    assert np.allclose(c, want, rtol=1e-14, atol=0)
+    assert float(M.norm_ratio_coefficient(np.ones(8), np.zeros(8))) == 0.0
+    assert float(M.norm_ratio_coefficient(np.zeros(8), np.ones(8))) == 0.0
+
+
+@pytest.mark.parametrize("chained", [False, True])
+def test_compress_group_stores_the_norm_ratio(chained):
+    """In norm-ratio mode the stored BF16 coefficient of every loop is the norm ratio
+    of that loop against its reference (the dequantized anchor, or the rebuilt
+    next loop when chained), and never negative."""
+    _, kv = synth.looped_kv(8, synth.WORKLOADS["toy"], batch=1, ntok=5)
+    R = synth.rotation(128).astype(np.float32).astype(np.float64)
+    x = kv[:, 0]                                      # K: [P, 1, H, n, d]
+    comp = M.compress_group(x, R, 32, chained=chained, scaling="norm")
+    P = x.shape[0]
+    for j in range(P - 1):
+        ref = comp["recon"][j + 1] if chained else comp["recon"][P - 1]
+        c_bits = comp["res"][j][3]
+        if not chained:   # the encoder's reference is exactly the decoder's anchor
+            assert np.array_equal(c_bits, F.bf16_encode(M.norm_ratio_coefficient(x[j], ref)))
+        assert np.all(F.bf16_decode(c_bits) >= 0)
+
+
 def test_residual_uses_bf16_coefficient_and_dequantized_anchor():
     w = synth.WORKLOADS["toy"]
     _, kv = synth.looped_kv(1, w, batch=1, ntok=8)
