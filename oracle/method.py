@@ -20,7 +20,7 @@ Sources, by page and section:
          (group size 32/16, effective bits count codes, FP8 scale and
          offset and the BF16 coefficient).
 
-Readings of what the pages leave open (each one listed in the design doc):
+Readings of what the pages leave open:
   * group quantizer: asymmetric min/max.  offset o = E4M3(min), scale
     s = E4M3((max - min) / (2^b - 1)); both rounded BEFORE coding; codes are
     the nearest grid point o + k*s of the exact value (ties to even k),

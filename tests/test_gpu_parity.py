@@ -1,6 +1,6 @@
 """GPU parity: the CUDA library (through the C ABI) against the CPU oracle.
 
-Bars (from the benchmark spec of the method and the oracle's readings):
+Bars (the precision targets for this method and the oracle's readings):
   * anchor planes (INT4 codes, E4M3 metadata): bit-exact, byte for byte;
   * residual planes: the BF16 coefficient bytes bit-exact (shared mode);
     codes and metadata equal except where the oracle's own float64 rotated
@@ -357,6 +357,36 @@ def test_norm_ratio_scaling(chained):
         out = gpu.decode(0, 0, loop, qb, kcb, vcb, seq, 1 / math.sqrt(128)).cpu().numpy()
         ref = oracle.decode_attention(obuf, geom, R, 0, 0, loop, q, kc, vc, seq, 1 / math.sqrt(128),
                                       chained=chained)
+        assert np.abs(out - ref).max() <= ATOL
+
+
+def test_walsh_hadamard_rotation():
+    """A normalised Walsh-Hadamard matrix as R (Sylvester construction, d = 128): the
+    library takes any orthogonal R as a dense matrix, so the same append and decode
+    paths must match the oracle run with the same binary32 R."""
+    import decode_attention_rq_gb300 as rq
+    d = 128
+    Hm = np.array([[1.0]])
+    while Hm.shape[0] < d:
+        Hm = np.block([[Hm, Hm], [Hm, -Hm]])
+    R32 = (Hm / np.sqrt(d)).astype(np.float32)
+    R = R32.astype(np.float64)
+    assert np.abs(R @ R.T - np.eye(d)).max() < 1e-6
+    case = Case(L=1, P=4, G=1, H=2, d=d, g=32, B=2, Nmax=192, seed=33)
+    gpu = GpuCache(case, R32)
+    geom = _geom(case)
+    obuf = np.zeros(geom.total_bytes, dtype=np.uint8)
+    kv_bf16, kv = kv_for(case, 3301, 150)
+    start = np.zeros(case.B, dtype=np.int64)
+    gpu.append(0, 0, kv_bf16, start)
+    oracle.append(obuf, geom, R, 0, 0, kv, start)
+    gbuf = gpu.bytes_host()
+    assert np.array_equal(gbuf, obuf), f"{int((gbuf != obuf).sum())} cache bytes differ"
+    seq = np.array([150, 77])
+    for loop in range(4):
+        qb, q, kcb, kc, vcb, vc = _queries(case, 70, loop)
+        out = gpu.decode(0, 0, loop, qb, kcb, vcb, seq, 1 / math.sqrt(d)).cpu().numpy()
+        ref = oracle.decode_attention(obuf, geom, R, 0, 0, loop, q, kc, vc, seq, 1 / math.sqrt(d))
         assert np.abs(out - ref).max() <= ATOL
 
 
