@@ -54,3 +54,23 @@ def test_reference_arm_runs_on_rank0_only(monkeypatch, capsys):
     monkeypatch.setenv("RANK", "1")
     bench.run_reference(None, None)                  # returns before touching its arguments
     assert capsys.readouterr().out == ""
+
+
+def test_algorithmic_bytes_follow_the_record_sizes():
+    """The metric's denominator: per (token, row, head, layer) the four loop calls
+    of a shared-anchor group read 2 * (3 * (72 + 42) + 72) = 828 bytes at d = 128,
+    g = 32 (anchor record 64 + 8, residual record 32 + 8 + 2, K and V); chained
+    loop l reads the anchor and the residual planes of loops l .. P-2."""
+    import synth
+    w = synth.WORKLOADS["ouro8k"]
+    B, N = w.batch, w.context
+    rows = B * w.num_heads
+    small = rows * (3 * 128 * 2 + 128 * 4)
+    shared = bench.algorithmic_bytes_per_step(w, B, N)
+    assert shared["per_loop"] == [2 * (72 + 42) * N * rows + small] * 3 + [2 * 72 * N * rows + small]
+    append = rows * 2 * ((64 + 8) + 3 * (32 + 8 + 2)) + rows * 4 * 2 * 128 * 2
+    assert shared["step"] == w.num_layers * (sum(shared["per_loop"]) + append)
+    assert abs(shared["step"] - 10.42e9) / 10.42e9 < 0.01   # 828 B x 8192 x 64 x 24
+    chained = bench.algorithmic_bytes_per_step(w, B, N, chained=True)
+    assert chained["per_loop"][0] == 2 * (72 + 3 * 42) * N * rows + small
+    assert chained["per_loop"][2] == shared["per_loop"][2]
