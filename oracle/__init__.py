@@ -26,19 +26,20 @@ from .layout import Geometry, TILE, pack_group, read_plane_tokens, bits_per_elem
 
 __all__ = ["formats", "method", "layout", "Geometry", "TILE", "quantize", "dequantize",
            "ls_coefficient", "compress_group", "attention", "pack_group", "read_plane_tokens",
-           "bits_per_element", "append", "reconstruct", "decode_attention",
+           "bits_per_element", "append", "reconstruct", "decode_attention", "decode_attention_append",
            "e4m3_encode", "e4m3_decode", "e4m3_round", "bf16_encode", "bf16_decode", "bf16_round"]
 
 
 def append(buf: np.ndarray, geom: Geometry, R: np.ndarray, layer: int, group: int,
            kv: np.ndarray, start, chained: bool = False, precision: str = "f32",
-           scaling: str = "ls") -> dict:
+           scaling: str = "ls", rows=None) -> dict:
     """Compress the P loops of n new tokens and write them at positions start[b].. .
 
     kv: float64 [P, 2, B, H, n, d] (exact BF16 values), anchor = last loop.
+    rows: the batch rows to write (default: all).
     Returns the compress_group result (codes, metadata, reconstructions)."""
     comp = compress_group(kv, R, geom.group_size, chained=chained, precision=precision, scaling=scaling)
-    pack_group(buf, geom, layer, group, comp, np.asarray(start, dtype=np.int64))
+    pack_group(buf, geom, layer, group, comp, np.asarray(start, dtype=np.int64), rows=rows)
     return comp
 
 
@@ -88,3 +89,28 @@ def decode_attention(buf: np.ndarray, geom: Geometry, R: np.ndarray, layer: int,
         V = np.concatenate([V, v_cur[b, h][None, :]], axis=0)
         out[b, h] = attention(q[b, h], K, V, scale)
     return out
+
+
+def decode_attention_append(buf: np.ndarray, geom: Geometry, R: np.ndarray, layer: int, group: int,
+                            q: np.ndarray, kv_cur: np.ndarray, seq_lens, scale: float,
+                            chained: bool = False, scaling: str = "ls", precision: str = "f32"):
+    """The group's last-loop call followed by the current token's append.
+
+    [EXPL], temporary-buffer paragraph: the loops of the current token stay in
+    BF16 until the last loop (the anchor) has run; only then can the group be
+    coded against its anchor.  So the anchor-loop call attends over the cache as
+    it stands plus the BF16 token (decode_attention, loop P-1) and then the
+    token of every loop is compressed into slot seq_lens[b] (append, one token).
+    kv_cur: float64 [P, 2, B, H, d].  A row whose slot would pass the capacity
+    is attended but not appended.  Returns (out [B, H, d], appended [B] bool)."""
+    P = geom.loops_per_group
+    seq = np.asarray(seq_lens, dtype=np.int64)
+    out = decode_attention(buf, geom, R, layer, group, P - 1, q, kv_cur[P - 1, 0], kv_cur[P - 1, 1], seq, scale,
+                           chained=chained)
+    ok = (seq >= 0) & (seq + 1 <= geom.max_seq_len)
+    rows = [int(b) for b in np.nonzero(ok)[0]]
+    if rows:
+        append(buf, geom, R, layer, group, kv_cur[:, :, :, :, None, :], np.where(ok, seq, 0),
+               chained=chained, precision=precision, scaling=scaling, rows=rows)
+    return out, ok
+

@@ -152,17 +152,18 @@ def _c_addresses(geom: Geometry, plane_base: int, pos):
 
 
 def pack_group(buf: np.ndarray, geom: Geometry, layer: int, group: int, comp: dict,
-               start: np.ndarray):
+               start: np.ndarray, rows=None):
     """Write a compressed loop group into the cache bytes.
 
     comp: output of method.compress_group for x of shape [P, 2, B, H, n, d].
     start: int [B], first position written for each batch row.
+    rows: the batch rows to write (default: all).
     """
     a_codes, a_s, a_o = comp["anchor"]           # [2, B, H, n, d], [2, B, H, n, ng] x2
     _, B, H, n, d = a_codes.shape
     P = geom.loops_per_group
     for kv in range(2):
-        for b in range(B):
+        for b in (range(B) if rows is None else rows):
             pos = int(start[b]) + np.arange(n, dtype=np.int64)
             if n and pos[-1] >= geom.max_seq_len:
                 raise ValueError("append past max_seq_len")
