@@ -1,12 +1,12 @@
 """Decode-step benchmark of the ResidualQuant path on GB300.
 
 One step = what a looped model does to produce one token per sequence: for
-every loop and every layer one rq_decode_attention call over the compressed
-cache (plus the current token from the BF16 temporary buffer), and after each
-layer's last loop one rq_append(n=1) that compresses that token into the cache.
-Ouro-1.4B shape at 8k context: 24 layers x 4 loops = 96 attention calls and 24
-appends per step, batch 4, 16 heads of width 128, INT4 anchor / INT2 residuals,
-g = 32.  The cache is kept at a fixed length (each step overwrites the same
+every loop and every layer one attention call over the compressed cache (plus
+the current token from the BF16 temporary buffer); each layer's last-loop call
+(rq_decode_attention_append) also compresses that token, every loop of it,
+into the cache.  Ouro-1.4B shape at 8k context: 24 layers x 4 loops = 96
+attention calls per step, 24 of them appending, batch 4, 16 heads of width
+128, INT4 anchor / INT2 residuals, g = 32.  The cache is kept at a fixed length (each step overwrites the same
 next slot), so every step does the same work.
 
 Prints one JSON line.  `--impl reference` times the CPU oracle instead.
@@ -307,30 +307,18 @@ def run_rq(args, w):
     order = [(lp, layer, grp) for grp in range(G) for lp in range(P) for layer in range(L)]
 
     s = torch.cuda.Stream(device=dev)
-    # Each layer's append follows its last-loop attention call on a second stream: it
-    # writes only the new token's slot (which no attention call of the step reads; the
-    # channel-major words it rewrites keep the other tokens' fields), so it overlaps
-    # the next attention calls.  The step joins it before ending.
-    s_app = torch.cuda.Stream(device=dev)
-    ev_after = [torch.cuda.Event() for _ in range(L * G)]
-    ev_join = torch.cuda.Event()
 
     def step(stream=None):
-        i = k = 0
-        for (lp, layer, grp) in order:
+        for i, (lp, layer, grp) in enumerate(order):
             t = temp_all[layer * G + grp]
-            rq.rq_decode_attention(handle, layer, grp, lp, B, q_all[i], t[lp, 0, :, :, 0], t[lp, 1, :, :, 0], seq,
-                                   scale, out_all[i], ws, ws_bytes, s.cuda_stream)
-            i += 1
-            if lp == P - 1:
-                ev_after[k].record(s)
-                s_app.wait_event(ev_after[k])
-                rq.rq_append(handle, layer, grp, B, t, seq, 1, status, s_app.cuda_stream)
-                k += 1
-        ev_join.record(s_app)
-        s.wait_event(ev_join)
+            if lp == P - 1:   # the anchor loop: attention, then the token joins the cache
+                rq.rq_decode_attention_append(handle, layer, grp, B, q_all[i], t[..., 0, :], seq, scale, out_all[i],
+                                              ws, ws_bytes, s.cuda_stream)
+            else:
+                rq.rq_decode_attention(handle, layer, grp, lp, B, q_all[i], t[lp, 0, :, :, 0], t[lp, 1, :, :, 0],
+                                       seq, scale, out_all[i], ws, ws_bytes, s.cuda_stream)
 
-    launches_per_step = 3 * ncalls + L * G   # a decode call is qprep + decode + merge kernels
+    launches_per_step = 3 * ncalls   # a call is qprep + decode + merge kernels (the append runs in the merge)
     torch.cuda.synchronize()
     with torch.cuda.stream(s):
         step(s.cuda_stream)   # eager once (also sets kernel attributes before capture)

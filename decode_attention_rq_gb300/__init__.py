@@ -16,7 +16,7 @@ __all__ = [
     "rq_cache_bytes", "rq_cache_create", "rq_cache_destroy", "rq_append",
     "rq_decode_workspace_bytes", "rq_decode_attention", "rq_bf16_workspace_bytes",
     "rq_decode_attention_bf16", "rq_status_string", "EXPORTED_SYMBOLS",
-    "rq_decode_attention_noalloc", "RQ_NOALLOC_WORKSPACE_BYTES",
+    "rq_decode_attention_noalloc", "RQ_NOALLOC_WORKSPACE_BYTES", "rq_decode_attention_append",
 ]
 
 LIB_PATH = os.path.join(os.path.dirname(os.path.abspath(__file__)), "librq.so")
@@ -32,6 +32,7 @@ EXPORTED_SYMBOLS = (
     "rq_cache_bytes", "rq_cache_create", "rq_cache_destroy", "rq_append",
     "rq_decode_workspace_bytes", "rq_decode_attention", "rq_bf16_workspace_bytes",
     "rq_decode_attention_bf16", "rq_status_string", "rq_decode_attention_noalloc",
+    "rq_decode_attention_append",
 )
 
 # size of the workspace built into the library for rq_decode_attention_noalloc (rq.h)
@@ -70,6 +71,8 @@ lib.rq_decode_attention.argtypes = [_p, _i32, _i32, _i32, _i32, _p, _p, _p, _p, 
 lib.rq_decode_attention.restype = ctypes.c_int
 lib.rq_decode_attention_noalloc.argtypes = [_p, _i32, _i32, _i32, _i32, _p, _p, _p, _p, _f, _p, _p, _p]
 lib.rq_decode_attention_noalloc.restype = ctypes.c_int
+lib.rq_decode_attention_append.argtypes = [_p, _i32, _i32, _i32, _p, _p, _p, _f, _p, _p, _sz, _p]
+lib.rq_decode_attention_append.restype = ctypes.c_int
 lib.rq_bf16_workspace_bytes.argtypes = [_i32, _i32, _i32]
 lib.rq_bf16_workspace_bytes.restype = _sz
 lib.rq_decode_attention_bf16.argtypes = [_p, _p, _p, _p, _p, _p, _i32, _i32, _i32, _i32, _f, _p, _p, _sz, _p]
@@ -135,6 +138,15 @@ def rq_decode_attention(handle, layer, group, loop, batch, q, k_cur, v_cur, seq_
     _check("rq_decode_attention", lib.rq_decode_attention(
         handle, layer, group, loop, batch, _ptr(q), _ptr(k_cur), _ptr(v_cur), _ptr(seq_lens),
         softmax_scale, _ptr(out), _ptr(workspace), workspace_bytes, _stream(stream)))
+
+
+def rq_decode_attention_append(handle, layer, group, batch, q, kv_cur, seq_lens, softmax_scale, out, workspace,
+                               workspace_bytes, stream=None):
+    """Anchor-loop attention call that also appends the current token of every
+    loop (kv_cur: [P, 2, batch, H, d] bf16) at position seq_lens[b]."""
+    _check("rq_decode_attention_append", lib.rq_decode_attention_append(
+        handle, layer, group, batch, _ptr(q), _ptr(kv_cur), _ptr(seq_lens), softmax_scale, _ptr(out),
+        _ptr(workspace), workspace_bytes, _stream(stream)))
 
 
 def rq_decode_attention_noalloc(handle, layer, group, loop, batch, q, k_cur, v_cur, seq_lens, softmax_scale,

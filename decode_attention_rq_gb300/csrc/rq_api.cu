@@ -132,6 +132,29 @@ rq_status rq_decode_attention(rq_cache* cache, int32_t layer, int32_t group, int
   return e == cudaSuccess ? RQ_OK : RQ_ERR_CUDA;
 }
 
+rq_status rq_decode_attention_append(rq_cache* cache, int32_t layer, int32_t group, int32_t batch,
+                                     const void* q, const void* kv_cur, const int32_t* seq_lens,
+                                     float softmax_scale, float* out, void* workspace,
+                                     size_t workspace_bytes, void* stream) {
+  if (!cache || !q || !kv_cur || !seq_lens || !out || !workspace) return RQ_ERR_INVALID_ARG;
+  const Geom& g = cache->geom;
+  if (layer < 0 || layer >= g.L || group < 0 || group >= g.G || batch <= 0) return RQ_ERR_INVALID_ARG;
+  if (batch > g.Bmax) return RQ_ERR_CAPACITY;
+  if ((g.mode & RQ_MODE_CHAINED) && g.P > decode_max_chained_loops()) return RQ_ERR_UNSUPPORTED;
+  if (workspace_bytes < decode_workspace_bytes(g, batch, cache->num_sms)) return RQ_ERR_WORKSPACE;
+  if (!aligned16(q) || !aligned16(kv_cur) || !aligned16(seq_lens) || !aligned16(out) ||
+      !aligned16(workspace))
+    return RQ_ERR_ALIGNMENT;
+  // the anchor loop's K and V of the current token: blocks (P-1, 0) and (P-1, 1) of kv_cur
+  const auto* kv = static_cast<const __nv_bfloat16*>(kv_cur);
+  const size_t block = (size_t)batch * g.H * g.d;
+  const __nv_bfloat16* k_cur = kv + (size_t)(2 * (g.P - 1)) * block;
+  cudaError_t e = launch_decode(*cache, layer, group, g.P - 1, batch, static_cast<const __nv_bfloat16*>(q),
+                                k_cur, k_cur + block, seq_lens, softmax_scale, out, workspace,
+                                static_cast<cudaStream_t>(stream), kv);
+  return e == cudaSuccess ? RQ_OK : RQ_ERR_CUDA;
+}
+
 size_t rq_bf16_workspace_bytes(int32_t batch, int32_t num_heads, int32_t head_dim) {
   if (batch <= 0 || num_heads <= 0 || (head_dim != 96 && head_dim != 128)) return 0;
   return bf16_workspace_bytes(batch, num_heads, head_dim, current_sms());

@@ -44,6 +44,7 @@
 #include <cuda_fp8.h>
 
 #include "rq_internal.cuh"
+#include "rq_token_append.cuh"
 
 namespace rq {
 namespace {
@@ -57,7 +58,7 @@ constexpr float kFix = 32767.f;        // 16-bit fixed point: values in [-32767,
 constexpr int kPackWords = 36;         // query pack per (row, head, group): anchor 16, residual 16, 4 scalars
 constexpr int kPrepThreads = 256;
 constexpr int kMergeThreads = 256;
-constexpr int kMaxContrib = 1024;      // decode CTAs one merge can combine (the grid is smaller)
+constexpr int kMaxContrib = 512;       // decode CTAs one merge can combine (the grid is smaller)
 
 struct DecodeArgs {
   Geom g;
@@ -69,6 +70,7 @@ struct DecodeArgs {
   const int32_t* seq_lens;
   float* out;
   int32_t* status;
+  const __nv_bfloat16* kv_all;   // [P][2][batch][H][d]: the anchor-loop call also appends it; else NULL
   float* partials;       // [(C + batch*H)][pstride]: (m, l, acc_anchor[d], acc_residual[d])
   uint32_t* packs;       // [batch*H][NG][kPackWords]
   int pstride;
@@ -699,24 +701,49 @@ __global__ void __launch_bounds__(kThreads, (Cfg<D, GS, NRES>::MINB)) decode_ker
 
 // Combines the partial softmax states of (row, head) blockIdx.x: the CTAs that
 // held its units are recomputed from seq_lens with the decode kernel's split.
-template <int D, int NRES>
-__global__ void __launch_bounds__(kMergeThreads) merge_kernel(DecodeArgs a, int Cn) {
-  extern __shared__ __align__(16) float R_s[];   // [D][D] when NRES > 0
+// APPEND (anchor-loop call only): the grid has two CTAs per (row, head); they
+// also compress the current token's K (first CTA, which also merges) and V
+// (second CTA) into the cache at position seq_lens[row] (rq_token_append.cuh).
+// They run 128 threads of at most 32 registers, small enough to sit beside the
+// decode kernel's CTAs and do that work while those stream.
+template <int D, int NRES, bool APPEND>
+__global__ void __launch_bounds__(APPEND ? kAppendThreads : kMergeThreads, APPEND ? 16 : 0)
+    merge_kernel(DecodeArgs a, int Cn) {
+  static_assert(!APPEND || NRES == 0, "append runs in the anchor-loop merge");
+  constexpr int NT = APPEND ? kAppendThreads : kMergeThreads;
+  static_assert(NRES == 0 ? NT >= D : NT >= 2 * D, "a thread per accumulator element");
+  extern __shared__ __align__(16) float R_s[];   // [D][D] when NRES > 0; the append's scratch with APPEND
   __shared__ float w_s[kMaxContrib];
   __shared__ float l_s[kMaxContrib];
   __shared__ float va_s[D];
   __shared__ float vr_s[D];
   __shared__ float rt_s[D];
-  __shared__ float redf_s[kMergeThreads / 32];
-  __shared__ int redi_s[2][kMergeThreads / 32];
+  __shared__ float redf_s[NT / 32];
+  __shared__ int redi_s[2][NT / 32];
   __shared__ float ml_s[2];
   __shared__ uint64_t r_bar;
   constexpr int UTOK = 2 * kTile;
   pdl_launch_dependents();   // the next call's prep may start loading R; it waits for this kernel
   const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
-  const int bh = blockIdx.x, H = a.g.H, B = a.batch, b = bh / H, h = bh - b * H;
+  const int H = a.g.H, B = a.batch;
+  const int bh = APPEND ? blockIdx.x % (B * H) : blockIdx.x, b = bh / H, h = bh - b * H;
 
   // ---- before the wait: inputs the decode kernel does not write ----
+  bool app_ok = false;
+  int app_pos = 0;
+  const int app_kvi = APPEND ? blockIdx.x / (B * H) : 0;
+  uint8_t* app_smem = reinterpret_cast<uint8_t*>(R_s);
+  if constexpr (APPEND) {
+    app_pos = a.seq_lens[b];
+    app_ok = token_append_compute<D>(a.g, const_cast<uint8_t*>(a.base), a.R, a.kv_all, B, a.layer, a.group, b, h,
+                                     app_kvi, app_pos, a.status, app_smem);
+    if (app_kvi == 1) {   // the V half: store after the wait; the first CTA merges
+      pdl_wait();
+      if (app_ok)
+        token_append_store<D>(a.g, const_cast<uint8_t*>(a.base), a.layer, a.group, b, h, 1, app_pos, app_smem);
+      return;
+    }
+  }
   if (NRES > 0 && tid == 0) {   // R -> shared memory, one bulk copy (R is 16-byte aligned)
     mbar_init(&r_bar, 1);
     fence_mbar_init();
@@ -725,12 +752,12 @@ __global__ void __launch_bounds__(kMergeThreads) merge_kernel(DecodeArgs a, int 
   }
   // current token's score (base 2)
   float sc = 0.f;
-  for (int k = tid; k < D; k += kMergeThreads)
+  for (int k = tid; k < D; k += NT)
     sc += __bfloat162float(a.q[(size_t)bh * D + k]) * a.qscale *
           __bfloat162float(a.k_cur[(size_t)bh * D + k]);
   // units before this row and in total (same clamping and unit size as the decode kernel)
   int before = 0, total = 0;
-  for (int r = tid; r < B; r += kMergeThreads) {
+  for (int r = tid; r < B; r += NT) {
     const int nt = (clamp_len(a.seq_lens[r], a.g.Nmax) + UTOK - 1) / UTOK;
     total += H * nt;
     if (r < b) before += H * nt;
@@ -745,13 +772,16 @@ __global__ void __launch_bounds__(kMergeThreads) merge_kernel(DecodeArgs a, int 
   float s_cur = 0.f;
   int pre = 0, U = 0;
 #pragma unroll
-  for (int w = 0; w < kMergeThreads / 32; ++w) { s_cur += redf_s[w]; pre += redi_s[0][w]; U += redi_s[1][w]; }
+  for (int w = 0; w < NT / 32; ++w) { s_cur += redf_s[w]; pre += redi_s[0][w]; U += redi_s[1][w]; }
   const int ntb = (clamp_len(a.seq_lens[b], a.g.Nmax) + UTOK - 1) / UTOK;
   if (ntb == 0) {   // empty cache: attention over the current token alone
-    for (int k = tid; k < D; k += kMergeThreads)
+    for (int k = tid; k < D; k += NT)
       a.out[(size_t)bh * D + k] = __bfloat162float(a.v_cur[(size_t)bh * D + k]);
     if (NRES > 0) (void)mbar_wait_bounded(&r_bar, 0);   // the R copy lands before the CTA exits
     pdl_wait();   // completion of this kernel implies the decode kernel's
+    if constexpr (APPEND)
+      if (app_ok)
+        token_append_store<D>(a.g, const_cast<uint8_t*>(a.base), a.layer, a.group, b, h, 0, app_pos, app_smem);
     return;
   }
   const Split split{U / Cn, U % Cn};
@@ -760,11 +790,14 @@ __global__ void __launch_bounds__(kMergeThreads) merge_kernel(DecodeArgs a, int 
   const int nc = min(c_hi - c_lo + 1, kMaxContrib);
 
   pdl_wait();   // every partial of the decode kernel is written and visible
+  if constexpr (APPEND)   // no kernel before this one is running: the new slot can be written
+    if (app_ok)
+      token_append_store<D>(a.g, const_cast<uint8_t*>(a.base), a.layer, a.group, b, h, 0, app_pos, app_smem);
 
   // this thread's element of the first contributors' accumulators, loaded while
   // warp 0 reads the (m, l) pairs
   constexpr int PF = 8;
-  const bool acc_thread = tid < (NRES > 0 ? 2 * D : D);
+  const bool acc_thread = tid < (NRES > 0 ? 2 * D : D);   // NT covers them (static_assert above)
   const float* pc = a.partials + (size_t)(c_lo + bh) * a.pstride + 2 + tid;
   float xa[PF];
 #pragma unroll
@@ -835,14 +868,39 @@ template <int D, int GS, int NRES>
 cudaError_t launch_t(const DecodeArgs& a, int num_sms, cudaStream_t stream) {
   using C = Cfg<D, GS, NRES>;
   auto k = decode_kernel<D, GS, NRES>;
-  auto km = merge_kernel<D, (NRES > 0 ? 1 : 0)>;
+  auto km = merge_kernel<D, (NRES > 0 ? 1 : 0), false>;
+  size_t km_smem = NRES > 0 ? (size_t)D * D * sizeof(float) : 0;
+  int km_threads = kMergeThreads, km_ctas_per_bh = 1;
+  if constexpr (NRES == 0)
+    if (a.kv_all) {
+      km = merge_kernel<D, 0, true>;
+      km_smem = TokenAppendSmem::bytes(a.g.P);
+      km_threads = kAppendThreads;
+      km_ctas_per_bh = 2;
+    }
   constexpr size_t merge_smem = NRES > 0 ? (size_t)D * D * sizeof(float) : 0;
   static int per_sm = 0;   // resident decode CTAs per SM (registers and shared memory)
   if (per_sm == 0) {
     cudaError_t e = cudaFuncSetAttribute(k, cudaFuncAttributeMaxDynamicSharedMemorySize, C::SMEM);
     if (e != cudaSuccess) return e;
-    e = cudaFuncSetAttribute(km, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)merge_smem);
+    e = cudaFuncSetAttribute(merge_kernel<D, (NRES > 0 ? 1 : 0), false>,
+                             cudaFuncAttributeMaxDynamicSharedMemorySize, (int)merge_smem);
     if (e != cudaSuccess) return e;
+    // All kernels of a call ask for the largest shared-memory carveout: the SM's
+    // split between L1 and shared memory is fixed while CTAs are resident, so
+    // a kernel that asks for another split waits for SMs to drain instead of
+    // starting beside the kernel before it (its programmatic-dependent launch).
+    e = cudaFuncSetAttribute(k, cudaFuncAttributePreferredSharedMemoryCarveout, 100);
+    if (e != cudaSuccess) return e;
+    e = cudaFuncSetAttribute(qprep_kernel<D, GS, NRES>, cudaFuncAttributePreferredSharedMemoryCarveout, 100);
+    if (e != cudaSuccess) return e;
+    e = cudaFuncSetAttribute(merge_kernel<D, (NRES > 0 ? 1 : 0), false>, cudaFuncAttributePreferredSharedMemoryCarveout,
+                             100);
+    if (e != cudaSuccess) return e;
+    if constexpr (NRES == 0) {
+      e = cudaFuncSetAttribute(merge_kernel<D, 0, true>, cudaFuncAttributePreferredSharedMemoryCarveout, 100);
+      if (e != cudaSuccess) return e;
+    }
     int occ = 0;
     e = cudaOccupancyMaxActiveBlocksPerMultiprocessor(&occ, k, kThreads, C::SMEM);
     if (e != cudaSuccess) return e;
@@ -856,7 +914,7 @@ cudaError_t launch_t(const DecodeArgs& a, int num_sms, cudaStream_t stream) {
   if (e != cudaSuccess) return e;
   e = launch_dependent(k, dim3(grid), dim3(kThreads), (size_t)C::SMEM, stream, a);
   if (e != cudaSuccess) return e;
-  return launch_dependent(km, dim3(bhs), dim3(kMergeThreads), merge_smem, stream, a, grid);
+  return launch_dependent(km, dim3(km_ctas_per_bh * bhs), dim3(km_threads), km_smem, stream, a, grid);
 }
 
 template <int D, int GS>
@@ -890,7 +948,8 @@ size_t decode_workspace_bytes(const Geom& g, int batch, int num_sms) {
 cudaError_t launch_decode(const rq_cache& c, int layer, int group, int loop, int batch,
                           const __nv_bfloat16* q, const __nv_bfloat16* k_cur,
                           const __nv_bfloat16* v_cur, const int32_t* seq_lens, float scale,
-                          float* out, void* workspace, cudaStream_t stream) {
+                          float* out, void* workspace, cudaStream_t stream,
+                          const __nv_bfloat16* kv_all) {
   if (batch > kMaxRows) return cudaErrorInvalidValue;
   const int P = c.geom.P;
   const bool chained = (c.geom.mode & RQ_MODE_CHAINED) != 0;
@@ -905,6 +964,7 @@ cudaError_t launch_decode(const rq_cache& c, int layer, int group, int loop, int
   a.v_cur = v_cur;
   a.seq_lens = seq_lens;
   a.out = out;
+  a.kv_all = loop == P - 1 ? kv_all : nullptr;
   uint8_t* ws = static_cast<uint8_t*>(workspace);
   a.status = reinterpret_cast<int32_t*>(ws);
   a.partials = reinterpret_cast<float*>(ws + 256);

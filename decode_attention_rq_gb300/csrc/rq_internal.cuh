@@ -56,10 +56,13 @@ cudaError_t launch_append(const rq_cache& c, int layer, int group, int batch,
 
 size_t decode_workspace_bytes(const Geom& g, int batch, int num_sms);
 int decode_max_chained_loops();   // chained-mode decode reads at most this many loops' planes
+// kv_all (anchor loop only, else ignored): [P][2][batch][H][d] current token of
+// every loop, compressed into the cache at seq_lens[b] by the call's merge kernel
 cudaError_t launch_decode(const rq_cache& c, int layer, int group, int loop, int batch,
                           const __nv_bfloat16* q, const __nv_bfloat16* k_cur,
                           const __nv_bfloat16* v_cur, const int32_t* seq_lens, float scale,
-                          float* out, void* workspace, cudaStream_t stream);
+                          float* out, void* workspace, cudaStream_t stream,
+                          const __nv_bfloat16* kv_all = nullptr);
 
 size_t bf16_workspace_bytes(int batch, int heads, int d, int num_sms);
 cudaError_t launch_bf16(const __nv_bfloat16* k, const __nv_bfloat16* v,

@@ -168,6 +168,30 @@ rq_status rq_decode_attention(rq_cache* cache, int32_t layer, int32_t group, int
                               const int32_t* seq_lens, float softmax_scale, float* out,
                               void* workspace, size_t workspace_bytes, void* stream);
 
+/* The group's last-loop (anchor-loop) call and the current token's append in
+ * one call: the same output as rq_decode_attention(loop = P-1) and then the
+ * same cache bytes as rq_append(n_tokens = 1) with the same kv_cur.  The
+ * explainer's temporary-buffer paragraph: the current token of every loop
+ * stays in BF16 until the anchor loop has produced its K/V; that is the moment
+ * this call compresses it.  The merge kernel of the call does the append, one
+ * CTA per (row, head); it computes while the attention kernel still streams
+ * the cache and writes the new slot only after that kernel has finished.
+ *   q          device bf16 [batch][H][d], query of loop P-1
+ *   kv_cur     device bf16 [P][2][batch][H][d] (loop, K/V, row, head, channel):
+ *              the current token of every loop (rq_append's kv with
+ *              n_tokens = 1); its loop P-1 blocks are the attention's k_cur, v_cur
+ *   seq_lens   device int32 [batch]: tokens already cached; the attention reads
+ *              them and the token is written at position seq_lens[b] (not
+ *              modified; the caller advances it afterwards).  A row with
+ *              seq_lens[b] + 1 > max_seq_len is attended but not appended, and
+ *              the workspace's status word gets [1] = 1.
+ *   softmax_scale, out, workspace, workspace_bytes: as rq_decode_attention
+ * Errors: as rq_decode_attention. */
+rq_status rq_decode_attention_append(rq_cache* cache, int32_t layer, int32_t group, int32_t batch,
+                                     const void* q, const void* kv_cur, const int32_t* seq_lens,
+                                     float softmax_scale, float* out, void* workspace,
+                                     size_t workspace_bytes, void* stream);
+
 /* Size of the workspace built into the library for rq_decode_attention_noalloc
  * (2 MiB of device memory, held on every device that loads the library until
  * the process exits).  With 152 SMs, head_dim 128 and group size 32 it

@@ -89,6 +89,18 @@ class GpuCache:
                                     out, self.ws, self.ws_bytes)
         return out
 
+    def decode_append(self, layer, group, q, kv_cur, seq_lens, scale, batch=None):
+        """Anchor-loop call that also appends kv_cur ([P, 2, batch, H, d] or with a
+        token axis of 1 before d) at position seq_lens[b]."""
+        batch = self.case.B if batch is None else batch
+        q = q.to(self.device).contiguous()
+        kv = kv_cur.to(self.device).contiguous()
+        sl = torch.as_tensor(np.asarray(seq_lens, dtype=np.int32), device=self.device)
+        out = torch.empty((batch, self.case.H, self.case.d), dtype=torch.float32, device=self.device)
+        self.rq.rq_decode_attention_append(self.handle, layer, group, batch, q, kv, sl, scale, out, self.ws,
+                                           self.ws_bytes)
+        return out
+
     def bytes_host(self) -> np.ndarray:
         torch.cuda.synchronize()
         return self.buf.cpu().numpy()
