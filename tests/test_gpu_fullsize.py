@@ -6,10 +6,13 @@ filled at the workload's batch, head count and context; a few (row, head)
 slices are drawn from synth.looped_kv_slice and the rest from the device
 generator.  The decode calls run at the full batch (so the grid, the work
 split and the merge are those of the benchmark), with one row shorter than the
-others.  For every sampled slice the oracle compresses the same values on its
-own and attends over them for every loop; the test checks
+others; as in the benchmark's step, the anchor loop's call also appends the
+current token (rq_decode_attention_append).  For every sampled slice the
+oracle compresses the same values on its own, attends over them for every
+loop and appends the token; the test checks
 
-  * the slice's cache region, byte for byte (codes, metadata, coefficients);
+  * the slice's cache region, byte for byte (codes, metadata, coefficients,
+    the appended slot included);
   * the decode output of every loop, max |gpu - oracle| <= 2e-3.
 
 The oracle slices run in a spawned process pool while the device side runs.
@@ -115,12 +118,17 @@ def _device_case(w, chained, samples, seed):
     scale = synth.softmax_scale(d)
     ins = _inputs(w, seed)
     outs = {}
+    # the current token of every loop, [P, 2, B, H, d]: the anchor-loop call appends it
+    kv_all = torch.stack([torch.stack([ins[l][1][0], ins[l][2][0]]) for l in range(P)]).to(dev).contiguous()
     for loop in range(P):
         (q, _), (kc, _), (vc, _) = ins[loop]
         q, kc, vc = q.to(dev), kc.to(dev), vc.to(dev)
         for grp in groups:
             out = torch.empty((B, H, d), dtype=torch.float32, device=dev)
-            rq.rq_decode_attention(handle, 0, grp, loop, B, q, kc, vc, sl, scale, out, ws, ws_bytes)
+            if loop < P - 1:
+                rq.rq_decode_attention(handle, 0, grp, loop, B, q, kc, vc, sl, scale, out, ws, ws_bytes)
+            else:
+                rq.rq_decode_attention_append(handle, 0, grp, B, q, kv_all, sl, scale, out, ws, ws_bytes)
             outs[(grp, loop)] = out.cpu().numpy()
     torch.cuda.synchronize()
     assert status.tolist() == [0, 0, 0, 0]
