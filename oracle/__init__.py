@@ -21,24 +21,25 @@ import numpy as np
 
 from . import formats, method, layout
 from .formats import (e4m3_encode, e4m3_decode, e4m3_round, bf16_encode, bf16_decode, bf16_round)
-from .method import quantize, dequantize, ls_coefficient, compress_group, attention
+from .method import quantize, dequantize, ls_coefficient, compress_group, attention, hadamard_matrix
 from .layout import Geometry, TILE, pack_group, read_plane_tokens, bits_per_element
 
 __all__ = ["formats", "method", "layout", "Geometry", "TILE", "quantize", "dequantize",
-           "ls_coefficient", "compress_group", "attention", "pack_group", "read_plane_tokens",
+           "ls_coefficient", "compress_group", "attention", "hadamard_matrix", "pack_group", "read_plane_tokens",
            "bits_per_element", "append", "reconstruct", "decode_attention", "decode_attention_append",
            "e4m3_encode", "e4m3_decode", "e4m3_round", "bf16_encode", "bf16_decode", "bf16_round"]
 
 
 def append(buf: np.ndarray, geom: Geometry, R: np.ndarray, layer: int, group: int,
            kv: np.ndarray, start, chained: bool = False, precision: str = "f32",
-           scaling: str = "ls", rows=None) -> dict:
+           scaling: str = "ls", rows=None, rotation: str = "dense") -> dict:
     """Compress the P loops of n new tokens and write them at positions start[b].. .
 
     kv: float64 [P, 2, B, H, n, d] (exact BF16 values), anchor = last loop.
     rows: the batch rows to write (default: all).
     Returns the compress_group result (codes, metadata, reconstructions)."""
-    comp = compress_group(kv, R, geom.group_size, chained=chained, precision=precision, scaling=scaling)
+    comp = compress_group(kv, R, geom.group_size, chained=chained, precision=precision, scaling=scaling,
+                          rotation=rotation)
     pack_group(buf, geom, layer, group, comp, np.asarray(start, dtype=np.int64), rows=rows)
     return comp
 
@@ -93,7 +94,8 @@ def decode_attention(buf: np.ndarray, geom: Geometry, R: np.ndarray, layer: int,
 
 def decode_attention_append(buf: np.ndarray, geom: Geometry, R: np.ndarray, layer: int, group: int,
                             q: np.ndarray, kv_cur: np.ndarray, seq_lens, scale: float,
-                            chained: bool = False, scaling: str = "ls", precision: str = "f32"):
+                            chained: bool = False, scaling: str = "ls", precision: str = "f32",
+                            rotation: str = "dense"):
     """The group's last-loop call followed by the current token's append.
 
     [EXPL], temporary-buffer paragraph: the loops of the current token stay in
@@ -111,6 +113,6 @@ def decode_attention_append(buf: np.ndarray, geom: Geometry, R: np.ndarray, laye
     rows = [int(b) for b in np.nonzero(ok)[0]]
     if rows:
         append(buf, geom, R, layer, group, kv_cur[:, :, :, :, None, :], np.where(ok, seq, 0),
-               chained=chained, precision=precision, scaling=scaling, rows=rows)
+               chained=chained, precision=precision, scaling=scaling, rows=rows, rotation=rotation)
     return out, ok
 

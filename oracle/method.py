@@ -40,6 +40,16 @@ Readings of what the pages leave open:
     (acc_i = sum_k R[k,i] r_hat_k in order, then fma(c_b, ref, acc)).
     precision="f64" keeps the float64 reading of the same formulas, used to
     bound the binary32 one.
+  * Walsh-Hadamard rotation (rotation="hadamard", d a power of two): R =
+    H_d / sqrt(d), H_d the Sylvester Hadamard matrix (entry (i, k) =
+    (-1)^popcount(i & k)).  The explainer's related-explainers list points to a
+    2-bit KV cache built on a Hadamard rotation, and the summary's ablation
+    paragraph compares rotation methods with the rotation fixed offline; H_d /
+    sqrt(d) is one fixed orthogonal R that needs no d x d product.  In
+    binary32 it is taken as the fast transform computes it: butterfly stages
+    h = 1, 2, 4, ..., d/2, each pair (j, j + h) with j & h == 0 becoming
+    (a + b, a - b) rounded to binary32, then one binary32 product with the
+    binary32 value of 1/sqrt(d).  R is symmetric, so R^T is the same transform.
 """
 from __future__ import annotations
 
@@ -48,7 +58,8 @@ import numpy as np
 from .formats import e4m3_round, e4m3_encode, e4m3_decode, bf16_round, bf16_encode, bf16_decode, fma_f32
 
 __all__ = ["quantize", "dequantize", "ls_coefficient", "compress_group", "attention",
-           "rotate_f32", "rotate_back_f32", "ANCHOR_BITS", "RESIDUAL_BITS"]
+           "rotate_f32", "rotate_back_f32", "hadamard_matrix", "fwht_f32", "hadamard_f32",
+           "ANCHOR_BITS", "RESIDUAL_BITS"]
 
 ANCHOR_BITS = 4     # [EXPL] worked example; [SUMM] overview (INT4 anchor)
 RESIDUAL_BITS = 2   # [EXPL] worked example; [SUMM] overview (INT2 residuals)
@@ -132,6 +143,40 @@ def rotate_back_f32(R: np.ndarray, r: np.ndarray) -> np.ndarray:
     return acc
 
 
+def hadamard_matrix(d: int) -> np.ndarray:
+    """H_d / sqrt(d) in float64 (d a power of two), from the Sylvester recursion
+    H_2n = [[H_n, H_n], [H_n, -H_n]]."""
+    if d < 1 or d & (d - 1):
+        raise ValueError("the Walsh-Hadamard rotation needs d a power of two")
+    H = np.ones((1, 1))
+    while H.shape[0] < d:
+        H = np.block([[H, H], [H, -H]])
+    return H / np.sqrt(d)
+
+
+def fwht_f32(e: np.ndarray) -> np.ndarray:
+    """Unnormalized fast Walsh-Hadamard transform over the last axis in binary32:
+    for h = 1, 2, 4, ..., d/2 every pair (j, j + h) with j & h == 0 becomes
+    (a + b, a - b), each sum rounded to binary32."""
+    v = np.array(e, dtype=np.float32)
+    d = v.shape[-1]
+    lead = v.shape[:-1]
+    h = 1
+    while h < d:
+        w = v.reshape(lead + (d // (2 * h), 2, h))
+        a, b = w[..., 0, :], w[..., 1, :]
+        v = np.stack([a + b, a - b], axis=-2).reshape(lead + (d,))
+        h *= 2
+    return v
+
+
+def hadamard_f32(e: np.ndarray) -> np.ndarray:
+    """u = H_d e / sqrt(d) in binary32: the butterflies, then one product with the
+    binary32 value of 1/sqrt(d); returns float32."""
+    d = np.asarray(e).shape[-1]
+    return (fwht_f32(e) * np.float32(1.0 / np.sqrt(d))).astype(np.float32)
+
+
 def norm_ratio_coefficient(x: np.ndarray, y: np.ndarray) -> np.ndarray:
     """c = ||x|| / ||y|| over the last axis, 0 where ||y|| == 0.  The scaling the
     arXiv summary lists beside least squares among the appendix comparisons
@@ -143,7 +188,7 @@ def norm_ratio_coefficient(x: np.ndarray, y: np.ndarray) -> np.ndarray:
 
 
 def compress_group(x: np.ndarray, R: np.ndarray, g: int, chained: bool = False, precision: str = "f32",
-                   scaling: str = "ls"):
+                   scaling: str = "ls", rotation: str = "dense"):
     """Compress the P loops of one loop group.
 
     x: float64 [P, ..., d], loop index first, the last loop is the anchor
@@ -152,6 +197,8 @@ def compress_group(x: np.ndarray, R: np.ndarray, g: int, chained: bool = False, 
     precision: "f32" (the residual and rotation as the device computes them,
        see the module docstring) or "f64".
     scaling: "ls" (least-squares coefficient, the method's) or "norm" (norm ratio).
+    rotation: "dense" (u = R e as given) or "hadamard" (R must then be
+       hadamard_matrix(d); the binary32 path takes the fast transform).
     Returns a dict with
       anchor: (codes, scale_b, offset_b)
       res[j] for j in 0..P-2: (codes, scale_b, offset_b, c_bf16_bits)
@@ -175,7 +222,7 @@ def compress_group(x: np.ndarray, R: np.ndarray, g: int, chained: bool = False, 
         cb = bf16_decode(c_bits)[..., None]
         if precision == "f32":
             e = fma_f32(-cb, ref, x[j])               # residual, one binary32 rounding
-            u = rotate_f32(R, e).astype(np.float64)
+            u = (hadamard_f32(e) if rotation == "hadamard" else rotate_f32(R, e)).astype(np.float64)
         else:
             e = x[j] - cb * ref
             u = e @ R.T
@@ -185,7 +232,8 @@ def compress_group(x: np.ndarray, R: np.ndarray, g: int, chained: bool = False, 
         recon[j] = cb * dec_ref + r_hat @ R           # R^T r_hat for each vector, float64
         if chained:
             if precision == "f32":
-                enc_ref = fma_f32(cb, enc_ref, rotate_back_f32(R, r_hat)).astype(np.float64)
+                back = hadamard_f32(r_hat) if rotation == "hadamard" else rotate_back_f32(R, r_hat)
+                enc_ref = fma_f32(cb, enc_ref, back).astype(np.float64)
             else:
                 enc_ref = recon[j]
         res[j] = (r_codes, r_s, r_o, c_bits)

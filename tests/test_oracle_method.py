@@ -323,3 +323,66 @@ def test_f32_and_f64_readings_agree_up_to_rounding(chained):
         assert np.allclose(c32["u"][j], c64["u"][j], rtol=0, atol=1e-4)
         diff = (c32["res"][j][0] != c64["res"][j][0]).mean()
         assert diff < 1e-3
+
+
+# ---- Walsh-Hadamard rotation ----
+
+def _popcount_hadamard(d):
+    """H_d by its entry formula (-1)^popcount(i & k), independent of the recursion
+    and of the butterflies."""
+    i = np.arange(d)
+    bits = np.bitwise_and(i[:, None], i[None, :])
+    pc = np.zeros_like(bits)
+    for b in range(int(np.log2(d))):
+        pc += (bits >> b) & 1
+    return np.where(pc % 2 == 0, 1.0, -1.0)
+
+
+@pytest.mark.parametrize("d", [2, 8, 128])
+def test_fwht_is_the_sylvester_matrix_exactly(d):
+    """On small integers every butterfly sum is exact in binary32, so the fast
+    transform must equal H_d e exactly; a wrong pairing, sign or stage order fails."""
+    rng = np.random.default_rng(d)
+    e = rng.integers(-50, 50, size=(6, d)).astype(np.float64)
+    H = _popcount_hadamard(d)
+    assert np.array_equal(M.fwht_f32(e).astype(np.float64), e @ H.T)
+    assert np.array_equal(M.hadamard_matrix(d) * np.sqrt(d), H)
+    assert np.array_equal(H @ H.T, d * np.eye(d))
+
+
+def test_hadamard_rotation_close_to_the_dense_product():
+    """Random data: the binary32 transform is within a few roundings of the float64
+    product, keeps norms (orthogonal), and is its own inverse (symmetric R)."""
+    rng = np.random.default_rng(11)
+    e = rng.standard_normal((50, 128))
+    R = M.hadamard_matrix(128)
+    u32 = M.hadamard_f32(e).astype(np.float64)
+    u64 = e @ R.T
+    assert np.abs(u32 - u64).max() <= 1e-5 * np.abs(e).max()
+    assert np.allclose(np.linalg.norm(u32, axis=-1), np.linalg.norm(e, axis=-1), rtol=1e-6)
+    back = M.hadamard_f32(u32).astype(np.float64)
+    assert np.abs(back - e).max() <= 1e-5 * np.abs(e).max()
+    assert np.float32(1.0 / np.sqrt(128)) == np.float32(float.fromhex("0x1.6a09e6p-4"))
+
+
+@pytest.mark.parametrize("chained", [False, True])
+def test_compress_group_with_hadamard_rotation(chained):
+    """The binary32 fast-transform path and the float64 dense reading of the same
+    R give the same codes except at rounding boundaries; the reconstruction
+    error of a loop equals its residual's quantization error (R orthogonal,
+    R^T used to rebuild)."""
+    w = synth.Workload("t", 1, 4, 1, 2, 128, 32, 2, 64, synth.OURO_ALPHAS, True)
+    _, kv = synth.looped_kv(3, w, batch=2, ntok=40)
+    R = M.hadamard_matrix(128)
+    c32 = M.compress_group(kv, R, 32, chained=chained, rotation="hadamard")
+    c64 = M.compress_group(kv, R, 32, chained=chained, precision="f64", rotation="hadamard")
+    same = np.mean([np.mean(c32["res"][j][0] == c64["res"][j][0]) for j in range(3)])
+    assert same > 0.99
+    for j in range(3):
+        if chained:
+            continue   # the reference itself carries the later loops' errors
+        # x_j = cb a_hat + R^T u, so ||recon_j - x_j|| = ||r_hat - u|| for an orthogonal R
+        r_hat = M.dequantize(*c64["res"][j][:3], 32)
+        lhs = np.linalg.norm(c64["recon"][j] - kv[j], axis=-1)
+        rhs = np.linalg.norm(r_hat - c64["u"][j], axis=-1)
+        assert np.allclose(lhs, rhs, rtol=1e-9, atol=1e-12)
