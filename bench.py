@@ -223,11 +223,12 @@ def run_reference(args, w):
     print(json.dumps(line))
 
 
-def _config(w, chained=False):
+def _config(w, chained=False, hadamard=False):
     return {"workload": f"{w.name}: {w.num_layers} layers x {w.loops_per_group} loops x {w.num_groups} groups, "
                         f"{w.num_heads} KV heads x {w.head_dim}, batch {w.batch}, {w.context}-token context, "
                         f"INT4 anchor + INT2 residuals, group {w.group_size}, "
-                        f"{'chained' if chained else 'shared'} anchor",
+                        f"{'chained' if chained else 'shared'} anchor"
+                        + (", Walsh-Hadamard rotation" if hadamard else ""),
             "global_batch": w.batch, "seq_len": w.context, "parallelism": "replicas",
             "l2": "inputs larger than L2 (every step streams the whole compressed cache)"}
 
@@ -248,6 +249,8 @@ def main():
                     help="seconds of oracle work per reference step (default: about 150 s per run)")
     ap.add_argument("--quiet", action="store_true")
     ap.add_argument("--chained", action="store_true", help="chained anchors (loop l coded against loop l+1)")
+    ap.add_argument("--hadamard", action="store_true",
+                    help="Walsh-Hadamard rotation applied as a fast transform (head_dim 128)")
     ap.add_argument("--layers", type=int, default=None,
                     help="fewer layers than the workload (a small case for profiler captures)")
     args = ap.parse_args()
@@ -278,8 +281,9 @@ def run_rq(args, w):
                               w.group_size, w.batch, w.context)
     gen = torch.Generator(device=dev)
     gen.manual_seed(1234 + rank)
-    R32 = torch.from_numpy(synth.rotation(d).astype(np.float32)).to(dev)
-    cfg = rq.rq_config(L, P, G, H, d, g, B, N + 64, rq.RQ_MODE_CHAINED if args.chained else rq.RQ_MODE_SHARED)
+    R32 = None if args.hadamard else torch.from_numpy(synth.rotation(d).astype(np.float32)).to(dev)
+    cfg = rq.rq_config(L, P, G, H, d, g, B, N + 64, (rq.RQ_MODE_CHAINED if args.chained else rq.RQ_MODE_SHARED)
+                       | (rq.RQ_MODE_HADAMARD if args.hadamard else 0))
     nbytes = rq.rq_cache_bytes(cfg)
     cache_buf = torch.empty(nbytes, dtype=torch.uint8, device=dev)
     handle = rq.rq_cache_create(cfg, cache_buf, nbytes, R32)
@@ -387,7 +391,8 @@ def run_rq(args, w):
         try:
             tj = json.load(open(tp))
             if (tj.get("workload") == w.name and tj.get("batch") == B and tj.get("group_size") == g
-                    and not args.chained and tj.get("kernel_source_hash") == _kernel_hash()):
+                    and not args.chained and not args.hadamard
+                    and tj.get("kernel_source_hash") == _kernel_hash()):
                 traffic = tj.get("bytes_per_launch")
         except Exception:
             traffic = None
@@ -397,7 +402,7 @@ def run_rq(args, w):
     line = {
         "metric": METRIC, "value": value, "unit": "tokens/s", "n_gpus": world, "steps": args.steps,
         "warmup": args.warmup, "ms_per_step": ms_step, "higher_is_better": True, "scaling": "weak",
-        "vs_baseline": None, "dtype": "int32/fp32", "data": "synthetic", "config": _config(w, args.chained),
+        "vs_baseline": None, "dtype": "int32/fp32", "data": "synthetic", "config": _config(w, args.chained, args.hadamard),
         "effective_gbps": step_gbs, "frac_of_hbm_peak": step_gbs / peak,
         "roofline": {"bound": "hbm", "achieved": achieved, "peak": peak, "unit": "GB/s",
                      "frac": achieved / peak, "traffic": traffic,

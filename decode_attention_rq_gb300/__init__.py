@@ -12,7 +12,8 @@ import ctypes
 import os
 
 __all__ = [
-    "RQ_OK", "RQ_MODE_SHARED", "RQ_MODE_CHAINED", "RQ_MODE_NORM_RATIO", "RqError", "rq_config", "lib", "LIB_PATH",
+    "RQ_OK", "RQ_MODE_SHARED", "RQ_MODE_CHAINED", "RQ_MODE_NORM_RATIO", "RQ_MODE_HADAMARD", "RqError", "rq_config",
+    "lib", "LIB_PATH",
     "rq_cache_bytes", "rq_cache_create", "rq_cache_destroy", "rq_append",
     "rq_decode_workspace_bytes", "rq_decode_attention", "rq_bf16_workspace_bytes",
     "rq_decode_attention_bf16", "rq_status_string", "EXPORTED_SYMBOLS",
@@ -25,6 +26,7 @@ RQ_OK = 0
 RQ_MODE_SHARED = 0
 RQ_MODE_CHAINED = 1
 RQ_MODE_NORM_RATIO = 2   # flag: norm-ratio coefficient instead of least squares
+RQ_MODE_HADAMARD = 4     # flag: R = H_d / sqrt(d) as a fast Walsh-Hadamard transform (d = 128); R_dev may be None
 _STATUS_NAMES = {0: "RQ_OK", 1: "RQ_ERR_INVALID_ARG", 2: "RQ_ERR_ALIGNMENT", 3: "RQ_ERR_CAPACITY",
                  4: "RQ_ERR_WORKSPACE", 5: "RQ_ERR_CUDA", 6: "RQ_ERR_UNSUPPORTED", 7: "RQ_ERR_TIMEOUT"}
 

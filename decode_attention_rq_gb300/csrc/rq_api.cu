@@ -14,7 +14,8 @@ bool make_geom(const rq_config& c, Geom* g) {
   if (c.head_dim != 96 && c.head_dim != 128) return false;
   if (c.group_size != 16 && c.group_size != 32) return false;
   if (c.head_dim % c.group_size) return false;
-  if (c.mode & ~(RQ_MODE_CHAINED | RQ_MODE_NORM_RATIO)) return false;
+  if (c.mode & ~(RQ_MODE_CHAINED | RQ_MODE_NORM_RATIO | RQ_MODE_HADAMARD)) return false;
+  if ((c.mode & RQ_MODE_HADAMARD) && c.head_dim != 128) return false;   // a power of two
   g->L = c.num_layers;
   g->P = c.loops_per_group;
   g->G = c.num_groups;
@@ -60,11 +61,13 @@ size_t rq_cache_bytes(const rq_config* cfg) {
 
 rq_status rq_cache_create(const rq_config* cfg, void* dev_buf, size_t bytes, const float* R_dev,
                           rq_cache** out) {
-  if (!cfg || !dev_buf || !R_dev || !out) return RQ_ERR_INVALID_ARG;
+  if (!cfg || !dev_buf || !out) return RQ_ERR_INVALID_ARG;
+  const bool hadamard = (cfg->mode & RQ_MODE_HADAMARD) != 0;
+  if (!R_dev && !hadamard) return RQ_ERR_INVALID_ARG;
   Geom g;
   if (!make_geom(*cfg, &g)) return RQ_ERR_UNSUPPORTED;
   if (bytes < rq_cache_bytes(cfg)) return RQ_ERR_CAPACITY;
-  if (!aligned16(dev_buf) || !aligned16(R_dev)) return RQ_ERR_ALIGNMENT;
+  if (!aligned16(dev_buf) || (R_dev && !aligned16(R_dev))) return RQ_ERR_ALIGNMENT;
   rq_cache* c = new (std::nothrow) rq_cache;
   if (!c) return RQ_ERR_INVALID_ARG;
   c->cfg = *cfg;

@@ -137,6 +137,19 @@ __device__ __forceinline__ void rotate_rows(const float* R, int i, const float (
   for (int t = 0; t < NT; ++t) u[t][i] = acc[t];
 }
 
+// u[t] = H e[t] / sqrt(128) for the first NT token slots (RQ_MODE_HADAMARD, d =
+// 128, thread = channel); every thread of the CTA calls it.  scratch: NT x 128
+// floats of shared memory, may be u itself.
+template <int NT>
+__device__ __forceinline__ void hadamard_rows(int i, const float (*e)[128], float (*u)[128], float* scratch) {
+  float v[NT];
+#pragma unroll
+  for (int t = 0; t < NT; ++t) v[t] = e[t][i];
+  hadamard128<NT>(v, i, scratch);
+#pragma unroll
+  for (int t = 0; t < NT; ++t) u[t][i] = v[t];
+}
+
 template <int D>
 __global__ void __launch_bounds__(kThreads) append_kernel(AppendArgs a) {
   constexpr int d = D;
@@ -146,6 +159,7 @@ __global__ void __launch_bounds__(kThreads) append_kernel(AppendArgs a) {
   const bool split = gridDim.z > 2;   // this CTA codes residual loop jz only
   const bool chained = (a.g.mode & RQ_MODE_CHAINED) != 0;
   const bool norm_ratio = (a.g.mode & RQ_MODE_NORM_RATIO) != 0;
+  const bool hadamard = (a.g.mode & RQ_MODE_HADAMARD) != 0;   // d = 128: every thread is a channel
 
   __shared__ float ref_s[kTok][128];     // anchor_hat (shared) or rebuilt loop l+1 (chained)
   __shared__ float x_s[kTok][128];       // current loop, then its residual
@@ -233,8 +247,12 @@ __global__ void __launch_bounds__(kThreads) append_kernel(AppendArgs a) {
     if (act)
       for (int t = 0; t < kTok; ++t) x_s[t][tid] = fmaf(-cb_s[t], ref_s[t][tid], x_s[t][tid]);
     __syncthreads();
-    // rotation u = R e, thread = output channel, sequential FMA over k
-    if (act) {
+    // rotation u = R e, thread = output channel: a sequential FMA chain over k,
+    // or the fast Walsh-Hadamard transform
+    if (hadamard) {
+      if (few) hadamard_rows<4>(tid, x_s + t4, u_s + t4, &u_s[t4][0]);
+      else hadamard_rows<kTok>(tid, x_s, u_s, &u_s[0][0]);
+    } else if (act) {
       if (few) rotate_rows<4, D>(a.R, tid, x_s + t4, u_s + t4);
       else rotate_rows<kTok, D>(a.R, tid, x_s, u_s);
     }
@@ -260,7 +278,11 @@ __global__ void __launch_bounds__(kThreads) append_kernel(AppendArgs a) {
       float acc[kTok];
 #pragma unroll
       for (int t = 0; t < kTok; ++t) acc[t] = 0.f;
-      if (act) {
+      if (hadamard) {   // R^T = R; x_s is free (this loop's residual is no longer read)
+#pragma unroll
+        for (int t = 0; t < kTok; ++t) acc[t] = u_s[t][tid];
+        hadamard128<kTok>(acc, tid, &x_s[0][0]);
+      } else if (act) {
         for (int k = 0; k < d; ++k) {
           float r = __ldg(a.R + (size_t)k * d + tid);
 #pragma unroll

@@ -158,8 +158,9 @@ __global__ void __launch_bounds__(kPrepThreads) qprep_kernel(DecodeArgs a) {
   // kernel ahead of this one.  Warp w holds rows w, w+8, ...; lane l columns
   // 4l..4l+3, so each warp-wide load reads one contiguous row.
   const int lane = tid & 31, warp = tid >> 5;
+  const bool hadamard = (a.g.mode & RQ_MODE_HADAMARD) != 0;   // fast transform instead of R (d = 128)
   float4 rv[NRES > 0 ? RPW : 1];
-  if (NRES > 0) {
+  if (NRES > 0 && !hadamard) {
 #pragma unroll
     for (int v = 0; v < RPW; ++v) {
       const int row = warp + 8 * v;
@@ -177,7 +178,12 @@ __global__ void __launch_bounds__(kPrepThreads) qprep_kernel(DecodeArgs a) {
   if (tid < D) q_s[tid] = __bfloat162float(a.q[(size_t)bh * D + tid]) * a.qscale;
   for (int i = tid; i < NG * kPackWords; i += kPrepThreads) img_s[i] = 0u;
   __syncthreads();
-  if (NRES > 0) {   // (R q)[row] for the warp's rows: lane partials, then a reduce-scatter
+  if (NRES > 0 && hadamard) {   // R q = H q / sqrt(128); qr_s serves as the butterflies' scratch
+    float v[1] = {tid < D ? q_s[tid] : 0.f};
+    hadamard128<1>(v, tid, qr_s);
+    if (tid < D) qr_s[tid] = v[0];
+    __syncthreads();
+  } else if (NRES > 0) {   // (R q)[row] for the warp's rows: lane partials, then a reduce-scatter
     const float4 x = lane < D / 4 ? reinterpret_cast<const float4*>(q_s)[lane] : make_float4(0.f, 0.f, 0.f, 0.f);
     float pv[RPW];
 #pragma unroll
@@ -729,6 +735,7 @@ __global__ void __launch_bounds__(APPEND ? kAppendThreads : kMergeThreads, APPEN
   const int bh = APPEND ? blockIdx.x % (B * H) : blockIdx.x, b = bh / H, h = bh - b * H;
 
   // ---- before the wait: inputs the decode kernel does not write ----
+  const bool hadamard = (a.g.mode & RQ_MODE_HADAMARD) != 0;   // R^T as the fast transform (d = 128)
   bool app_ok = false;
   int app_pos = 0;
   const int app_kvi = APPEND ? blockIdx.x / (B * H) : 0;
@@ -744,7 +751,7 @@ __global__ void __launch_bounds__(APPEND ? kAppendThreads : kMergeThreads, APPEN
       return;
     }
   }
-  if (NRES > 0 && tid == 0) {   // R -> shared memory, one bulk copy (R is 16-byte aligned)
+  if (NRES > 0 && !hadamard && tid == 0) {   // R -> shared memory, one bulk copy (R is 16-byte aligned)
     mbar_init(&r_bar, 1);
     fence_mbar_init();
     mbar_arrive_expect_tx(&r_bar, (uint32_t)(D * D * sizeof(float)));
@@ -777,7 +784,7 @@ __global__ void __launch_bounds__(APPEND ? kAppendThreads : kMergeThreads, APPEN
   if (ntb == 0) {   // empty cache: attention over the current token alone
     for (int k = tid; k < D; k += NT)
       a.out[(size_t)bh * D + k] = __bfloat162float(a.v_cur[(size_t)bh * D + k]);
-    if (NRES > 0) (void)mbar_wait_bounded(&r_bar, 0);   // the R copy lands before the CTA exits
+    if (NRES > 0 && !hadamard) (void)mbar_wait_bounded(&r_bar, 0);   // the R copy lands before the CTA exits
     pdl_wait();   // completion of this kernel implies the decode kernel's
     if constexpr (APPEND)
       if (app_ok)
@@ -835,7 +842,11 @@ __global__ void __launch_bounds__(APPEND ? kAppendThreads : kMergeThreads, APPEN
   }
   __syncthreads();
   float o = 0.f;
-  if (NRES > 0) {
+  if (NRES > 0 && hadamard) {
+    float v[1] = {tid < D ? vr_s[tid] : 0.f};
+    hadamard128<1>(v, tid, rt_s);
+    o = v[0];
+  } else if (NRES > 0) {
     // R in shared memory (bounded wait; a timeout sets the status word, decided for the CTA)
     const bool ok = mbar_wait_bounded(&r_bar, 0);
     if (__syncthreads_or(!ok)) {
@@ -870,6 +881,7 @@ cudaError_t launch_t(const DecodeArgs& a, int num_sms, cudaStream_t stream) {
   auto k = decode_kernel<D, GS, NRES>;
   auto km = merge_kernel<D, (NRES > 0 ? 1 : 0), false>;
   size_t km_smem = NRES > 0 ? (size_t)D * D * sizeof(float) : 0;
+  if (a.g.mode & RQ_MODE_HADAMARD) km_smem = 0;   // no R to stage
   int km_threads = kMergeThreads, km_ctas_per_bh = 1;
   if constexpr (NRES == 0)
     if (a.kv_all) {

@@ -158,6 +158,43 @@ __device__ __forceinline__ float2 e4m3x2_to_f32x2(uint16_t v) {
   __half2 hh = *reinterpret_cast<__half2*>(&h2);
   return __half22float2(hh);
 }
+// Walsh-Hadamard rotation (RQ_MODE_HADAMARD, d = 128): u = H v / sqrt(128) for
+// NT vectors whose channels are held one per thread (thread i < 128 holds
+// channel i of each).  Butterfly stages h = 1, 2, ..., 64 turn every pair
+// (a, b) = (v[j], v[j + h]), j & h == 0, into (a + b, a - b), each rounded to
+// binary32 -- stages below 32 across lanes, 32 and 64 through xs ([NT][128]
+// floats of shared memory) -- then one binary32 product with the binary32 value
+// of 1/sqrt(128).  H is symmetric: the same call applies R^T.  It holds
+// barriers: every thread of the CTA calls it; threads >= 128 only take part
+// in those (their values are not used).
+constexpr float kInvSqrt128 = 0x1.6a09e6p-4f;
+template <int NT>
+__device__ __forceinline__ void hadamard128(float (&v)[NT], int i, float* xs) {
+#pragma unroll
+  for (int h = 1; h < 32; h <<= 1) {
+#pragma unroll
+    for (int t = 0; t < NT; ++t) {
+      const float p = __shfl_xor_sync(0xffffffffu, v[t], h);
+      v[t] = (i & h) ? __fsub_rn(p, v[t]) : __fadd_rn(v[t], p);
+    }
+  }
+#pragma unroll
+  for (int h = 32; h < 128; h <<= 1) {
+    if (i < 128) {
+#pragma unroll
+      for (int t = 0; t < NT; ++t) xs[t * 128 + i] = v[t];
+    }
+    __syncthreads();
+    float p[NT];
+#pragma unroll
+    for (int t = 0; t < NT; ++t) p[t] = i < 128 ? xs[t * 128 + (i ^ h)] : 0.f;
+    __syncthreads();
+#pragma unroll
+    for (int t = 0; t < NT; ++t) v[t] = (i & h) ? __fsub_rn(p[t], v[t]) : __fadd_rn(v[t], p[t]);
+  }
+#pragma unroll
+  for (int t = 0; t < NT; ++t) v[t] = __fmul_rn(v[t], kInvSqrt128);
+}
 // Programmatic dependent launch: let the next kernel of the stream start its
 // prologue; wait until the kernel before this one has finished and its writes
 // are visible (returns at once when launched without the dependency).

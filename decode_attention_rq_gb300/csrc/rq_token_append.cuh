@@ -115,10 +115,21 @@ __device__ __forceinline__ void quantize_residuals(const TokenAppendSmem& s, int
 }
 
 // u_t[i] = sum_k R[i][k] e_t[k] for the NJ residuals in s.e, k ascending, one
-// float32 FMA chain each (the append kernel's order); then u replaces e.
+// float32 FMA chain each (the append kernel's order), or the fast Walsh-Hadamard
+// transform (RQ_MODE_HADAMARD); then u replaces e.
 template <int D, int NJ>
-__device__ __forceinline__ void rotate_chunk(const TokenAppendSmem& s, const float4* Rrow, int i, bool act) {
+__device__ __forceinline__ void rotate_chunk(const TokenAppendSmem& s, const float4* Rrow, int i, bool act,
+                                             bool hadamard) {
   float u[NJ];
+  if (hadamard) {   // d = 128; s.e serves as the butterflies' scratch (each thread reads its own slot first)
+#pragma unroll
+    for (int t = 0; t < NJ; ++t) u[t] = s.e[t * 128 + i];
+    hadamard128<NJ>(u, i, s.e);
+    __syncthreads();
+#pragma unroll
+    for (int t = 0; t < NJ; ++t) s.e[t * 128 + i] = u[t];
+    return;
+  }
 #pragma unroll
   for (int t = 0; t < NJ; ++t) u[t] = 0.f;
 #pragma unroll 4
@@ -151,6 +162,7 @@ __device__ bool token_append_compute(const Geom& g, uint8_t* base, const float* 
   const bool act = i < D;
   const bool chained = (g.mode & RQ_MODE_CHAINED) != 0;
   const bool norm_ratio = (g.mode & RQ_MODE_NORM_RATIO) != 0;
+  const bool hadamard = (g.mode & RQ_MODE_HADAMARD) != 0;
   if (pos < 0 || pos + 1 > g.Nmax) {
     if (i == 0 && status) atomicExch(&status[1], 1);
     return false;
@@ -179,7 +191,7 @@ __device__ bool token_append_compute(const Geom& g, uint8_t* base, const float* 
   }
   __syncthreads();
 
-  const float4* Rrow = reinterpret_cast<const float4*>(R + (size_t)(act ? i : 0) * D);
+  const float4* Rrow = hadamard ? nullptr : reinterpret_cast<const float4*>(R + (size_t)(act ? i : 0) * D);
   if (!chained) {
     // coefficients of every residual loop against the anchor, one warp each
 #pragma unroll 1
@@ -200,10 +212,10 @@ __device__ bool token_append_compute(const Geom& g, uint8_t* base, const float* 
         s.e[jj * 128 + i] = fmaf(-s.cb[j0 + jj], s.ref[i], __bfloat162float(s.x[(j0 + jj) * 128 + i]));
       __syncthreads();
       switch (nj) {
-        case 1: rotate_chunk<D, 1>(s, Rrow, i, act); break;
-        case 2: rotate_chunk<D, 2>(s, Rrow, i, act); break;
-        case 3: rotate_chunk<D, 3>(s, Rrow, i, act); break;
-        default: rotate_chunk<D, 4>(s, Rrow, i, act); break;
+        case 1: rotate_chunk<D, 1>(s, Rrow, i, act, hadamard); break;
+        case 2: rotate_chunk<D, 2>(s, Rrow, i, act, hadamard); break;
+        case 3: rotate_chunk<D, 3>(s, Rrow, i, act, hadamard); break;
+        default: rotate_chunk<D, 4>(s, Rrow, i, act, hadamard); break;
       }
       quantize_residuals(s, nj, j0, gs, i, act);
       __syncthreads();
@@ -222,13 +234,17 @@ __device__ bool token_append_compute(const Geom& g, uint8_t* base, const float* 
       __syncthreads();
       s.e[i] = act ? fmaf(-s.cb[j], s.ref[i], __bfloat162float(s.x[j * 128 + i])) : 0.f;
       __syncthreads();
-      rotate_chunk<D, 1>(s, Rrow, i, act);
+      rotate_chunk<D, 1>(s, Rrow, i, act, hadamard);
       quantize_residuals(s, 1, j, gs, i, act);
       if (j > 0) {
         // rebuilt loop j = cb * ref + R^T r_hat becomes the reference of loop j-1
         __syncthreads();
         float acc = 0.f;
-        if (act) {
+        if (hadamard) {   // R^T = R; s.e is free here
+          float v[1] = {s.rhat[i]};
+          hadamard128<1>(v, i, s.e);
+          acc = v[0];
+        } else if (act) {
 #pragma unroll 8
           for (int k = 0; k < D; ++k) acc = fmaf(__ldg(R + (size_t)k * D + i), s.rhat[k], acc);
         }

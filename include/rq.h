@@ -78,10 +78,16 @@ typedef enum rq_status {
 typedef enum rq_mode {
   RQ_MODE_SHARED = 0,   /* every earlier loop coded against the anchor: 2 plane reads per loop */
   RQ_MODE_CHAINED = 1,  /* loop l coded against the rebuilt loop l+1: reads grow with distance */
-  RQ_MODE_NORM_RATIO = 2 /* flag, OR'd with one of the above: the stored coefficient is the
+  RQ_MODE_NORM_RATIO = 2, /* flag, OR'd with one of the above: the stored coefficient is the
                             norm ratio ||kv_l|| / ||ref|| (the scaling the arXiv summary lists
                             beside least squares among its appendix comparisons) instead of
                             the least-squares <kv_l, ref> / <ref, ref>; decode is unchanged */
+  RQ_MODE_HADAMARD = 4  /* flag: the rotation is R = H_d / sqrt(d), H_d the Sylvester Hadamard
+                           matrix (entry (i, k) = (-1)^popcount(i & k)), applied as a fast
+                           Walsh-Hadamard transform (d log d adds) wherever R or R^T acts;
+                           head_dim 128 only.  The explainer's related-explainers list points
+                           to a 2-bit KV cache built on a Hadamard rotation; the summary's
+                           ablation compares rotation methods.  R_dev may then be NULL. */
 } rq_mode;
 
 /* Shape of one cache.  The anchor is 4-bit and residuals 2-bit (fixed). */
@@ -104,12 +110,17 @@ typedef struct rq_cache rq_cache;   /* opaque host-side handle; holds no device 
 size_t rq_cache_bytes(const rq_config* cfg);
 
 /* Bind a cache to caller memory.
- *   cfg    host; copied.
+ *   cfg    host; copied.  cfg->mode: RQ_MODE_SHARED or RQ_MODE_CHAINED, optionally
+ *          OR'd with RQ_MODE_NORM_RATIO and RQ_MODE_HADAMARD.  In binary32 the
+ *          Hadamard transform runs butterfly stages h = 1, 2, ..., d/2, each pair
+ *          (j, j+h) becoming (a+b, a-b) rounded, then one product with the
+ *          binary32 value of 1/sqrt(d); the stored codes follow that order.
  *   dev_buf device, >= rq_cache_bytes(cfg) bytes, 16-byte aligned.  Its
  *          contents are the cache; the caller zero-fills it before first use
  *          (only needed for byte-exact comparisons: unwritten slots are never read).
  *   R_dev  device float32 [d][d] row-major, the rotation (orthogonal); caller
- *          keeps it alive and unchanged while the cache is used.
+ *          keeps it alive and unchanged while the cache is used.  Unused (may be
+ *          NULL) with RQ_MODE_HADAMARD.
  *   out    host; receives the handle.  Free it with rq_cache_destroy.
  * Errors: INVALID_ARG (null), UNSUPPORTED (shape), CAPACITY (bytes too small),
  * ALIGNMENT. */

@@ -27,6 +27,7 @@ class Case:
     chained: bool = False
     seed: int = 0
     scaling: str = "ls"      # "ls" (least squares) or "norm" (norm ratio)
+    rotation: str = "dense"  # "dense" (R as given) or "hadamard" (fast Walsh-Hadamard, no R on the device)
 
     def workload(self, anchor_is_base=True):
         alphas = synth.OURO_ALPHAS if self.P == 4 and anchor_is_base else tuple(
@@ -35,8 +36,14 @@ class Case:
                               alphas, anchor_is_base)
 
 
-def rotation32(d, seed=0):
-    """The rotation as the device receives it (float32), and the same values in float64."""
+def rotation32(d, seed=0, kind="dense"):
+    """The rotation as the device receives it (float32), and the same values in
+    float64; for the Walsh-Hadamard mode the device gets none and the oracle
+    takes H_d / sqrt(d)."""
+    if kind == "hadamard":
+        import oracle
+        R = oracle.hadamard_matrix(d)
+        return R.astype(np.float32), R
     R32 = synth.rotation(d, seed).astype(np.float32)
     return R32, R32.astype(np.float64)
 
@@ -51,11 +58,12 @@ class GpuCache:
         self.device = device
         self.cfg = rq.rq_config(case.L, case.P, case.G, case.H, case.d, case.g, case.B, case.Nmax,
                                 (rq.RQ_MODE_CHAINED if case.chained else rq.RQ_MODE_SHARED)
-                                | (rq.RQ_MODE_NORM_RATIO if case.scaling == "norm" else 0))
+                                | (rq.RQ_MODE_NORM_RATIO if case.scaling == "norm" else 0)
+                                | (rq.RQ_MODE_HADAMARD if case.rotation == "hadamard" else 0))
         self.nbytes = rq.rq_cache_bytes(self.cfg)
         assert self.nbytes > 0
         self.buf = torch.zeros(self.nbytes, dtype=torch.uint8, device=device)
-        self.R = torch.from_numpy(R32).to(device)
+        self.R = None if case.rotation == "hadamard" else torch.from_numpy(R32).to(device)
         self.handle = rq.rq_cache_create(self.cfg, self.buf, self.nbytes, self.R)
         self.ws_bytes = rq.rq_decode_workspace_bytes(self.cfg, case.B)
         self.ws = torch.zeros(self.ws_bytes, dtype=torch.uint8, device=device)

@@ -27,21 +27,24 @@ def _geom(case: Case):
     return oracle.Geometry(case.L, case.P, case.G, case.H, case.d, case.g, case.B, case.Nmax)
 
 
-# d, g, loops per group, chained, scaling, batch, heads
+# d, g, loops per group, chained, scaling, rotation, batch, heads
 CASES = [
-    (128, 32, 4, False, "ls", 3, 2),
-    (128, 16, 4, True, "ls", 2, 3),
-    (96, 32, 4, False, "norm", 2, 2),
-    (96, 16, 8, False, "ls", 2, 2),
-    (128, 32, 16, False, "ls", 1, 2),
-    (128, 32, 4, True, "norm", 2, 2),
+    (128, 32, 4, False, "ls", "dense", 3, 2),
+    (128, 16, 4, True, "ls", "dense", 2, 3),
+    (96, 32, 4, False, "norm", "dense", 2, 2),
+    (96, 16, 8, False, "ls", "dense", 2, 2),
+    (128, 32, 16, False, "ls", "dense", 1, 2),
+    (128, 32, 4, True, "norm", "dense", 2, 2),
+    (128, 32, 8, False, "ls", "hadamard", 2, 2),
+    (128, 32, 4, True, "ls", "hadamard", 2, 2),
 ]
 
 
-@pytest.mark.parametrize("d,g,P,chained,scaling,B,H", CASES)
-def test_fused_call_equals_decode_then_append_and_the_oracle(d, g, P, chained, scaling, B, H):
-    case = Case(L=2, P=P, G=1, H=H, d=d, g=g, B=B, Nmax=192, chained=chained, scaling=scaling, seed=40 + P)
-    R32, R = rotation32(d)
+@pytest.mark.parametrize("d,g,P,chained,scaling,rotation,B,H", CASES)
+def test_fused_call_equals_decode_then_append_and_the_oracle(d, g, P, chained, scaling, rotation, B, H):
+    case = Case(L=2, P=P, G=1, H=H, d=d, g=g, B=B, Nmax=192, chained=chained, scaling=scaling, seed=40 + P,
+                rotation=rotation)
+    R32, R = rotation32(d, kind=rotation)
     sep, fused = GpuCache(case, R32), GpuCache(case, R32)
     geom = _geom(case)
     obuf = np.zeros(geom.total_bytes, dtype=np.uint8)
@@ -52,7 +55,7 @@ def test_fused_call_equals_decode_then_append_and_the_oracle(d, g, P, chained, s
     kvb, kv = kv_for(case, 7, n0, base)
     for c in (sep, fused):
         c.append(1, 0, kvb, start)
-    oracle.append(obuf, geom, R, 1, 0, kv, start, chained=chained, scaling=scaling)
+    oracle.append(obuf, geom, R, 1, 0, kv, start, chained=chained, scaling=scaling, rotation=rotation)
     seq = start + n0
     scale = 1.0 / math.sqrt(d)
     worst = 0.0
@@ -63,7 +66,7 @@ def test_fused_call_equals_decode_then_append_and_the_oracle(d, g, P, chained, s
         sep.append(1, 0, kvb_c, seq)
         out_f = fused.decode_append(1, 0, qb, kvb_c[..., 0, :], seq, scale)
         ref, ok = oracle.decode_attention_append(obuf, geom, R, 1, 0, q, kv_c[..., 0, :], seq, scale,
-                                                 chained=chained, scaling=scaling)
+                                                 chained=chained, scaling=scaling, rotation=rotation)
         assert ok.all()
         o_s, o_f = out_s.cpu().numpy(), out_f.cpu().numpy()
         assert np.array_equal(o_s, o_f), f"step {step}: fused output differs from the two calls"
@@ -75,7 +78,8 @@ def test_fused_call_equals_decode_then_append_and_the_oracle(d, g, P, chained, s
         assert np.array_equal(g_f, obuf), f"step {step}: {int((g_f != obuf).sum())} bytes differ from the oracle"
         seq = seq + 1
     assert sep.status.tolist() == [0, 0, 0, 0] and fused.status.tolist() == [0, 0, 0, 0]
-    print(f"d={d} g={g} P={P} chained={chained} {scaling}: worst max-abs error {worst:.3e}; bytes equal")
+    print(f"d={d} g={g} P={P} chained={chained} {scaling} {rotation}: worst max-abs error {worst:.3e}; "
+          f"bytes equal")
 
 
 def test_fused_call_empty_rows_and_capacity():

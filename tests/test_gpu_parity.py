@@ -84,7 +84,7 @@ def check_residual_parity(gbuf, obuf, geom, comp_u, layer, group, n, B, H, chain
 
 def _build_both(case: Case, chunks, seq_start=None, anchor_is_base=True):
     """Append the same tokens (in the given chunk sizes) on both sides; return everything."""
-    R32, R = rotation32(case.d)
+    R32, R = rotation32(case.d, kind=case.rotation)
     gpu = GpuCache(case, R32)
     geom = _geom(case)
     obuf = np.zeros(geom.total_bytes, dtype=np.uint8)
@@ -98,7 +98,7 @@ def _build_both(case: Case, chunks, seq_start=None, anchor_is_base=True):
                 kv_bf16, kv = kv_for(case, seed * 1000 + layer * 100 + group * 10 + ci, n, anchor_is_base)
                 gpu.append(layer, group, kv_bf16, pos)
                 comp = oracle.append(obuf, geom, R, layer, group, kv, pos, chained=case.chained,
-                                     scaling=case.scaling)
+                                     scaling=case.scaling, rotation=case.rotation)
                 if layer == 0 and group == 0:
                     for j in range(case.P - 1):
                         us[j] = comp["u"][j] if us[j] is None else np.concatenate([us[j], comp["u"][j]], axis=-2)
@@ -388,6 +388,30 @@ def test_walsh_hadamard_rotation():
         out = gpu.decode(0, 0, loop, qb, kcb, vcb, seq, 1 / math.sqrt(d)).cpu().numpy()
         ref = oracle.decode_attention(obuf, geom, R, 0, 0, loop, q, kc, vc, seq, 1 / math.sqrt(d))
         assert np.abs(out - ref).max() <= ATOL
+
+
+@pytest.mark.parametrize("chained", [False, True])
+def test_hadamard_mode_fast_transform(chained):
+    """RQ_MODE_HADAMARD: no R on the device; the append, the query prep and the
+    merge run the fast Walsh-Hadamard transform.  Every cache byte equals the
+    oracle's (whose binary32 path follows the same butterfly order), every loop
+    decodes within 2e-3 of the oracle attention over those bytes."""
+    case = Case(L=1, P=4, G=1, H=3, d=128, g=32, B=2, Nmax=256, seed=34, chained=chained, rotation="hadamard")
+    gpu, geom, obuf, R, _ = _build_both(case, chunks=[190, 1, 9])
+    gbuf = gpu.bytes_host()
+    assert np.array_equal(gbuf, obuf), f"{int((gbuf != obuf).sum())} cache bytes differ"
+    seq = np.array([200, 131])
+    worst = 0.0
+    for loop in range(4):
+        qb, q, kcb, kc, vcb, vc = _queries(case, 80, loop)
+        out = gpu.decode(0, 0, loop, qb, kcb, vcb, seq, 1 / math.sqrt(128)).cpu().numpy()
+        ref = oracle.decode_attention(obuf, geom, R, 0, 0, loop, q, kc, vc, seq, 1 / math.sqrt(128),
+                                      chained=chained)
+        err = float(np.abs(out - ref).max())
+        worst = max(worst, err)
+        assert err <= ATOL, f"loop {loop}: max abs err {err:.3e}"
+    assert gpu.status.tolist() == [0, 0, 0, 0]
+    print(f"hadamard chained={chained}: worst max-abs error {worst:.3e}; cache bytes equal")
 
 
 def test_huginn_groups_and_layers():

@@ -61,8 +61,8 @@ def test_cache_bytes_matches_storage_accounting(rq):
 
 
 @pytest.mark.parametrize("kw", [dict(head_dim=64), dict(group_size=8), dict(head_dim=96, group_size=64),
-                                dict(loops_per_group=0), dict(loops_per_group=17), dict(mode=4),
-                                dict(num_heads=0), dict(max_seq_len=0)])
+                                dict(loops_per_group=0), dict(loops_per_group=17), dict(mode=8),
+                                dict(head_dim=96, mode=4), dict(num_heads=0), dict(max_seq_len=0)])
 def test_unsupported_shapes(rq, kw):
     cfg = _cfg(rq, **kw)
     assert rq.rq_cache_bytes(cfg) == 0
@@ -80,6 +80,10 @@ def test_create_argument_checks(rq):
     assert rq.lib.rq_cache_create(ctypes.byref(cfg), 0x1008, need, 0x2000, ctypes.byref(h)) == 2
     assert rq.lib.rq_cache_create(ctypes.byref(cfg), 0x1000, need, 0x2004, ctypes.byref(h)) == 2
     assert rq.lib.rq_cache_destroy(None) == 0
+    # the rotation may be NULL only with the Walsh-Hadamard mode (which needs d = 128)
+    assert rq.lib.rq_cache_create(ctypes.byref(cfg), 0x1000, need, None, ctypes.byref(h)) == 1
+    hcfg = _cfg(rq, num_layers=1, max_seq_len=64, max_batch=1, num_heads=1, mode=rq.RQ_MODE_HADAMARD)
+    assert rq.rq_cache_bytes(hcfg) == need
 
 
 def test_bf16_argument_checks(rq):
