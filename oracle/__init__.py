@@ -22,11 +22,11 @@ import numpy as np
 from . import formats, method, layout
 from .formats import (e4m3_encode, e4m3_decode, e4m3_round, bf16_encode, bf16_decode, bf16_round)
 from .method import quantize, dequantize, ls_coefficient, compress_group, attention, hadamard_matrix
-from .layout import Geometry, TILE, pack_group, read_plane_tokens, bits_per_element
+from .layout import Geometry, TILE, pack_group, read_plane_tokens, bits_per_element, paged_pool
 
 __all__ = ["formats", "method", "layout", "Geometry", "TILE", "quantize", "dequantize",
            "ls_coefficient", "compress_group", "attention", "hadamard_matrix", "pack_group", "read_plane_tokens",
-           "bits_per_element", "append", "reconstruct", "decode_attention", "decode_attention_append",
+           "bits_per_element", "paged_pool", "append", "reconstruct", "decode_attention", "decode_attention_append",
            "e4m3_encode", "e4m3_decode", "e4m3_round", "bf16_encode", "bf16_decode", "bf16_round"]
 
 

@@ -100,6 +100,42 @@ class Geometry:
         return 2 * self.ntiles * self.a_tile + (2 * j + kv) * self.ntiles * self.r_tile
 
 
+def paged_pool(buf: np.ndarray, geom: Geometry, table: np.ndarray, num_pages: int) -> np.ndarray:
+    """The paged layout's pool holding the same cache as the contiguous bytes buf.
+
+    Paged layout (a block table, as a paged serving engine lays out its KV cache;
+    the pages integrate the method into such an engine): each (layer, group)
+    owns num_pages pages; page p holds, for every head h in order, the tiles
+    of one 64-token block of every plane -- anchor K, anchor V, then residual
+    plane j's K and V for j = 0 .. P-2 -- each tile byte for byte as in the
+    contiguous plane.  Tile t of batch row b is in page table[b, t]; entries
+    below 0 map nothing.  Pages no (row, tile) maps to stay zero."""
+    P, H = geom.loops_per_group, geom.num_heads
+    planes = [(geom.anchor_plane(0), geom.a_tile), (geom.anchor_plane(1), geom.a_tile)]
+    for j in range(P - 1):
+        planes += [(geom.res_plane(j, 0), geom.r_tile), (geom.res_plane(j, 1), geom.r_tile)]
+    head_block = sum(tb for _, tb in planes)
+    page_bytes = H * head_block
+    L, G = geom.num_layers, geom.num_groups
+    pool = np.zeros(L * G * num_pages * page_bytes, dtype=np.uint8)
+    table = np.asarray(table)
+    for layer in range(L):
+        for group in range(G):
+            for b in range(table.shape[0]):
+                for t in range(min(table.shape[1], geom.ntiles)):
+                    page = int(table[b, t])
+                    if page < 0:
+                        continue
+                    for h in range(H):
+                        dst = ((layer * G + group) * num_pages + page) * page_bytes + h * head_block
+                        src_region = geom.region_offset(layer, group, b, h)
+                        for plane_base, tb in planes:
+                            src = src_region + plane_base + t * tb
+                            pool[dst:dst + tb] = buf[src:src + tb]
+                            dst += tb
+    return pool
+
+
 def _code_addresses(geom: Geometry, plane_base: int, tile_bytes: int, pos: np.ndarray,
                     bits: int, channel_major: bool):
     """Byte address and bit shift of every (token, channel) code.

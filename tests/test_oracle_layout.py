@@ -218,3 +218,41 @@ def test_decode_attention_append_writes_the_next_slot(chained):
                     worst[loop] = max(worst.get(loop, 0.0), rel)
     print("relative reconstruction error of the appended token per loop", worst)
     assert all(v < 0.25 for v in worst.values())
+
+
+def test_paged_pool_moves_whole_tiles():
+    """The paged view holds every mapped tile byte for byte at its page (a page =
+    one 64-token block of every plane of every head: 396 B x 64 x H at d = 128,
+    g = 32, 4 loops); unmapped pages stay zero; reading the pool back through
+    the table gives the contiguous cache again."""
+    geom, buf, R, kv, comps = _small_cache(False)          # 2 layers, 2 groups, B = 2, H = 3, 200 slots
+    ntiles = geom.ntiles
+    num_pages = 2 * ntiles + 2
+    rng = np.random.default_rng(4)
+    perm = rng.permutation(num_pages)
+    table = perm[: 2 * ntiles].reshape(2, ntiles)
+    pool = Lo.paged_pool(buf, geom, table, num_pages)
+    head_block = 396 * 64
+    page_bytes = 3 * head_block
+    assert pool.size == 2 * 2 * num_pages * page_bytes
+    # unmapped pages are zero
+    for lg in range(4):
+        for p in perm[2 * ntiles:]:
+            o = (lg * num_pages + p) * page_bytes
+            assert not pool[o:o + page_bytes].any()
+    # back through the table: every region equals the contiguous one
+    back = np.zeros_like(buf)
+    for layer in range(2):
+        for group in range(2):
+            for b in range(2):
+                for h in range(3):
+                    r0 = geom.region_offset(layer, group, b, h)
+                    for t in range(ntiles):
+                        src = ((layer * 2 + group) * num_pages + table[b, t]) * page_bytes + h * head_block
+                        off = 0
+                        for plane, tb in [(geom.anchor_plane(0), geom.a_tile), (geom.anchor_plane(1), geom.a_tile)] + \
+                                [(geom.res_plane(j, kv_), geom.r_tile) for j in range(3) for kv_ in (0, 1)]:
+                            back[r0 + plane + t * tb: r0 + plane + (t + 1) * tb] = pool[src + off: src + off + tb]
+                            off += tb
+                    assert off == head_block
+    assert np.array_equal(back, buf)
