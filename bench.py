@@ -223,12 +223,12 @@ def run_reference(args, w):
     print(json.dumps(line))
 
 
-def _config(w, chained=False, hadamard=False):
+def _config(w, chained=False, hadamard=False, paged=False):
     return {"workload": f"{w.name}: {w.num_layers} layers x {w.loops_per_group} loops x {w.num_groups} groups, "
                         f"{w.num_heads} KV heads x {w.head_dim}, batch {w.batch}, {w.context}-token context, "
                         f"INT4 anchor + INT2 residuals, group {w.group_size}, "
                         f"{'chained' if chained else 'shared'} anchor"
-                        + (", Walsh-Hadamard rotation" if hadamard else ""),
+                        + (", Walsh-Hadamard rotation" if hadamard else "") + (", paged layout" if paged else ""),
             "global_batch": w.batch, "seq_len": w.context, "parallelism": "replicas",
             "l2": "inputs larger than L2 (every step streams the whole compressed cache)"}
 
@@ -249,6 +249,8 @@ def main():
                     help="seconds of oracle work per reference step (default: about 150 s per run)")
     ap.add_argument("--quiet", action="store_true")
     ap.add_argument("--chained", action="store_true", help="chained anchors (loop l coded against loop l+1)")
+    ap.add_argument("--paged", action="store_true",
+                    help="paged cache layout: pages assigned through a shuffled block table")
     ap.add_argument("--hadamard", action="store_true",
                     help="Walsh-Hadamard rotation applied as a fast transform (head_dim 128)")
     ap.add_argument("--layers", type=int, default=None,
@@ -284,9 +286,19 @@ def run_rq(args, w):
     R32 = None if args.hadamard else torch.from_numpy(synth.rotation(d).astype(np.float32)).to(dev)
     cfg = rq.rq_config(L, P, G, H, d, g, B, N + 64, (rq.RQ_MODE_CHAINED if args.chained else rq.RQ_MODE_SHARED)
                        | (rq.RQ_MODE_HADAMARD if args.hadamard else 0))
-    nbytes = rq.rq_cache_bytes(cfg)
-    cache_buf = torch.empty(nbytes, dtype=torch.uint8, device=dev)
-    handle = rq.rq_cache_create(cfg, cache_buf, nbytes, R32)
+    if args.paged:
+        # every row's tiles on pages of a shuffled table (the pool holds exactly those pages)
+        ntiles = -(-(N + 64) // 64)
+        num_pages = B * ntiles
+        perm = torch.randperm(num_pages, generator=torch.Generator().manual_seed(5 + rank))
+        table = perm.reshape(B, ntiles).to(torch.int32).to(dev)
+        nbytes = rq.rq_cache_paged_bytes(cfg, num_pages)
+        cache_buf = torch.empty(nbytes, dtype=torch.uint8, device=dev)
+        handle = rq.rq_cache_create_paged(cfg, num_pages, cache_buf, nbytes, table, ntiles, R32)
+    else:
+        nbytes = rq.rq_cache_bytes(cfg)
+        cache_buf = torch.empty(nbytes, dtype=torch.uint8, device=dev)
+        handle = rq.rq_cache_create(cfg, cache_buf, nbytes, R32)
     ws_bytes = rq.rq_decode_workspace_bytes(cfg, B)
     ws = torch.zeros(ws_bytes, dtype=torch.uint8, device=dev)
     status = ws[:16].view(torch.int32)
@@ -312,15 +324,19 @@ def run_rq(args, w):
 
     s = torch.cuda.Stream(device=dev)
 
+    def call(i):
+        lp, layer, grp = order[i]
+        t = temp_all[layer * G + grp]
+        if lp == P - 1:   # the anchor loop: attention, then the token joins the cache
+            rq.rq_decode_attention_append(handle, layer, grp, B, q_all[i], t[..., 0, :], seq, scale, out_all[i],
+                                          ws, ws_bytes, s.cuda_stream)
+        else:
+            rq.rq_decode_attention(handle, layer, grp, lp, B, q_all[i], t[lp, 0, :, :, 0], t[lp, 1, :, :, 0],
+                                   seq, scale, out_all[i], ws, ws_bytes, s.cuda_stream)
+
     def step(stream=None):
-        for i, (lp, layer, grp) in enumerate(order):
-            t = temp_all[layer * G + grp]
-            if lp == P - 1:   # the anchor loop: attention, then the token joins the cache
-                rq.rq_decode_attention_append(handle, layer, grp, B, q_all[i], t[..., 0, :], seq, scale, out_all[i],
-                                              ws, ws_bytes, s.cuda_stream)
-            else:
-                rq.rq_decode_attention(handle, layer, grp, lp, B, q_all[i], t[lp, 0, :, :, 0], t[lp, 1, :, :, 0],
-                                       seq, scale, out_all[i], ws, ws_bytes, s.cuda_stream)
+        for i in range(ncalls):
+            call(i)
 
     launches_per_step = 3 * ncalls   # a call is qprep + decode + merge kernels (the append runs in the merge)
     torch.cuda.synchronize()
@@ -357,33 +373,41 @@ def run_rq(args, w):
     if st.any():
         raise RuntimeError(f"device status word reports an error: {st.tolist()}")
 
-    # duration of one decode call (its three kernels; decode_kernel dominates), CUDA events on its stream
+    # time per call (its three kernels; decode_kernel dominates), CUDA events on its stream.
+    # The step's own call sequence is replayed with events only where the kind of call
+    # changes (a run of residual-loop calls, a run of anchor-loop calls): inside a run the
+    # calls keep their programmatic-dependent overlap, as in the step, and a run's time
+    # divided by its calls is the time per call.
     byts = algorithmic_bytes_per_step(w, B, N, args.chained)
-    dur_res, dur_anchor, bytes_res = [], [], 0
-    ev = [torch.cuda.Event(enable_timing=True) for _ in range(2 * ncalls)]
+    kinds = [lp < P - 1 for (lp, _, _) in order]
+    bounds = [0] + [i for i in range(1, ncalls) if kinds[i] != kinds[i - 1]] + [ncalls]
+    ev = [torch.cuda.Event(enable_timing=True) for _ in bounds]
+    t_res = t_anchor = 0.0
+    n_res = n_anchor = bytes_res = 0
     with torch.cuda.stream(s):
-        for r in range(3):
-            i = 0
-            for (lp, layer, grp) in order:
-                t = temp_all[layer * G + grp]
-                ev[2 * i].record(s)
-                rq.rq_decode_attention(handle, layer, grp, lp, B, q_all[i], t[lp, 0, :, :, 0], t[lp, 1, :, :, 0],
-                                       seq, scale, out_all[i], ws, ws_bytes, s.cuda_stream)
-                ev[2 * i + 1].record(s)
-                i += 1
+        for r in range(4):
+            ev[0].record(s)
+            for k in range(len(bounds) - 1):
+                for i in range(bounds[k], bounds[k + 1]):
+                    call(i)
+                ev[k + 1].record(s)
             torch.cuda.synchronize()
-            if r > 0:
-                for k, (lp, _, _) in enumerate(order):
-                    (dur_anchor if lp == P - 1 else dur_res).append(ev[2 * k].elapsed_time(ev[2 * k + 1]))
-                    if lp < P - 1:
-                        bytes_res += byts["per_loop"][lp]
+            if r == 0:
+                continue   # warm-up pass
+            for k in range(len(bounds) - 1):
+                ms, n = ev[k].elapsed_time(ev[k + 1]), bounds[k + 1] - bounds[k]
+                if kinds[bounds[k]]:
+                    t_res, n_res = t_res + ms, n_res + n
+                    bytes_res += sum(byts["per_loop"][order[i][0]] for i in range(bounds[k], bounds[k + 1]))
+                else:
+                    t_anchor, n_anchor = t_anchor + ms, n_anchor + n
     # the dominant launch: a residual-loop call (shared: anchor + one residual plane;
     # chained: anchor + the planes down to the loop), bytes and time summed over those calls
-    per_launch_bytes = bytes_res / len(dur_res)
-    avg_launch_ms = statistics.mean(dur_res)
+    per_launch_bytes = bytes_res / n_res
+    avg_launch_ms = t_res / n_res
     peak, peak_kind = _peaks()
     achieved = per_launch_bytes / (avg_launch_ms / 1e3) / 1e9
-    anchor_ms = statistics.mean(dur_anchor)
+    anchor_ms = t_anchor / n_anchor
     anchor_gbs = byts["call_anchor"] / (anchor_ms / 1e3) / 1e9
     traffic = None
     tp = os.path.join(ROOT, "profiles", "traffic_per_launch.json")
@@ -391,7 +415,7 @@ def run_rq(args, w):
         try:
             tj = json.load(open(tp))
             if (tj.get("workload") == w.name and tj.get("batch") == B and tj.get("group_size") == g
-                    and not args.chained and not args.hadamard
+                    and not args.chained and not args.hadamard and not args.paged
                     and tj.get("kernel_source_hash") == _kernel_hash()):
                 traffic = tj.get("bytes_per_launch")
         except Exception:
@@ -402,7 +426,7 @@ def run_rq(args, w):
     line = {
         "metric": METRIC, "value": value, "unit": "tokens/s", "n_gpus": world, "steps": args.steps,
         "warmup": args.warmup, "ms_per_step": ms_step, "higher_is_better": True, "scaling": "weak",
-        "vs_baseline": None, "dtype": "int32/fp32", "data": "synthetic", "config": _config(w, args.chained, args.hadamard),
+        "vs_baseline": None, "dtype": "int32/fp32", "data": "synthetic", "config": _config(w, args.chained, args.hadamard, args.paged),
         "effective_gbps": step_gbs, "frac_of_hbm_peak": step_gbs / peak,
         "roofline": {"bound": "hbm", "achieved": achieved, "peak": peak, "unit": "GB/s",
                      "frac": achieved / peak, "traffic": traffic,
@@ -410,7 +434,7 @@ def run_rq(args, w):
                                "decode_kernel<d, g, 1> + merge_kernel)",
                      "peak_source": f"MEASURED_PEAKS.json hbm_gbs ({peak_kind})",
                      "avg_launch_ms": avg_launch_ms, "bytes_per_launch": per_launch_bytes,
-                     "anchor_loop_call": {"avg_ms": anchor_ms, "bytes": byts["call_anchor"],
+                     "anchor_loop_call": {"avg_ms": anchor_ms, "bytes": byts["call_anchor"], "includes_token_append": True,
                                           "achieved": anchor_gbs, "frac": anchor_gbs / peak}},
         "gpu_launches": launches_per_step * args.steps,
         "clocks": clk.summary(),

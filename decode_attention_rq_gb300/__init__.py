@@ -18,6 +18,7 @@ __all__ = [
     "rq_decode_workspace_bytes", "rq_decode_attention", "rq_bf16_workspace_bytes",
     "rq_decode_attention_bf16", "rq_status_string", "EXPORTED_SYMBOLS",
     "rq_decode_attention_noalloc", "RQ_NOALLOC_WORKSPACE_BYTES", "rq_decode_attention_append",
+    "rq_cache_paged_bytes", "rq_cache_create_paged",
 ]
 
 LIB_PATH = os.path.join(os.path.dirname(os.path.abspath(__file__)), "librq.so")
@@ -34,7 +35,7 @@ EXPORTED_SYMBOLS = (
     "rq_cache_bytes", "rq_cache_create", "rq_cache_destroy", "rq_append",
     "rq_decode_workspace_bytes", "rq_decode_attention", "rq_bf16_workspace_bytes",
     "rq_decode_attention_bf16", "rq_status_string", "rq_decode_attention_noalloc",
-    "rq_decode_attention_append",
+    "rq_decode_attention_append", "rq_cache_paged_bytes", "rq_cache_create_paged",
 )
 
 # size of the workspace built into the library for rq_decode_attention_noalloc (rq.h)
@@ -63,6 +64,10 @@ lib.rq_cache_bytes.argtypes = [_cfgp]
 lib.rq_cache_bytes.restype = _sz
 lib.rq_cache_create.argtypes = [_cfgp, _p, _sz, _p, ctypes.POINTER(_p)]
 lib.rq_cache_create.restype = ctypes.c_int
+lib.rq_cache_paged_bytes.argtypes = [_cfgp, _i32]
+lib.rq_cache_paged_bytes.restype = _sz
+lib.rq_cache_create_paged.argtypes = [_cfgp, _i32, _p, _sz, _p, _i32, _p, ctypes.POINTER(_p)]
+lib.rq_cache_create_paged.restype = ctypes.c_int
 lib.rq_cache_destroy.argtypes = [_p]
 lib.rq_cache_destroy.restype = ctypes.c_int
 lib.rq_append.argtypes = [_p, _i32, _i32, _i32, _p, _p, _i32, _p, _p]
@@ -119,6 +124,21 @@ def rq_cache_create(cfg: rq_config, dev_buf, nbytes: int, R_dev) -> int:
     h = _p()
     _check("rq_cache_create", lib.rq_cache_create(ctypes.byref(cfg), _ptr(dev_buf), nbytes, _ptr(R_dev),
                                                   ctypes.byref(h)))
+    return h.value
+
+
+def rq_cache_paged_bytes(cfg: rq_config, num_pages: int) -> int:
+    return lib.rq_cache_paged_bytes(ctypes.byref(cfg), num_pages)
+
+
+def rq_cache_create_paged(cfg: rq_config, num_pages: int, pool, nbytes: int, block_table, max_tiles_per_row: int,
+                          R_dev) -> int:
+    """Paged layout: tile t of row b lives in page block_table[b, t] of each
+    (layer, group)'s pool.  Returns the opaque handle (int)."""
+    h = _p()
+    _check("rq_cache_create_paged", lib.rq_cache_create_paged(
+        ctypes.byref(cfg), num_pages, _ptr(pool), nbytes, _ptr(block_table), max_tiles_per_row, _ptr(R_dev),
+        ctypes.byref(h)))
     return h.value
 
 

@@ -35,6 +35,12 @@ bool make_geom(const rq_config& c, Geom* g) {
   g->plane_a = (int64_t)g->ntiles * g->a_tile;
   g->plane_r = (int64_t)g->ntiles * g->r_tile;
   g->region = 2 * g->plane_a + 2 * (int64_t)(g->P - 1) * g->plane_r;
+  g->paged = 0;
+  g->num_pages = 0;
+  g->max_tiles = g->ntiles;
+  g->table = nullptr;
+  g->head_block = 2 * g->a_tile + 2 * (int64_t)(g->P - 1) * g->r_tile;
+  g->page_bytes = (int64_t)g->H * g->head_block;
   return true;
 }
 
@@ -73,6 +79,44 @@ rq_status rq_cache_create(const rq_config* cfg, void* dev_buf, size_t bytes, con
   c->cfg = *cfg;
   c->geom = g;
   c->base = static_cast<uint8_t*>(dev_buf);
+  c->R = R_dev;
+  c->device = 0;
+  cudaGetDevice(&c->device);
+  c->num_sms = current_sms();
+  if (c->num_sms <= 0) {
+    delete c;
+    return RQ_ERR_CUDA;
+  }
+  *out = c;
+  return RQ_OK;
+}
+
+size_t rq_cache_paged_bytes(const rq_config* cfg, int32_t num_pages) {
+  Geom g;
+  if (!cfg || !make_geom(*cfg, &g) || num_pages <= 0) return 0;
+  return (size_t)g.L * g.G * (size_t)num_pages * (size_t)g.page_bytes;
+}
+
+rq_status rq_cache_create_paged(const rq_config* cfg, int32_t num_pages, void* dev_pool, size_t bytes,
+                                const int32_t* block_table, int32_t max_tiles_per_row, const float* R_dev,
+                                rq_cache** out) {
+  if (!cfg || !dev_pool || !block_table || !out) return RQ_ERR_INVALID_ARG;
+  const bool hadamard = (cfg->mode & RQ_MODE_HADAMARD) != 0;
+  if (!R_dev && !hadamard) return RQ_ERR_INVALID_ARG;
+  Geom g;
+  if (!make_geom(*cfg, &g)) return RQ_ERR_UNSUPPORTED;
+  if (num_pages <= 0 || max_tiles_per_row < g.ntiles) return RQ_ERR_INVALID_ARG;
+  if (bytes < rq_cache_paged_bytes(cfg, num_pages)) return RQ_ERR_CAPACITY;
+  if (!aligned16(dev_pool) || !aligned16(block_table) || (R_dev && !aligned16(R_dev))) return RQ_ERR_ALIGNMENT;
+  g.paged = 1;
+  g.num_pages = num_pages;
+  g.max_tiles = max_tiles_per_row;
+  g.table = block_table;
+  rq_cache* c = new (std::nothrow) rq_cache;
+  if (!c) return RQ_ERR_INVALID_ARG;
+  c->cfg = *cfg;
+  c->geom = g;
+  c->base = static_cast<uint8_t*>(dev_pool);
   c->R = R_dev;
   c->device = 0;
   cudaGetDevice(&c->device);

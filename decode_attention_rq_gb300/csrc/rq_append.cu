@@ -48,9 +48,11 @@ __device__ __forceinline__ float load_x(const AppendArgs& a, int p, int kvi, int
   return __bfloat162float(a.kv[idx * a.g.d + k]);
 }
 
-// Write the codes / metadata (and c) of the CTA's tokens into one plane.
-__device__ void write_plane(const AppendArgs& a, uint8_t* plane, int64_t tile_bytes,
-                            int64_t codes_bytes, int bits, bool channel_major, int p0,
+// Write the codes / metadata (and c) of the CTA's tokens into one plane; `tile`
+// is that plane's tile holding positions p0 .. p0 + kTok - 1 (one tile: p0 is a
+// multiple of kTok, which divides kTile).
+__device__ void write_plane(const AppendArgs& a, uint8_t* tile, int64_t codes_bytes, int bits, bool channel_major,
+                            int p0,
                             const bool* valid, const uint8_t (*codes)[128],
                             const uint16_t (*meta)[8], const uint16_t* cbits) {
   const int d = a.g.d, ng = a.g.ng, tid = threadIdx.x;
@@ -61,7 +63,7 @@ __device__ void write_plane(const AppendArgs& a, uint8_t* plane, int64_t tile_by
     for (int t = 0; t < kTok; ++t) {
       if (!valid[t] || tid >= row_bytes) continue;
       int pos = p0 + t;
-      uint8_t* row = plane + (int64_t)(pos / kTile) * tile_bytes + (pos % kTile) * row_bytes;
+      uint8_t* row = tile + (pos % kTile) * row_bytes;
       uint32_t byte = 0;
       for (int m = 0; m < per_byte; ++m) byte |= (uint32_t)codes[t][tid * per_byte + m] << (bits * m);
       row[tid] = (uint8_t)byte;
@@ -78,8 +80,7 @@ __device__ void write_plane(const AppendArgs& a, uint8_t* plane, int64_t tile_by
         for (int q = 0; q < tpw; ++q) any |= valid[t0 + q];
         if (!any) continue;
         const int pos0 = p0 + t0;   // word-aligned: p0 is a multiple of kTok
-        uint32_t* wp = reinterpret_cast<uint32_t*>(plane + (int64_t)(pos0 / kTile) * tile_bytes +
-                                                   tid * row_bytes + (pos0 % kTile) / per_byte);
+        uint32_t* wp = reinterpret_cast<uint32_t*>(tile + tid * row_bytes + (pos0 % kTile) / per_byte);
         uint32_t word = *wp;
         for (int q = 0; q < tpw; ++q) {
           if (!valid[t0 + q]) continue;
@@ -95,14 +96,12 @@ __device__ void write_plane(const AppendArgs& a, uint8_t* plane, int64_t tile_by
     int t = i / ng, gi = i % ng;
     if (!valid[t]) continue;
     int pos = p0 + t;
-    uint8_t* tile = plane + (int64_t)(pos / kTile) * tile_bytes;
     *reinterpret_cast<uint16_t*>(tile + codes_bytes + (pos % kTile) * ng * 2 + gi * 2) = meta[t][gi];
   }
   if (cbits) {
     for (int t = tid; t < kTok; t += kThreads) {
       if (!valid[t]) continue;
       int pos = p0 + t;
-      uint8_t* tile = plane + (int64_t)(pos / kTile) * tile_bytes;
       *reinterpret_cast<uint16_t*>(tile + codes_bytes + a.g.meta + (pos % kTile) * 2) = cbits[t];
     }
   }
@@ -192,7 +191,15 @@ __global__ void __launch_bounds__(kThreads) append_kernel(AppendArgs a) {
   }
   __syncthreads();
 
-  uint8_t* region = a.base + a.g.region_offset(a.layer, a.group, b, h);
+  // the tile of the CTA's block (paged layout: its page; a bad table entry skips the block)
+  int page = 0;
+  if (a.g.paged) {
+    page = checked_page(a.g, raw_page(a.g, b, p0 / kTile), a.status);
+    if (page < 0) return;   // every thread of the CTA reads the same entry
+  }
+  auto tile_ptr = [&](bool anchor, int j, int kv) {
+    return a.base + a.g.tile_offset(a.layer, a.group, b, h, anchor, j, kv, p0 / kTile, page);
+  };
   // all valid slots inside one aligned quad (a short append): rotate 4 slots, not 16
   int t_lo = kTok, t_hi = 0;
   for (int t = 0; t < kTok; ++t)
@@ -219,7 +226,7 @@ __global__ void __launch_bounds__(kThreads) append_kernel(AppendArgs a) {
   }
   __syncthreads();
   if (!split || jz == 0)
-    write_plane(a, region + a.g.anchor_plane(kvi), a.g.a_tile, a.g.a_codes, 4, kvi == 1, p0, valid_s,
+    write_plane(a, tile_ptr(true, 0, kvi), a.g.a_codes, 4, kvi == 1, p0, valid_s,
                 codes_s, meta_s, nullptr);
   __syncthreads();
 
@@ -271,7 +278,7 @@ __global__ void __launch_bounds__(kThreads) append_kernel(AppendArgs a) {
       }
     }
     __syncthreads();
-    write_plane(a, region + a.g.res_plane(j, kvi), a.g.r_tile, a.g.r_codes, 2, kvi == 1, p0,
+    write_plane(a, tile_ptr(false, j, kvi), a.g.r_codes, 2, kvi == 1, p0,
                 valid_s, codes_s, meta_s, c_s);
     if (chained && j > 0) {
       // rebuilt loop j = cb * ref + R^T r_hat becomes the reference of loop j-1

@@ -254,7 +254,8 @@ __global__ void __launch_bounds__(kPrepThreads) qprep_kernel(DecodeArgs a) {
   for (int i = tid; i < NG * kPackWords / 4; i += kPrepThreads) dst[i] = src[i];
 }
 
-template <int D, int GS, int NRES>
+// PAGED: the cache uses the block-table layout (tile addresses through the table).
+template <int D, int GS, int NRES, bool PAGED>
 __global__ void __launch_bounds__(kThreads, (Cfg<D, GS, NRES>::MINB)) decode_kernel(DecodeArgs a) {
   using C = Cfg<D, GS, NRES>;
   constexpr int NG = C::NG, NGP = C::NGP, AW = C::AW, RW = C::RW, STAGES = C::STAGES;
@@ -327,29 +328,47 @@ __global__ void __launch_bounds__(kThreads, (Cfg<D, GS, NRES>::MINB)) decode_ker
   };
   Cursor pc = locate(u0);   // producer cursor (thread 0 only)
   const uint64_t pol = l2_evict_first_policy();   // the cache is read once per call
+  // layout tiles of the producer's unit that hold tokens (the last unit of a row may have one)
+  auto unit_tiles = [&]() { return min(C::UT, (sl_s[pc.b] - pc.t * C::UT * kTile + kTile - 1) / kTile); };
+  // paged layout: block-table entries of the next unit's tiles, loaded one unit
+  // ahead by the producer thread so that the copies never wait on them
+  int next_raw[PAGED ? C::UT : 1];
+  int pu = u0;   // unit the producer issues next
+  auto fetch_pages = [&]() {
+    const int nt = unit_tiles();
+#pragma unroll
+    for (int k = 0; k < (PAGED ? C::UT : 1); ++k) next_raw[k] = k < nt ? raw_page(a.g, pc.b, pc.t * C::UT + k) : 0;
+  };
   auto issue = [&](int stage) {
-    const uint8_t* region = a.base + a.g.region_offset(a.layer, a.group, pc.b, pc.h);
     const int t0 = pc.t * C::UT;
-    // layout tiles of this unit that hold tokens (the last unit of a row may have one)
-    const int ntile = min(C::UT, (sl_s[pc.b] - t0 * kTile + kTile - 1) / kTile);
+    const int ntile = unit_tiles();
+    const uint8_t* region = PAGED ? a.base : a.base + a.g.region_offset(a.layer, a.group, pc.b, pc.h);
     uint8_t* dst = smem + stage * C::STAGE;
     mbar_arrive_expect_tx(&full_bar[stage], (uint32_t)(ntile * C::SUB));
     for (int k = 0; k < ntile; ++k) {
       uint8_t* d = dst + k * C::SUB;
-      const int64_t tile = t0 + k;
-      bulk_g2s_hint(d, region + a.g.anchor_plane(0) + tile * C::A_TILE, C::A_TILE, &full_bar[stage], pol);
-      bulk_g2s_hint(d + C::A_TILE, region + a.g.anchor_plane(1) + tile * C::A_TILE, C::A_TILE, &full_bar[stage],
-                    pol);
+      const int tile = t0 + k;
+      int page = 0;
+      if constexpr (PAGED) page = max(checked_page(a.g, next_raw[k], a.status), 0);   // a bad entry reads page 0
+      auto src = [&](bool anchor, int j, int kv) {
+        if constexpr (PAGED)
+          return region + a.g.tile_offset(a.layer, a.group, pc.b, pc.h, anchor, j, kv, tile, page);
+        else
+          return region + (anchor ? a.g.anchor_plane(kv) : a.g.res_plane(j, kv)) +
+                 (int64_t)tile * (anchor ? C::A_TILE : C::R_TILE);
+      };
+      bulk_g2s_hint(d, src(true, 0, 0), C::A_TILE, &full_bar[stage], pol);
+      bulk_g2s_hint(d + C::A_TILE, src(true, 0, 1), C::A_TILE, &full_bar[stage], pol);
 #pragma unroll
       for (int r = 0; r < NRES; ++r) {
         uint8_t* d0 = d + 2 * C::A_TILE + 2 * r * C::R_TILE;
-        bulk_g2s_hint(d0, region + a.g.res_plane(a.res0 + r, 0) + tile * C::R_TILE, C::R_TILE, &full_bar[stage],
-                      pol);
-        bulk_g2s_hint(d0 + C::R_TILE, region + a.g.res_plane(a.res0 + r, 1) + tile * C::R_TILE, C::R_TILE,
-                      &full_bar[stage], pol);
+        bulk_g2s_hint(d0, src(false, a.res0 + r, 0), C::R_TILE, &full_bar[stage], pol);
+        bulk_g2s_hint(d0 + C::R_TILE, src(false, a.res0 + r, 1), C::R_TILE, &full_bar[stage], pol);
       }
     }
     advance(pc);
+    if constexpr (PAGED)
+      if (++pu < u1) fetch_pages();
   };
 
   if (tid == 0) {
@@ -358,8 +377,10 @@ __global__ void __launch_bounds__(kThreads, (Cfg<D, GS, NRES>::MINB)) decode_ker
   }
   for (int i = tid; i < 2 * NITEM; i += kThreads) (&tmax_s[0][0])[i] = 0u;
   __syncthreads();
-  if (tid == 0)
+  if (tid == 0) {
+    if constexpr (PAGED) fetch_pages();
     for (int s = 0; s < STAGES && u0 + s < u1; ++s) issue(s);
+  }
   Cursor cc = locate(u0);   // consumer cursor
   pdl_wait();               // the query packs of qprep_kernel are complete
 
@@ -737,17 +758,18 @@ __global__ void __launch_bounds__(APPEND ? kAppendThreads : kMergeThreads, APPEN
   // ---- before the wait: inputs the decode kernel does not write ----
   const bool hadamard = (a.g.mode & RQ_MODE_HADAMARD) != 0;   // R^T as the fast transform (d = 128)
   bool app_ok = false;
-  int app_pos = 0;
+  int app_pos = 0, app_page = 0;
   const int app_kvi = APPEND ? blockIdx.x / (B * H) : 0;
   uint8_t* app_smem = reinterpret_cast<uint8_t*>(R_s);
   if constexpr (APPEND) {
     app_pos = a.seq_lens[b];
     app_ok = token_append_compute<D>(a.g, const_cast<uint8_t*>(a.base), a.R, a.kv_all, B, a.layer, a.group, b, h,
-                                     app_kvi, app_pos, a.status, app_smem);
+                                     app_kvi, app_pos, a.status, app_smem, &app_page);
     if (app_kvi == 1) {   // the V half: store after the wait; the first CTA merges
       pdl_wait();
       if (app_ok)
-        token_append_store<D>(a.g, const_cast<uint8_t*>(a.base), a.layer, a.group, b, h, 1, app_pos, app_smem);
+        token_append_store<D>(a.g, const_cast<uint8_t*>(a.base), a.layer, a.group, b, h, 1, app_pos, app_page,
+                              app_smem);
       return;
     }
   }
@@ -788,7 +810,8 @@ __global__ void __launch_bounds__(APPEND ? kAppendThreads : kMergeThreads, APPEN
     pdl_wait();   // completion of this kernel implies the decode kernel's
     if constexpr (APPEND)
       if (app_ok)
-        token_append_store<D>(a.g, const_cast<uint8_t*>(a.base), a.layer, a.group, b, h, 0, app_pos, app_smem);
+        token_append_store<D>(a.g, const_cast<uint8_t*>(a.base), a.layer, a.group, b, h, 0, app_pos, app_page,
+                              app_smem);
     return;
   }
   const Split split{U / Cn, U % Cn};
@@ -799,7 +822,8 @@ __global__ void __launch_bounds__(APPEND ? kAppendThreads : kMergeThreads, APPEN
   pdl_wait();   // every partial of the decode kernel is written and visible
   if constexpr (APPEND)   // no kernel before this one is running: the new slot can be written
     if (app_ok)
-      token_append_store<D>(a.g, const_cast<uint8_t*>(a.base), a.layer, a.group, b, h, 0, app_pos, app_smem);
+      token_append_store<D>(a.g, const_cast<uint8_t*>(a.base), a.layer, a.group, b, h, 0, app_pos, app_page,
+                            app_smem);
 
   // this thread's element of the first contributors' accumulators, loaded while
   // warp 0 reads the (m, l) pairs
@@ -875,10 +899,10 @@ __global__ void __launch_bounds__(APPEND ? kAppendThreads : kMergeThreads, APPEN
   if (tid < D) a.out[(size_t)bh * D + tid] = (va_s[tid] + o) / L;
 }
 
-template <int D, int GS, int NRES>
+template <int D, int GS, int NRES, bool PAGED>
 cudaError_t launch_t(const DecodeArgs& a, int num_sms, cudaStream_t stream) {
   using C = Cfg<D, GS, NRES>;
-  auto k = decode_kernel<D, GS, NRES>;
+  auto k = decode_kernel<D, GS, NRES, PAGED>;
   auto km = merge_kernel<D, (NRES > 0 ? 1 : 0), false>;
   size_t km_smem = NRES > 0 ? (size_t)D * D * sizeof(float) : 0;
   if (a.g.mode & RQ_MODE_HADAMARD) km_smem = 0;   // no R to stage
@@ -929,15 +953,20 @@ cudaError_t launch_t(const DecodeArgs& a, int num_sms, cudaStream_t stream) {
   return launch_dependent(km, dim3(km_ctas_per_bh * bhs), dim3(km_threads), km_smem, stream, a, grid);
 }
 
-template <int D, int GS>
-cudaError_t launch_d(const DecodeArgs& a, int num_sms, int nres, cudaStream_t stream) {
+template <int D, int GS, bool PAGED>
+cudaError_t launch_p(const DecodeArgs& a, int num_sms, int nres, cudaStream_t stream) {
   switch (nres) {
-    case 0: return launch_t<D, GS, 0>(a, num_sms, stream);
-    case 1: return launch_t<D, GS, 1>(a, num_sms, stream);
-    case 2: return launch_t<D, GS, 2>(a, num_sms, stream);
-    case 3: return launch_t<D, GS, 3>(a, num_sms, stream);
+    case 0: return launch_t<D, GS, 0, PAGED>(a, num_sms, stream);
+    case 1: return launch_t<D, GS, 1, PAGED>(a, num_sms, stream);
+    case 2: return launch_t<D, GS, 2, PAGED>(a, num_sms, stream);
+    case 3: return launch_t<D, GS, 3, PAGED>(a, num_sms, stream);
   }
   return cudaErrorNotSupported;
+}
+
+template <int D, int GS>
+cudaError_t launch_d(const DecodeArgs& a, int num_sms, int nres, cudaStream_t stream) {
+  return a.g.paged ? launch_p<D, GS, true>(a, num_sms, nres, stream) : launch_p<D, GS, false>(a, num_sms, nres, stream);
 }
 
 int pstride_for(int d) { return ((2 + 2 * d) + 3) / 4 * 4; }

@@ -23,6 +23,11 @@ struct Geom {
   int L, P, G, H, d, g, ng, Bmax, Nmax, ntiles, mode;
   int64_t a_codes, r_codes, meta, a_tile, r_tile;   // per tile, bytes
   int64_t plane_a, plane_r, region;                 // bytes
+  // paged layout (rq_cache_create_paged): tile t of row b is page table[b * max_tiles + t]
+  // of the (layer, group)'s pool; a page holds that tile of every plane of every head
+  int paged, num_pages, max_tiles;
+  const int32_t* table;                             // device
+  int64_t head_block, page_bytes;                   // one head's tiles of all planes; H of them
 
   __host__ __device__ int64_t region_offset(int layer, int group, int b, int h) const {
     return ((((int64_t)layer * G + group) * Bmax + b) * H + h) * region;
@@ -30,6 +35,16 @@ struct Geom {
   __host__ __device__ int64_t anchor_plane(int kv) const { return (int64_t)kv * plane_a; }
   __host__ __device__ int64_t res_plane(int j, int kv) const {
     return 2 * plane_a + (int64_t)(2 * j + kv) * plane_r;
+  }
+  // Byte offset of tile t of one plane (anchor, or residual plane j; kv 0 = K, 1 = V)
+  // of (layer, group, row b, head h); `page` is that tile's page in the paged layout.
+  __host__ __device__ int64_t tile_offset(int layer, int group, int b, int h, bool anchor, int j, int kv, int t,
+                                          int page) const {
+    if (paged)
+      return (((int64_t)layer * G + group) * num_pages + page) * page_bytes + (int64_t)h * head_block +
+             (anchor ? (int64_t)kv * a_tile : 2 * a_tile + (int64_t)(2 * j + kv) * r_tile);
+    return region_offset(layer, group, b, h) + (anchor ? anchor_plane(kv) : res_plane(j, kv)) +
+           (int64_t)t * (anchor ? a_tile : r_tile);
   }
 };
 
@@ -194,6 +209,17 @@ __device__ __forceinline__ void hadamard128(float (&v)[NT], int i, float* xs) {
   }
 #pragma unroll
   for (int t = 0; t < NT; ++t) v[t] = __fmul_rn(v[t], kInvSqrt128);
+}
+// Page of tile t of row b (paged layout) from a raw block-table entry.  An entry
+// outside [0, num_pages) sets status[2] and gives -1 (the caller skips the tile
+// or reads page 0 instead: nothing outside the pool is touched).
+__device__ __forceinline__ int checked_page(const Geom& g, int raw, int32_t* status) {
+  if (raw >= 0 && raw < g.num_pages) return raw;
+  if (status) atomicExch(&status[2], 1);
+  return -1;
+}
+__device__ __forceinline__ int raw_page(const Geom& g, int b, int t) {
+  return __ldg(g.table + (size_t)b * g.max_tiles + t);
 }
 // Programmatic dependent launch: let the next kernel of the stream start its
 // prologue; wait until the kernel before this one has finished and its writes

@@ -79,14 +79,16 @@ struct SlotRef {
   int64_t codes_bytes;
 };
 
-__device__ __forceinline__ SlotRef slot_in_plane(const Geom& g, uint8_t* region, int p, int kvi, int pos) {
+// The slot of plane p (P-1: the anchor) of (layer, group, b, h); `page` is the
+// slot's tile's page in the paged layout.
+__device__ __forceinline__ SlotRef slot_in_plane(const Geom& g, uint8_t* base, int layer, int group, int b, int h,
+                                                 int page, int p, int kvi, int pos) {
   const bool anchor = p == g.P - 1;
   SlotRef r;
   r.bits = anchor ? kAnchorBits : kResBits;
   r.per_byte = 8 / r.bits;
   r.codes_bytes = anchor ? g.a_codes : g.r_codes;
-  uint8_t* plane = region + (anchor ? g.anchor_plane(kvi) : g.res_plane(p, kvi));
-  r.tile = plane + (int64_t)(pos / kTile) * (anchor ? g.a_tile : g.r_tile);
+  r.tile = base + g.tile_offset(layer, group, b, h, anchor, p, kvi, pos / kTile, page);
   r.row = pos % kTile;
   return r;
 }
@@ -151,11 +153,12 @@ __device__ __forceinline__ void rotate_chunk(const TokenAppendSmem& s, const flo
 
 // Before the wait: the append of vector type kvi (0 = K, 1 = V).  Returns
 // whether the slot fits (same on every thread); a row whose slot would
-// overflow the capacity is skipped and status[1] set.
+// overflow the capacity is skipped and status[1] set, one whose page entry is
+// out of range is skipped and status[2] set.  *page: the slot's page (paged layout).
 template <int D>
 __device__ bool token_append_compute(const Geom& g, uint8_t* base, const float* R, const __nv_bfloat16* kv,
                                      int batch, int layer, int group, int b, int h, int kvi, int pos,
-                                     int32_t* status, uint8_t* smem) {
+                                     int32_t* status, uint8_t* smem, int* page) {
   const int P = g.P, gs = g.g;
   const TokenAppendSmem s(smem, P);
   const int i = threadIdx.x, lane = i & 31, warp = i >> 5;
@@ -167,7 +170,11 @@ __device__ bool token_append_compute(const Geom& g, uint8_t* base, const float* 
     if (i == 0 && status) atomicExch(&status[1], 1);
     return false;
   }
-  uint8_t* region = base + g.region_offset(layer, group, b, h);
+  *page = 0;
+  if (g.paged) {
+    *page = checked_page(g, raw_page(g, b, pos / kTile), status);
+    if (*page < 0) return false;
+  }
 #pragma unroll 4
   for (int l = 0; l < P; ++l)   // block (l, kvi) of the temporary buffer
     s.x[l * 128 + i] = act ? kv[((((size_t)l * 2 + kvi) * batch + b) * g.H + h) * D + i] : __float2bfloat16(0.f);
@@ -175,7 +182,7 @@ __device__ bool token_append_compute(const Geom& g, uint8_t* base, const float* 
 #pragma unroll 4
     for (int l = 0; l < P; ++l) {
       int sh;
-      s.vword[l * 128 + i] = *vword_ptr(slot_in_plane(g, region, l, 1, pos), i, &sh);
+      s.vword[l * 128 + i] = *vword_ptr(slot_in_plane(g, base, layer, group, b, h, *page, l, 1, pos), i, &sh);
     }
   }
   __syncthreads();
@@ -261,15 +268,14 @@ __device__ bool token_append_compute(const Geom& g, uint8_t* base, const float* 
 // only when token_append_compute returned true).
 template <int D>
 __device__ void token_append_store(const Geom& g, uint8_t* base, int layer, int group, int b, int h, int kvi,
-                                   int pos, uint8_t* smem) {
+                                   int pos, int page, uint8_t* smem) {
   const int P = g.P, gs = g.g;
   const TokenAppendSmem s(smem, P);
   const int i = threadIdx.x;
   const bool act = i < D;
-  uint8_t* region = base + g.region_offset(layer, group, b, h);
 #pragma unroll 1
   for (int p = 0; p < P; ++p) {
-    const SlotRef r = slot_in_plane(g, region, p, kvi, pos);
+    const SlotRef r = slot_in_plane(g, base, layer, group, b, h, page, p, kvi, pos);
     if (kvi == 0) {
       // K rows are token-major: byte m of the slot's row holds channels m*per_byte ..
       const int row_bytes = D / r.per_byte;

@@ -127,6 +127,36 @@ size_t rq_cache_bytes(const rq_config* cfg);
 rq_status rq_cache_create(const rq_config* cfg, void* dev_buf, size_t bytes,
                           const float* R_dev, rq_cache** out);
 
+/* Paged layout (block table, as a paged serving engine lays out its KV cache).
+ * Instead of a contiguous capacity per (layer, group, row, head), each
+ * (layer, group) owns a pool of num_pages pages; a page holds one 64-token tile
+ * of every plane (anchor K/V, every residual K/V, with their metadata and
+ * coefficients, laid out as in the contiguous tile) of every head:
+ *   pool(layer, group) = base + (layer * G + group) * num_pages * page_bytes
+ *   page p, head h:      pool + p * page_bytes + h * head_block
+ *   head_block = 2 * anchor_tile + 2 * (P - 1) * residual_tile, page_bytes = H * head_block
+ *   inside a head block: anchor K tile, anchor V tile, then residual plane j's
+ *   K and V tiles for j = 0 .. P-2.
+ * Tile t (token positions 64t .. 64t+63) of batch row b lives in page
+ * block_table[b * max_tiles_per_row + t]; the same table serves every layer and
+ * group.  The caller assigns pages (distinct for distinct (row, tile) pairs in
+ * use) before a call touches the tile, and keeps the table unchanged while
+ * calls that read it run.  An entry outside [0, num_pages) for a tile a call
+ * touches is not followed: the call sets status word [2], reads page 0 for the
+ * attention, and skips the append's write.  Everything else (appends, decode,
+ * the fused call, all modes) is the same as for the contiguous layout. */
+size_t rq_cache_paged_bytes(const rq_config* cfg, int32_t num_pages);   /* 0 if invalid */
+
+/*   dev_pool     device, >= rq_cache_paged_bytes(cfg, num_pages), 16-byte aligned
+ *   block_table  device int32 [max_batch][max_tiles_per_row], 16-byte aligned,
+ *                max_tiles_per_row >= ceil(max_seq_len / 64); caller-owned
+ *   R_dev, out   as rq_cache_create
+ * Errors: INVALID_ARG (null, num_pages <= 0, table too narrow), UNSUPPORTED,
+ * CAPACITY, ALIGNMENT, CUDA. */
+rq_status rq_cache_create_paged(const rq_config* cfg, int32_t num_pages, void* dev_pool, size_t bytes,
+                                const int32_t* block_table, int32_t max_tiles_per_row, const float* R_dev,
+                                rq_cache** out);
+
 /* Free the host handle (not the caller's device memory).  NULL is accepted. */
 rq_status rq_cache_destroy(rq_cache* cache);
 
@@ -152,7 +182,8 @@ rq_status rq_append(rq_cache* cache, int32_t layer, int32_t group, int32_t batch
  * on the current device.  The workspace must be zero-filled once before its
  * first use (the status word must start at zero).  Its first 16 bytes
  * are the status word (int32[4]): [0] != 0 after a device-side wait timed out,
- * [1] != 0 after an append skipped a row that would overflow. */
+ * [1] != 0 after an append skipped a row that would overflow, [2] != 0 after a
+ * call met a block-table entry outside the page pool (paged layout). */
 size_t rq_decode_workspace_bytes(const rq_config* cfg, int32_t batch);
 
 /* One decode-attention call: query loop `loop` (0-based; loop == P-1 is the
