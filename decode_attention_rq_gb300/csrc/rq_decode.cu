@@ -331,13 +331,14 @@ __global__ void __launch_bounds__(kThreads, (Cfg<D, GS, NRES>::MINB)) decode_ker
   // layout tiles of the producer's unit that hold tokens (the last unit of a row may have one)
   auto unit_tiles = [&]() { return min(C::UT, (sl_s[pc.b] - pc.t * C::UT * kTile + kTile - 1) / kTile); };
   // paged layout: block-table entries of the next unit's tiles, loaded one unit
-  // ahead by the producer thread so that the copies never wait on them
-  int next_raw[PAGED ? C::UT : 1];
-  int pu = u0;   // unit the producer issues next
+  // ahead by the producer thread so that the copies never wait on them (kept in
+  // shared memory: the producer's state costs the other threads no registers)
+  __shared__ int next_raw_s[C::UT];
+  __shared__ int pu_s;   // unit the producer issues next
   auto fetch_pages = [&]() {
     const int nt = unit_tiles();
 #pragma unroll
-    for (int k = 0; k < (PAGED ? C::UT : 1); ++k) next_raw[k] = k < nt ? raw_page(a.g, pc.b, pc.t * C::UT + k) : 0;
+    for (int k = 0; k < C::UT; ++k) next_raw_s[k] = k < nt ? raw_page(a.g, pc.b, pc.t * C::UT + k) : 0;
   };
   auto issue = [&](int stage) {
     const int t0 = pc.t * C::UT;
@@ -348,11 +349,15 @@ __global__ void __launch_bounds__(kThreads, (Cfg<D, GS, NRES>::MINB)) decode_ker
     for (int k = 0; k < ntile; ++k) {
       uint8_t* d = dst + k * C::SUB;
       const int tile = t0 + k;
-      int page = 0;
-      if constexpr (PAGED) page = max(checked_page(a.g, next_raw[k], a.status), 0);   // a bad entry reads page 0
+      const uint8_t* blk = region;   // paged: this head's block of the tile's page
+      if constexpr (PAGED) {
+        const int page = max(checked_page(a.g, next_raw_s[k], a.status), 0);   // a bad entry reads page 0
+        blk = a.base + (((int64_t)a.layer * a.g.G + a.group) * a.g.num_pages + page) * a.g.page_bytes +
+              (int64_t)pc.h * a.g.head_block;
+      }
       auto src = [&](bool anchor, int j, int kv) {
-        if constexpr (PAGED)
-          return region + a.g.tile_offset(a.layer, a.group, pc.b, pc.h, anchor, j, kv, tile, page);
+        if constexpr (PAGED)   // same offsets as Geom::tile_offset, with the tile sizes as constants
+          return blk + (anchor ? kv * C::A_TILE : 2 * C::A_TILE + (2 * j + kv) * C::R_TILE);
         else
           return region + (anchor ? a.g.anchor_plane(kv) : a.g.res_plane(j, kv)) +
                  (int64_t)tile * (anchor ? C::A_TILE : C::R_TILE);
@@ -368,7 +373,7 @@ __global__ void __launch_bounds__(kThreads, (Cfg<D, GS, NRES>::MINB)) decode_ker
     }
     advance(pc);
     if constexpr (PAGED)
-      if (++pu < u1) fetch_pages();
+      if (++pu_s < u1) fetch_pages();
   };
 
   if (tid == 0) {
@@ -378,7 +383,10 @@ __global__ void __launch_bounds__(kThreads, (Cfg<D, GS, NRES>::MINB)) decode_ker
   for (int i = tid; i < 2 * NITEM; i += kThreads) (&tmax_s[0][0])[i] = 0u;
   __syncthreads();
   if (tid == 0) {
-    if constexpr (PAGED) fetch_pages();
+    if constexpr (PAGED) {
+      pu_s = u0;
+      fetch_pages();
+    }
     for (int s = 0; s < STAGES && u0 + s < u1; ++s) issue(s);
   }
   Cursor cc = locate(u0);   // consumer cursor
