@@ -78,17 +78,25 @@ def decode_attention(buf: np.ndarray, geom: Geometry, R: np.ndarray, layer: int,
     Keys/values: the seq_lens[b] cached tokens rebuilt for this loop, plus the
     current token's K/V straight from the BF16 temporary buffer ([EXPL]: the
     current token stays in BF16 until its last loop has run).
-    q, k_cur, v_cur: float64 [B, H, d].  rows: optional iterable of (b, h) to
-    evaluate (others left NaN).  Returns float64 [B, H, d]."""
-    B, H, d = q.shape
-    out = np.full((B, H, d), np.nan)
-    todo = rows if rows is not None else [(b, h) for b in range(B) for h in range(H)]
-    for b, h in todo:
+    q: float64 [B, Hq, d]; k_cur, v_cur: float64 [B, H, d] (H = the cache's KV
+    heads).  Hq = H is multi-head attention, the pages' models; Hq a multiple
+    of H is grouped-query attention (a reading: query head qh attends with KV
+    head qh // (Hq / H), consecutive query heads sharing one).  rows: optional
+    iterable of (b, qh) to evaluate (others left NaN).  Returns float64 [B, Hq, d]."""
+    B, Hq, d = q.shape
+    H = geom.num_heads
+    if Hq % H:
+        raise ValueError("query heads must be a multiple of the KV heads")
+    qpk = Hq // H
+    out = np.full((B, Hq, d), np.nan)
+    todo = rows if rows is not None else [(b, qh) for b in range(B) for qh in range(Hq)]
+    for b, qh in todo:
+        h = qh // qpk
         n = int(seq_lens[b])
         K, V = reconstruct(buf, geom, R, layer, group, b, h, loop, n, chained)
         K = np.concatenate([K, k_cur[b, h][None, :]], axis=0)
         V = np.concatenate([V, v_cur[b, h][None, :]], axis=0)
-        out[b, h] = attention(q[b, h], K, V, scale)
+        out[b, qh] = attention(q[b, qh], K, V, scale)
     return out
 
 

@@ -256,3 +256,34 @@ def test_paged_pool_moves_whole_tiles():
                             off += tb
                     assert off == head_block
     assert np.array_equal(back, buf)
+
+
+def test_grouped_query_attention_is_multi_head_over_copied_kv_heads():
+    """Grouped-query reading: query head qh attends with KV head qh // (Hq / H).
+    Pinned against multi-head attention over a cache whose heads are copies
+    (head qh of the copy = KV head qh // 2): the outputs are identical, and a
+    mapping like qh % H would fail."""
+    H, Hq, d, g, B = 2, 4, 64, 32, 2
+    geom = Lo.Geometry(1, 4, 1, H, d, g, B, 96)
+    geom_mha = Lo.Geometry(1, 4, 1, Hq, d, g, B, 96)
+    R = synth.rotation(d).astype(np.float32).astype(np.float64)
+    w = synth.Workload("t", 1, 4, 1, H, d, g, B, 96, synth.OURO_ALPHAS, True)
+    _, kv = synth.looped_kv(9, w, batch=B, ntok=70)                   # [P, 2, B, H, n, d]
+    buf = np.zeros(geom.total_bytes, dtype=np.uint8)
+    oracle.append(buf, geom, R, 0, 0, kv, [0, 0])
+    buf_mha = np.zeros(geom_mha.total_bytes, dtype=np.uint8)
+    oracle.append(buf_mha, geom_mha, R, 0, 0, np.repeat(kv, 2, axis=3), [0, 0])
+    buf_tiled = np.zeros(geom_mha.total_bytes, dtype=np.uint8)        # head qh = KV head qh % H
+    oracle.append(buf_tiled, geom_mha, R, 0, 0, np.tile(kv, (1, 1, 1, 2, 1, 1)), [0, 0])
+    rng = np.random.default_rng(2)
+    q = rng.standard_normal((B, Hq, d))
+    kc, vc = rng.standard_normal((B, H, d)), rng.standard_normal((B, H, d))
+    seq = np.array([70, 41])
+    for loop in (0, 3):
+        out = oracle.decode_attention(buf, geom, R, 0, 0, loop, q, kc, vc, seq, 0.125)
+        ref = oracle.decode_attention(buf_mha, geom_mha, R, 0, 0, loop, q, np.repeat(kc, 2, axis=1),
+                                      np.repeat(vc, 2, axis=1), seq, 0.125)
+        assert np.array_equal(out, ref)
+        wrong = oracle.decode_attention(buf_tiled, geom_mha, R, 0, 0, loop, q, np.tile(kc, (1, 2, 1)),
+                                        np.tile(vc, (1, 2, 1)), seq, 0.125)
+        assert not np.allclose(out, wrong)
