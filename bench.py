@@ -223,12 +223,13 @@ def run_reference(args, w):
     print(json.dumps(line))
 
 
-def _config(w, chained=False, hadamard=False, paged=False):
+def _config(w, chained=False, hadamard=False, paged=False, query_heads=None):
     return {"workload": f"{w.name}: {w.num_layers} layers x {w.loops_per_group} loops x {w.num_groups} groups, "
                         f"{w.num_heads} KV heads x {w.head_dim}, batch {w.batch}, {w.context}-token context, "
                         f"INT4 anchor + INT2 residuals, group {w.group_size}, "
                         f"{'chained' if chained else 'shared'} anchor"
-                        + (", Walsh-Hadamard rotation" if hadamard else "") + (", paged layout" if paged else ""),
+                        + (", Walsh-Hadamard rotation" if hadamard else "") + (", paged layout" if paged else "")
+                        + (f", {query_heads} query heads (grouped-query)" if query_heads else ""),
             "global_batch": w.batch, "seq_len": w.context, "parallelism": "replicas",
             "l2": "inputs larger than L2 (every step streams the whole compressed cache)"}
 
@@ -249,6 +250,8 @@ def main():
                     help="seconds of oracle work per reference step (default: about 150 s per run)")
     ap.add_argument("--quiet", action="store_true")
     ap.add_argument("--chained", action="store_true", help="chained anchors (loop l coded against loop l+1)")
+    ap.add_argument("--query-heads", type=int, default=None,
+                    help="query heads per row (a multiple of the KV heads: grouped-query attention)")
     ap.add_argument("--paged", action="store_true",
                     help="paged cache layout: pages assigned through a shuffled block table")
     ap.add_argument("--hadamard", action="store_true",
@@ -284,8 +287,9 @@ def run_rq(args, w):
     gen = torch.Generator(device=dev)
     gen.manual_seed(1234 + rank)
     R32 = None if args.hadamard else torch.from_numpy(synth.rotation(d).astype(np.float32)).to(dev)
+    Hq = args.query_heads or H   # grouped-query attention when Hq > H (the pages' models: Hq = H)
     cfg = rq.rq_config(L, P, G, H, d, g, B, N + 64, (rq.RQ_MODE_CHAINED if args.chained else rq.RQ_MODE_SHARED)
-                       | (rq.RQ_MODE_HADAMARD if args.hadamard else 0))
+                       | (rq.RQ_MODE_HADAMARD if args.hadamard else 0), Hq)
     if args.paged:
         # every row's tiles on pages of a shuffled table (the pool holds exactly those pages)
         ntiles = -(-(N + 64) // 64)
@@ -316,9 +320,9 @@ def run_rq(args, w):
     scale = 1.0 / math.sqrt(d)
     ncalls = L * G * P
     # per-step inputs: queries per call, the BF16 temporary buffer per (layer, group)
-    q_all = torch.randn((ncalls, B, H, d), generator=gen, device=dev).to(torch.bfloat16)
+    q_all = torch.randn((ncalls, B, Hq, d), generator=gen, device=dev).to(torch.bfloat16)
     temp_all = torch.stack([synth.looped_kv_torch(gen, w, B, 1, dev) for _ in range(L * G)])  # [LG,P,2,B,H,1,d]
-    out_all = torch.empty((ncalls, B, H, d), dtype=torch.float32, device=dev)
+    out_all = torch.empty((ncalls, B, Hq, d), dtype=torch.float32, device=dev)
 
     order = [(lp, layer, grp) for grp in range(G) for lp in range(P) for layer in range(L)]
 
@@ -415,7 +419,7 @@ def run_rq(args, w):
         try:
             tj = json.load(open(tp))
             if (tj.get("workload") == w.name and tj.get("batch") == B and tj.get("group_size") == g
-                    and not args.chained and not args.hadamard and not args.paged
+                    and not args.chained and not args.hadamard and not args.paged and not args.query_heads
                     and tj.get("kernel_source_hash") == _kernel_hash()):
                 traffic = tj.get("bytes_per_launch")
         except Exception:
@@ -426,7 +430,7 @@ def run_rq(args, w):
     line = {
         "metric": METRIC, "value": value, "unit": "tokens/s", "n_gpus": world, "steps": args.steps,
         "warmup": args.warmup, "ms_per_step": ms_step, "higher_is_better": True, "scaling": "weak",
-        "vs_baseline": None, "dtype": "int32/fp32", "data": "synthetic", "config": _config(w, args.chained, args.hadamard, args.paged),
+        "vs_baseline": None, "dtype": "int32/fp32", "data": "synthetic", "config": _config(w, args.chained, args.hadamard, args.paged, args.query_heads),
         "effective_gbps": step_gbs, "frac_of_hbm_peak": step_gbs / peak,
         "roofline": {"bound": "hbm", "achieved": achieved, "peak": peak, "unit": "GB/s",
                      "frac": achieved / peak, "traffic": traffic,
@@ -441,7 +445,7 @@ def run_rq(args, w):
         "prefill_s": prefill_s,
     }
     # BF16 comparator: the same 96 calls over uncompressed K/V
-    if not args.no_bf16:
+    if not args.no_bf16 and not args.query_heads:   # the BF16 comparator is multi-head
         line["bf16_comparator"] = bench_bf16(args, w, dev, gen, scale)
         # whole compressed step (appends included) against the BF16 attention calls alone
         line["speedup_vs_bf16"] = line["bf16_comparator"]["ms_per_step_attention"] / ms_step

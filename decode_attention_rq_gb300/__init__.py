@@ -49,9 +49,10 @@ class RqError(RuntimeError):
 
 
 class rq_config(ctypes.Structure):
+    """rq.h's rq_config; num_query_heads (last, default 0) > num_heads selects grouped-query attention."""
     _fields_ = [(n, ctypes.c_int32) for n in (
         "num_layers", "loops_per_group", "num_groups", "num_heads", "head_dim", "group_size",
-        "max_batch", "max_seq_len", "mode")]
+        "max_batch", "max_seq_len", "mode", "num_query_heads")]
 
 
 if not os.path.exists(LIB_PATH):

@@ -20,6 +20,9 @@ bool make_geom(const rq_config& c, Geom* g) {
   g->P = c.loops_per_group;
   g->G = c.num_groups;
   g->H = c.num_heads;
+  if (c.num_query_heads < 0 || (c.num_query_heads > 0 && c.num_query_heads % c.num_heads)) return false;
+  g->Hq = c.num_query_heads > 0 ? c.num_query_heads : c.num_heads;
+  g->qpk = g->Hq / g->H;
   g->d = c.head_dim;
   g->g = c.group_size;
   g->ng = c.head_dim / c.group_size;

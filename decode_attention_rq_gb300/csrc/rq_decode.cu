@@ -277,7 +277,7 @@ __global__ void __launch_bounds__(kThreads, (Cfg<D, GS, NRES>::MINB)) decode_ker
 
   pdl_launch_dependents();   // the merge kernel may start staging R
   const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
-  const int H = a.g.H, B = a.batch;
+  const int H = a.g.Hq, B = a.batch;   // units run over (row, query head); query head h reads KV head h / qpk
   const int Cn = gridDim.x, cta = blockIdx.x;
 
   // ---- per-row unit counts and prefix over (row, head) ----
@@ -343,7 +343,8 @@ __global__ void __launch_bounds__(kThreads, (Cfg<D, GS, NRES>::MINB)) decode_ker
   auto issue = [&](int stage) {
     const int t0 = pc.t * C::UT;
     const int ntile = unit_tiles();
-    const uint8_t* region = PAGED ? a.base : a.base + a.g.region_offset(a.layer, a.group, pc.b, pc.h);
+    const int kvh = pc.h / a.g.qpk;
+    const uint8_t* region = PAGED ? a.base : a.base + a.g.region_offset(a.layer, a.group, pc.b, kvh);
     uint8_t* dst = smem + stage * C::STAGE;
     mbar_arrive_expect_tx(&full_bar[stage], (uint32_t)(ntile * C::SUB));
     for (int k = 0; k < ntile; ++k) {
@@ -353,7 +354,7 @@ __global__ void __launch_bounds__(kThreads, (Cfg<D, GS, NRES>::MINB)) decode_ker
       if constexpr (PAGED) {
         const int page = max(checked_page(a.g, next_raw_s[k], a.status), 0);   // a bad entry reads page 0
         blk = a.base + (((int64_t)a.layer * a.g.G + a.group) * a.g.num_pages + page) * a.g.page_bytes +
-              (int64_t)pc.h * a.g.head_block;
+              (int64_t)kvh * a.g.head_block;
       }
       auto src = [&](bool anchor, int j, int kv) {
         if constexpr (PAGED)   // same offsets as Geom::tile_offset, with the tile sizes as constants
@@ -760,23 +761,40 @@ __global__ void __launch_bounds__(APPEND ? kAppendThreads : kMergeThreads, APPEN
   constexpr int UTOK = 2 * kTile;
   pdl_launch_dependents();   // the next call's prep may start loading R; it waits for this kernel
   const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
-  const int H = a.g.H, B = a.batch;
-  const int bh = APPEND ? blockIdx.x % (B * H) : blockIdx.x, b = bh / H, h = bh - b * H;
+  const int H = a.g.Hq, B = a.batch, Hkv = a.g.H;   // merge CTAs: one per (row, query head)
+  // APPEND: CTAs [0, B*Hq) merge, the first query head of each KV head also coding
+  // the token's K; CTAs [B*Hq, B*Hq + B*Hkv) code the V of one (row, KV head)
+  const bool v_cta = APPEND && (int)blockIdx.x >= B * H;
+  int bh, b, h, kvh;
+  if (v_cta) {
+    const int r = blockIdx.x - B * H;
+    b = r / Hkv;
+    kvh = r - b * Hkv;
+    h = kvh * a.g.qpk;
+    bh = b * H + h;
+  } else {
+    bh = blockIdx.x;
+    b = bh / H;
+    h = bh - b * H;
+    kvh = h / a.g.qpk;
+  }
+  const int kvbh = b * Hkv + kvh;   // the current token's K/V are per KV head
 
   // ---- before the wait: inputs the decode kernel does not write ----
   const bool hadamard = (a.g.mode & RQ_MODE_HADAMARD) != 0;   // R^T as the fast transform (d = 128)
   bool app_ok = false;
   int app_pos = 0, app_page = 0;
-  const int app_kvi = APPEND ? blockIdx.x / (B * H) : 0;
   uint8_t* app_smem = reinterpret_cast<uint8_t*>(R_s);
   if constexpr (APPEND) {
-    app_pos = a.seq_lens[b];
-    app_ok = token_append_compute<D>(a.g, const_cast<uint8_t*>(a.base), a.R, a.kv_all, B, a.layer, a.group, b, h,
-                                     app_kvi, app_pos, a.status, app_smem, &app_page);
-    if (app_kvi == 1) {   // the V half: store after the wait; the first CTA merges
+    if (v_cta || h % a.g.qpk == 0) {   // the same for every thread of the CTA
+      app_pos = a.seq_lens[b];
+      app_ok = token_append_compute<D>(a.g, const_cast<uint8_t*>(a.base), a.R, a.kv_all, B, a.layer, a.group, b,
+                                       kvh, v_cta ? 1 : 0, app_pos, a.status, app_smem, &app_page);
+    }
+    if (v_cta) {   // store after the wait; the merge CTAs merge
       pdl_wait();
       if (app_ok)
-        token_append_store<D>(a.g, const_cast<uint8_t*>(a.base), a.layer, a.group, b, h, 1, app_pos, app_page,
+        token_append_store<D>(a.g, const_cast<uint8_t*>(a.base), a.layer, a.group, b, kvh, 1, app_pos, app_page,
                               app_smem);
       return;
     }
@@ -791,7 +809,7 @@ __global__ void __launch_bounds__(APPEND ? kAppendThreads : kMergeThreads, APPEN
   float sc = 0.f;
   for (int k = tid; k < D; k += NT)
     sc += __bfloat162float(a.q[(size_t)bh * D + k]) * a.qscale *
-          __bfloat162float(a.k_cur[(size_t)bh * D + k]);
+          __bfloat162float(a.k_cur[(size_t)kvbh * D + k]);
   // units before this row and in total (same clamping and unit size as the decode kernel)
   int before = 0, total = 0;
   for (int r = tid; r < B; r += NT) {
@@ -813,12 +831,12 @@ __global__ void __launch_bounds__(APPEND ? kAppendThreads : kMergeThreads, APPEN
   const int ntb = (clamp_len(a.seq_lens[b], a.g.Nmax) + UTOK - 1) / UTOK;
   if (ntb == 0) {   // empty cache: attention over the current token alone
     for (int k = tid; k < D; k += NT)
-      a.out[(size_t)bh * D + k] = __bfloat162float(a.v_cur[(size_t)bh * D + k]);
+      a.out[(size_t)bh * D + k] = __bfloat162float(a.v_cur[(size_t)kvbh * D + k]);
     if (NRES > 0 && !hadamard) (void)mbar_wait_bounded(&r_bar, 0);   // the R copy lands before the CTA exits
     pdl_wait();   // completion of this kernel implies the decode kernel's
     if constexpr (APPEND)
       if (app_ok)
-        token_append_store<D>(a.g, const_cast<uint8_t*>(a.base), a.layer, a.group, b, h, 0, app_pos, app_page,
+        token_append_store<D>(a.g, const_cast<uint8_t*>(a.base), a.layer, a.group, b, kvh, 0, app_pos, app_page,
                               app_smem);
     return;
   }
@@ -830,7 +848,7 @@ __global__ void __launch_bounds__(APPEND ? kAppendThreads : kMergeThreads, APPEN
   pdl_wait();   // every partial of the decode kernel is written and visible
   if constexpr (APPEND)   // no kernel before this one is running: the new slot can be written
     if (app_ok)
-      token_append_store<D>(a.g, const_cast<uint8_t*>(a.base), a.layer, a.group, b, h, 0, app_pos, app_page,
+      token_append_store<D>(a.g, const_cast<uint8_t*>(a.base), a.layer, a.group, b, kvh, 0, app_pos, app_page,
                             app_smem);
 
   // this thread's element of the first contributors' accumulators, loaded while
@@ -869,7 +887,7 @@ __global__ void __launch_bounds__(APPEND ? kAppendThreads : kMergeThreads, APPEN
     for (int k = 0; k < PF; ++k)
       if (k < nc) v = fmaf(w_s[k], xa[k], v);
     for (int i = PF; i < nc; ++i) v = fmaf(w_s[i], __ldcg(pc + (size_t)i * a.pstride), v);
-    if (tid < D) va_s[tid] = fmaf(exp2f(s_cur - M), __bfloat162float(a.v_cur[(size_t)bh * D + tid]), v);
+    if (tid < D) va_s[tid] = fmaf(exp2f(s_cur - M), __bfloat162float(a.v_cur[(size_t)kvbh * D + tid]), v);
     else vr_s[tid - D] = v;
   }
   __syncthreads();
@@ -914,13 +932,13 @@ cudaError_t launch_t(const DecodeArgs& a, int num_sms, cudaStream_t stream) {
   auto km = merge_kernel<D, (NRES > 0 ? 1 : 0), false>;
   size_t km_smem = NRES > 0 ? (size_t)D * D * sizeof(float) : 0;
   if (a.g.mode & RQ_MODE_HADAMARD) km_smem = 0;   // no R to stage
-  int km_threads = kMergeThreads, km_ctas_per_bh = 1;
+  int km_threads = kMergeThreads, km_extra = 0;
   if constexpr (NRES == 0)
     if (a.kv_all) {
       km = merge_kernel<D, 0, true>;
       km_smem = TokenAppendSmem::bytes(a.g.P);
       km_threads = kAppendThreads;
-      km_ctas_per_bh = 2;
+      km_extra = a.batch * a.g.H;   // the V-coding CTAs, one per (row, KV head)
     }
   constexpr size_t merge_smem = NRES > 0 ? (size_t)D * D * sizeof(float) : 0;
   static int per_sm = 0;   // resident decode CTAs per SM (registers and shared memory)
@@ -953,12 +971,12 @@ cudaError_t launch_t(const DecodeArgs& a, int num_sms, cudaStream_t stream) {
   }
   const int grid = num_sms * per_sm;
   if (grid > kMaxContrib) return cudaErrorNotSupported;   // merge_kernel's contributor table
-  const int bhs = a.batch * a.g.H;
+  const int bhs = a.batch * a.g.Hq;   // (row, query head) pairs
   cudaError_t e = launch_dependent(qprep_kernel<D, GS, NRES>, dim3(bhs), dim3(kPrepThreads), 0, stream, a);
   if (e != cudaSuccess) return e;
   e = launch_dependent(k, dim3(grid), dim3(kThreads), (size_t)C::SMEM, stream, a);
   if (e != cudaSuccess) return e;
-  return launch_dependent(km, dim3(km_ctas_per_bh * bhs), dim3(km_threads), km_smem, stream, a, grid);
+  return launch_dependent(km, dim3(bhs + km_extra), dim3(km_threads), km_smem, stream, a, grid);
 }
 
 template <int D, int GS, bool PAGED>
@@ -985,12 +1003,12 @@ int decode_max_chained_loops() { return kMaxRes + 1; }
 
 // Workspace: status word (256 B slot) | partials (C + batch*H) x pstride floats | query packs.
 static size_t partials_bytes(const Geom& g, int batch, int num_sms) {
-  const size_t C = (size_t)num_sms * kMaxCtasPerSm, bh = (size_t)batch * g.H;
+  const size_t C = (size_t)num_sms * kMaxCtasPerSm, bh = (size_t)batch * g.Hq;
   return ((C + bh) * pstride_for(g.d) * sizeof(float) + 255) / 256 * 256;
 }
 
 size_t decode_workspace_bytes(const Geom& g, int batch, int num_sms) {
-  const size_t bh = (size_t)batch * g.H;
+  const size_t bh = (size_t)batch * g.Hq;
   return 256 + partials_bytes(g, batch, num_sms) + bh * g.ng * kPackWords * sizeof(uint32_t);
 }
 

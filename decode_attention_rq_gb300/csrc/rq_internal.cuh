@@ -21,6 +21,7 @@ constexpr unsigned long long kWaitNs = 2000000000ull;  // give up an mbarrier wa
 // Byte geometry of a cache (mirrors the layout statement in rq.h).
 struct Geom {
   int L, P, G, H, d, g, ng, Bmax, Nmax, ntiles, mode;
+  int Hq, qpk;                                      // query heads; query heads per KV head
   int64_t a_codes, r_codes, meta, a_tile, r_tile;   // per tile, bytes
   int64_t plane_a, plane_r, region;                 // bytes
   // paged layout (rq_cache_create_paged): tile t of row b is page table[b * max_tiles + t]

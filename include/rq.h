@@ -95,12 +95,16 @@ typedef struct rq_config {
   int32_t num_layers;       /* L: layers of the shared block */
   int32_t loops_per_group;  /* P: loops per anchor group; the last one is the anchor */
   int32_t num_groups;       /* G: loop groups (Ouro-1.4B: 1 group of 4; Huginn-3.5B: 8 of 4) */
-  int32_t num_heads;        /* H: KV heads (= query heads; multi-head attention) */
+  int32_t num_heads;        /* H: KV heads (the cache stores these) */
   int32_t head_dim;         /* d: 96 or 128 */
   int32_t group_size;       /* g: 16 or 32 channels per quantization group */
   int32_t max_batch;        /* rows of the cache */
   int32_t max_seq_len;      /* token capacity per (layer, group, row, head) */
-  int32_t mode;             /* rq_mode: SHARED or CHAINED, optionally | NORM_RATIO */
+  int32_t mode;             /* rq_mode: SHARED or CHAINED, optionally | NORM_RATIO | HADAMARD */
+  int32_t num_query_heads;  /* Hq: query heads; 0 (or H) = multi-head attention, else a multiple
+                               of H (grouped-query: query head qh attends with KV head
+                               qh / (Hq / H)).  Decode calls take q and out with Hq heads and
+                               the current token's K/V with H heads. */
 } rq_config;
 
 typedef struct rq_cache rq_cache;   /* opaque host-side handle; holds no device memory */

@@ -28,6 +28,7 @@ class Case:
     seed: int = 0
     scaling: str = "ls"      # "ls" (least squares) or "norm" (norm ratio)
     rotation: str = "dense"  # "dense" (R as given) or "hadamard" (fast Walsh-Hadamard, no R on the device)
+    Hq: int = 0              # query heads (0: = H, multi-head; else a multiple of H, grouped-query)
 
     def workload(self, anchor_is_base=True):
         alphas = synth.OURO_ALPHAS if self.P == 4 and anchor_is_base else tuple(
@@ -59,7 +60,7 @@ class GpuCache:
         self.cfg = rq.rq_config(case.L, case.P, case.G, case.H, case.d, case.g, case.B, case.Nmax,
                                 (rq.RQ_MODE_CHAINED if case.chained else rq.RQ_MODE_SHARED)
                                 | (rq.RQ_MODE_NORM_RATIO if case.scaling == "norm" else 0)
-                                | (rq.RQ_MODE_HADAMARD if case.rotation == "hadamard" else 0))
+                                | (rq.RQ_MODE_HADAMARD if case.rotation == "hadamard" else 0), case.Hq)
         self.nbytes = rq.rq_cache_bytes(self.cfg)
         assert self.nbytes > 0
         self.buf = torch.zeros(self.nbytes, dtype=torch.uint8, device=device)
@@ -92,7 +93,7 @@ class GpuCache:
         k_cur = k_cur.to(self.device).contiguous()
         v_cur = v_cur.to(self.device).contiguous()
         sl = torch.as_tensor(np.asarray(seq_lens, dtype=np.int32), device=self.device)
-        out = torch.empty((batch, self.case.H, self.case.d), dtype=torch.float32, device=self.device)
+        out = torch.empty((batch, self.case.Hq or self.case.H, self.case.d), dtype=torch.float32, device=self.device)
         self.rq.rq_decode_attention(self.handle, layer, group, loop, batch, q, k_cur, v_cur, sl, scale,
                                     out, self.ws, self.ws_bytes)
         return out
@@ -104,7 +105,7 @@ class GpuCache:
         q = q.to(self.device).contiguous()
         kv = kv_cur.to(self.device).contiguous()
         sl = torch.as_tensor(np.asarray(seq_lens, dtype=np.int32), device=self.device)
-        out = torch.empty((batch, self.case.H, self.case.d), dtype=torch.float32, device=self.device)
+        out = torch.empty((batch, self.case.Hq or self.case.H, self.case.d), dtype=torch.float32, device=self.device)
         self.rq.rq_decode_attention_append(self.handle, layer, group, batch, q, kv, sl, scale, out, self.ws,
                                            self.ws_bytes)
         return out
