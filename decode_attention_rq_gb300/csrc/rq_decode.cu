@@ -41,6 +41,14 @@
 //     shifts are needed.  The masks and the dot products run on separate
 //     pipes of the SM and overlap.
 //   * Online softmax in base 2 (scale * log2(e) folded into q).
+//   * Variants: grouped-query attention runs the units, the prep and the merge
+//     over (row, query head), each query head reading its KV head's tiles;
+//     the paged layout (decode_kernel<..., PAGED>) takes each tile's address
+//     from the block table, fetched one unit ahead by the producer thread;
+//     the Walsh-Hadamard mode replaces R q and R^T acc by the fast transform;
+//     the anchor-loop call can also append the current token in its merge
+//     kernel (rq_token_append.cuh).  Every kernel asks for the largest
+//     shared-memory carveout so that each can start beside the one before it.
 #include <cuda_fp8.h>
 
 #include "rq_internal.cuh"

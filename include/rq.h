@@ -23,7 +23,17 @@
  *     RQ_ERR_CUDA.  Faults inside a kernel surface on a later CUDA call.
  *   - Device pointers must be 16-byte aligned (RQ_ERR_ALIGNMENT).
  *   - Supported shapes: head_dim in {96, 128}; group_size in {16, 32} dividing
- *     head_dim; loops_per_group in [1, 16].  Others: RQ_ERR_UNSUPPORTED.
+ *     head_dim; loops_per_group in [1, 16]; num_query_heads a multiple of
+ *     num_heads.  Others: RQ_ERR_UNSUPPORTED.
+ *
+ * Entry points: rq_cache_bytes / rq_cache_create (contiguous layout) or
+ * rq_cache_paged_bytes / rq_cache_create_paged (block-table layout);
+ * rq_append (compress new tokens: prefill, or one decode token);
+ * rq_decode_workspace_bytes, rq_decode_attention (one loop's attention) and
+ * rq_decode_attention_append (the anchor loop's attention plus the current
+ * token's append); rq_decode_attention_noalloc (scratch inside the library);
+ * rq_bf16_workspace_bytes / rq_decode_attention_bf16 (the uncompressed
+ * comparator); rq_status_string.
  *
  * ---------------------------------------------------------------------------
  * Cache byte layout (this library's format; the pages fix the record
