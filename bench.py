@@ -538,11 +538,18 @@ def bench_e2e(args, graph, s, q_all, temp_all, out_all, B):
 
 
 def _kernel_hash():
+    """Hash of the kernel sources with comments and blank lines dropped (a comment
+    edit does not change the kernels the traffic counters were taken on)."""
     import hashlib
+    import re
     h = hashlib.sha256()
     csrc = os.path.join(ROOT, "decode_attention_rq_gb300", "csrc")
     for f in sorted(os.listdir(csrc)):
-        h.update(open(os.path.join(csrc, f), "rb").read())
+        text = open(os.path.join(csrc, f), encoding="utf-8").read()
+        text = re.sub(r"/\*.*?\*/", "", text, flags=re.S)
+        text = re.sub(r"//[^\n]*", "", text)
+        code = "\n".join(line.rstrip() for line in text.splitlines() if line.strip())
+        h.update(f.encode() + b"\0" + code.encode())
     return h.hexdigest()[:16]
 
 
