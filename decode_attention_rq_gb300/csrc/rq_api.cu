@@ -169,6 +169,7 @@ rq_status rq_decode_attention(rq_cache* cache, int32_t layer, int32_t group, int
       batch <= 0)
     return RQ_ERR_INVALID_ARG;
   if (batch > g.Bmax) return RQ_ERR_CAPACITY;
+  if (batch > RQ_MAX_DECODE_BATCH) return RQ_ERR_UNSUPPORTED;
   if ((g.mode & RQ_MODE_CHAINED) && g.P > decode_max_chained_loops()) return RQ_ERR_UNSUPPORTED;
   if (workspace_bytes < decode_workspace_bytes(g, batch, cache->num_sms)) return RQ_ERR_WORKSPACE;
   if (!aligned16(q) || !aligned16(k_cur) || !aligned16(v_cur) || !aligned16(seq_lens) ||
@@ -190,6 +191,7 @@ rq_status rq_decode_attention_append(rq_cache* cache, int32_t layer, int32_t gro
   const Geom& g = cache->geom;
   if (layer < 0 || layer >= g.L || group < 0 || group >= g.G || batch <= 0) return RQ_ERR_INVALID_ARG;
   if (batch > g.Bmax) return RQ_ERR_CAPACITY;
+  if (batch > RQ_MAX_DECODE_BATCH) return RQ_ERR_UNSUPPORTED;
   if ((g.mode & RQ_MODE_CHAINED) && g.P > decode_max_chained_loops()) return RQ_ERR_UNSUPPORTED;
   if (workspace_bytes < decode_workspace_bytes(g, batch, cache->num_sms)) return RQ_ERR_WORKSPACE;
   if (!aligned16(q) || !aligned16(kv_cur) || !aligned16(seq_lens) || !aligned16(out) ||
@@ -218,6 +220,7 @@ rq_status rq_decode_attention_bf16(const void* k_cache, const void* v_cache, con
   if (!k_cache || !v_cache || !k_cur || !v_cur || !q || !seq_lens || !out || !workspace)
     return RQ_ERR_INVALID_ARG;
   if (batch <= 0 || num_heads <= 0 || max_seq <= 0) return RQ_ERR_INVALID_ARG;
+  if (batch > RQ_MAX_DECODE_BATCH) return RQ_ERR_UNSUPPORTED;
   if (head_dim != 96 && head_dim != 128) return RQ_ERR_UNSUPPORTED;
   int sms = current_sms();
   if (sms <= 0) return RQ_ERR_CUDA;

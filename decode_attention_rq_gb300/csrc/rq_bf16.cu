@@ -14,7 +14,7 @@ namespace {
 constexpr int kThreads = 256;
 constexpr int kCtasPerSm = 2;
 constexpr int kStages = 3;
-constexpr int kMaxRows = 256;
+constexpr int kMaxRows = RQ_MAX_DECODE_BATCH;
 constexpr float kLog2e = 1.4426950408889634f;
 
 struct Bf16Args {

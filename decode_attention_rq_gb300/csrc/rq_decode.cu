@@ -59,7 +59,7 @@ namespace {
 
 constexpr int kThreads = 256;
 constexpr int kMaxCtasPerSm = 3;     // the workspace holds partials for this many CTAs per SM
-constexpr int kMaxRows = 256;          // batch rows one call may cover
+constexpr int kMaxRows = RQ_MAX_DECODE_BATCH;   // batch rows one call may cover
 constexpr int kMaxRes = 3;             // residual planes one call may read (chained, 4 loops)
 constexpr float kLog2e = 1.4426950408889634f;
 constexpr float kFix = 32767.f;        // 16-bit fixed point: values in [-32767, 32767]

@@ -71,6 +71,7 @@ extern "C" rq_status rq_decode_attention_noalloc(rq_cache* cache, int32_t layer,
       batch <= 0)
     return RQ_ERR_INVALID_ARG;
   if (batch > g.Bmax) return RQ_ERR_CAPACITY;
+  if (batch > RQ_MAX_DECODE_BATCH) return RQ_ERR_UNSUPPORTED;
   if ((g.mode & RQ_MODE_CHAINED) && g.P > decode_max_chained_loops()) return RQ_ERR_UNSUPPORTED;
   const size_t need = decode_workspace_bytes(g, batch, cache->num_sms);
   if (need > (size_t)RQ_NOALLOC_WORKSPACE_BYTES) return RQ_ERR_WORKSPACE;

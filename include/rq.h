@@ -248,6 +248,10 @@ rq_status rq_decode_attention_append(rq_cache* cache, int32_t layer, int32_t gro
                                      float softmax_scale, float* out, void* workspace,
                                      size_t workspace_bytes, void* stream);
 
+/* Rows one decode call (rq_decode_attention, _append, _noalloc, _bf16) may
+ * cover; a larger batch returns RQ_ERR_UNSUPPORTED (split it into calls). */
+#define RQ_MAX_DECODE_BATCH 256
+
 /* Size of the workspace built into the library for rq_decode_attention_noalloc
  * (2 MiB of device memory, held on every device that loads the library until
  * the process exits).  With 152 SMs, head_dim 128 and group size 32 it

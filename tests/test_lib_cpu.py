@@ -92,6 +92,7 @@ def test_bf16_argument_checks(rq):
     assert f(p, p, p, p, p, p, 2, 4, 64, 100, 0.1, p, p, 1 << 30, None) == 6      # head_dim
     assert f(p, p, p, p, p, None, 2, 4, 128, 100, 0.1, p, p, 1 << 30, None) == 1  # null
     assert f(p, p, p, p, p, p, 0, 4, 128, 100, 0.1, p, p, 1 << 30, None) == 1     # batch
+    assert f(p, p, p, p, p, p, 257, 4, 128, 100, 0.1, p, p, 1 << 30, None) == 6   # above RQ_MAX_DECODE_BATCH
     assert rq.rq_bf16_workspace_bytes(2, 4, 64) == 0
 
 
