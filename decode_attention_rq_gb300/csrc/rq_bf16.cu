@@ -225,9 +225,9 @@ __global__ void __launch_bounds__(kThreads, kCtasPerSm) bf16_kernel(Bf16Args a) 
     }
     __syncthreads();
     const float m_new = fmaxf(m_run, fmaxf(red_s[0], red_s[1]));
-    const float alpha = exp2f(m_run - m_new);
+    const float alpha = ex2_fast(m_run - m_new);
     if (tid < kTile) {
-      float p = tid < n_valid ? exp2f(s_tok - m_new) : 0.f;
+      float p = tid < n_valid ? ex2_fast(s_tok - m_new) : 0.f;
       p_s[tid] = p;
       for (int off = 16; off > 0; off >>= 1) p += __shfl_xor_sync(0xffffffffu, p, off);
       if (lane == 0) red_s[2 + warp] = p;

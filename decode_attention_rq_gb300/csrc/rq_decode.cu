@@ -597,7 +597,7 @@ __global__ void __launch_bounds__(kThreads, (Cfg<D, GS, NRES>::MINB)) decode_ker
 #pragma unroll
     for (int w = 1; w < kThreads / 32; ++w) m_tile = fmaxf(m_tile, red_s[buf][w]);
     const float m_new = fmaxf(m_run, m_tile);
-    const float alpha = exp2f(m_run - m_new);   // 0 on the first unit (m_run = -inf)
+    const float alpha = ex2_fast(m_run - m_new);   // 0 on the first unit (m_run = -inf)
     m_run = m_new;
 
     // the maxima of the other parity were last read before B1: clear them for the next unit
@@ -611,7 +611,7 @@ __global__ void __launch_bounds__(kThreads, (Cfg<D, GS, NRES>::MINB)) decode_ker
 #pragma unroll
     for (int pp = 0; pp < PPT; ++pp) {
       const int tok = (tid + pp * kThreads) / NGP;
-      const float pt = exp2f(sc[pp] - m_new);          // 0 for masked tokens
+      const float pt = ex2_fast(sc[pp] - m_new);       // 0 for masked tokens
       if (gi1 == 0) l_part = fmaf(l_part, pp == 0 ? alpha : 1.f, pt);
 #pragma unroll
       for (int j = 0; j <= NRES; ++j) wv[pp][j] = 0.f;
@@ -647,7 +647,9 @@ __global__ void __launch_bounds__(kThreads, (Cfg<D, GS, NRES>::MINB)) decode_ker
 #pragma unroll
       for (int j = 0; j <= NRES; ++j) {
         const float mx = __uint_as_float(tmax_s[buf][j * NG + gi1]);
-        const float inv = mx > 0.f ? kFix / mx : 0.f;
+        // any scale near kFix / mx works: the weights are clamped to the 16-bit
+        // range and dequantized with mx / kFix
+        const float inv = mx > 0.f ? __fdividef(kFix, mx) : 0.f;
         uint8_t* wq = wq_s[j * NG + gi1];
 #pragma unroll
         for (int pp = 0; pp < PPT; ++pp) {

@@ -174,6 +174,15 @@ __device__ __forceinline__ float2 e4m3x2_to_f32x2(uint16_t v) {
   __half2 hh = *reinterpret_cast<__half2*>(&h2);
   return __half22float2(hh);
 }
+// 2^x by the SFU's approximation (relative error about 2^-22; results below the
+// normal range flush to 0; 2^-inf = 0): the softmax weights of the streaming
+// loops, which are then rounded to 16-bit fixed point or summed in float32.
+__device__ __forceinline__ float ex2_fast(float x) {
+  float y;
+  asm("ex2.approx.ftz.f32 %0, %1;" : "=f"(y) : "f"(x));
+  return y;
+}
+
 // Walsh-Hadamard rotation (RQ_MODE_HADAMARD, d = 128): u = H v / sqrt(128) for
 // NT vectors whose channels are held one per thread (thread i < 128 holds
 // channel i of each).  Butterfly stages h = 1, 2, ..., 64 turn every pair
