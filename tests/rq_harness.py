@@ -6,7 +6,6 @@ side is oracle/.  The only thing they share is the input generator (synth).
 from __future__ import annotations
 
 import dataclasses
-from typing import Optional
 
 import numpy as np
 import torch

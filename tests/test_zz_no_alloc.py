@@ -12,7 +12,6 @@ run every other test; it also passes when run on its own.
 """
 import math
 
-import numpy as np
 import pytest
 import torch
 
