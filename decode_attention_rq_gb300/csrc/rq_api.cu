@@ -180,7 +180,7 @@ rq_status rq_decode_attention(rq_cache* cache, int32_t layer, int32_t group, int
                                 static_cast<const __nv_bfloat16*>(k_cur),
                                 static_cast<const __nv_bfloat16*>(v_cur), seq_lens, softmax_scale,
                                 out, workspace, static_cast<cudaStream_t>(stream));
-  return e == cudaSuccess ? RQ_OK : RQ_ERR_CUDA;
+  return e == cudaSuccess ? RQ_OK : (e == cudaErrorNotSupported ? RQ_ERR_UNSUPPORTED : RQ_ERR_CUDA);
 }
 
 rq_status rq_decode_attention_append(rq_cache* cache, int32_t layer, int32_t group, int32_t batch,
@@ -204,7 +204,7 @@ rq_status rq_decode_attention_append(rq_cache* cache, int32_t layer, int32_t gro
   cudaError_t e = launch_decode(*cache, layer, group, g.P - 1, batch, static_cast<const __nv_bfloat16*>(q),
                                 k_cur, k_cur + block, seq_lens, softmax_scale, out, workspace,
                                 static_cast<cudaStream_t>(stream), kv);
-  return e == cudaSuccess ? RQ_OK : RQ_ERR_CUDA;
+  return e == cudaSuccess ? RQ_OK : (e == cudaErrorNotSupported ? RQ_ERR_UNSUPPORTED : RQ_ERR_CUDA);
 }
 
 size_t rq_bf16_workspace_bytes(int32_t batch, int32_t num_heads, int32_t head_dim) {

@@ -89,7 +89,7 @@ extern "C" rq_status rq_decode_attention_noalloc(rq_cache* cache, int32_t layer,
                                 static_cast<const __nv_bfloat16*>(k_cur),
                                 static_cast<const __nv_bfloat16*>(v_cur), seq_lens, softmax_scale,
                                 out, ws, st);
-  if (e != cudaSuccess) return RQ_ERR_CUDA;
+  if (e != cudaSuccess) return e == cudaErrorNotSupported ? RQ_ERR_UNSUPPORTED : RQ_ERR_CUDA;
   // the status word sits in the array's first 16 bytes; hand it to the caller if asked
   if (status && cudaMemcpyAsync(status, ws, 16, cudaMemcpyDeviceToDevice, st) != cudaSuccess)
     return RQ_ERR_CUDA;

@@ -216,7 +216,9 @@ size_t rq_decode_workspace_bytes(const rq_config* cfg, int32_t batch);
  * then combines the partial softmax
  * states, adds the current token and applies R^T once.
  * Chained mode reads the anchor and every residual plane from this loop to
- * the anchor; decode supports it for loops_per_group <= 4 (UNSUPPORTED beyond).
+ * the anchor; decode supports it for loops_per_group <= 8 (UNSUPPORTED beyond,
+ * and for head_dim 128 with group_size 16 and 8 loops: one call's working set
+ * would not fit one SM's shared memory).
  * Errors: INVALID_ARG, CAPACITY (batch > max_batch), WORKSPACE, ALIGNMENT,
  * UNSUPPORTED, CUDA. */
 rq_status rq_decode_attention(rq_cache* cache, int32_t layer, int32_t group, int32_t loop,

@@ -328,17 +328,32 @@ def test_large_loop_groups_shared(P, d):
     print(f"P={P}: worst max-abs error {worst:.3e}; cache bytes equal")
 
 
-def test_large_chained_group_appends_and_decode_limit():
-    """Chained groups of 8 loops: appends (each loop coded against the rebuilt next
-    one) match byte for byte; decode supports chained groups of up to 4 loops and
-    refuses longer ones with UNSUPPORTED."""
+@pytest.mark.parametrize("d,g", [(128, 32), (96, 16)])
+def test_large_chained_groups(d, g):
+    """Chained groups of 8 loops: appends (each loop coded against the rebuilt
+    next one) match byte for byte; every loop decodes within 2e-3 (loop 0 reads
+    the anchor and seven residual planes).  Chained groups of 16 loops are
+    refused with UNSUPPORTED (a call would read fifteen planes)."""
     import decode_attention_rq_gb300 as rq
-    case = Case(L=1, P=8, G=1, H=2, d=128, g=32, B=1, Nmax=128, seed=21, chained=True)
-    gpu, geom, obuf, R, _ = _build_both(case, chunks=[100], anchor_is_base=False)
+    case = Case(L=1, P=8, G=1, H=2, d=d, g=g, B=2, Nmax=192, seed=21, chained=True)
+    gpu, geom, obuf, R, _ = _build_both(case, chunks=[130, 1], anchor_is_base=False)
     assert np.array_equal(gpu.bytes_host(), obuf)
-    qb, q, kcb, kc, vcb, vc = _queries(case, 50, 0)
+    seq = np.array([131, 70])
+    scale = 1 / math.sqrt(d)
+    worst = 0.0
+    for loop in (0, 3, 6, 7):
+        qb, q, kcb, kc, vcb, vc = _queries(case, 50, loop)
+        out = gpu.decode(0, 0, loop, qb, kcb, vcb, seq, scale).cpu().numpy()
+        ref = oracle.decode_attention(obuf, geom, R, 0, 0, loop, q, kc, vc, seq, scale, chained=True)
+        err = float(np.abs(out - ref).max())
+        worst = max(worst, err)
+        assert err <= ATOL, f"loop {loop}: max abs err {err:.3e}"
+    assert gpu.status.tolist() == [0, 0, 0, 0]
+    print(f"chained P=8 d={d} g={g}: worst max-abs error {worst:.3e}; cache bytes equal")
+    big = GpuCache(Case(L=1, P=16, G=1, H=2, d=d, g=g, B=1, Nmax=64, seed=22, chained=True), rotation32(d)[0])
+    qb, q, kcb, kc, vcb, vc = _queries(case, 51, 0)
     with pytest.raises(rq.RqError) as e:
-        gpu.decode(0, 0, 0, qb, kcb, vcb, np.array([100]), 0.1)
+        big.decode(0, 0, 0, qb[:1], kcb[:1], vcb[:1], np.array([10]), 0.1, batch=1)
     assert e.value.status == 6   # RQ_ERR_UNSUPPORTED
 
 
