@@ -35,7 +35,7 @@ class PagedCache(GpuCache):
         self.rq, self.case, self.device = rq, case, device
         self.cfg = rq.rq_config(case.L, case.P, case.G, case.H, case.d, case.g, case.B, case.Nmax,
                                 (rq.RQ_MODE_CHAINED if case.chained else rq.RQ_MODE_SHARED)
-                                | (rq.RQ_MODE_HADAMARD if case.rotation == "hadamard" else 0))
+                                | (rq.RQ_MODE_HADAMARD if case.rotation == "hadamard" else 0), case.Hq)
         self.nbytes = rq.rq_cache_paged_bytes(self.cfg, num_pages)
         assert self.nbytes > 0
         self.buf = torch.zeros(self.nbytes, dtype=torch.uint8, device=device)
@@ -141,3 +141,42 @@ def test_paged_out_of_range_entry_is_not_followed():
     torch.cuda.synchronize()
     assert torch.isfinite(out).all()
     assert int(bad.status[2]) == 1 and int(bad.status[0]) == 0
+
+
+def test_paged_grouped_query_chained_eight_loops_hadamard():
+    """The options together: paged layout, grouped-query heads (Hq = 2H), chained
+    groups of 8 loops (a call reads up to seven residual planes), Walsh-Hadamard
+    rotation.  Pool bytes equal the oracle's paged view after the prefill and
+    after a fused anchor-loop call; every loop within 2e-3 of the oracle."""
+    case = Case(L=1, P=8, G=1, H=2, d=128, g=32, B=2, Nmax=192, seed=73, chained=True, rotation="hadamard", Hq=4)
+    R32, R = rotation32(case.d, kind="hadamard")
+    table, num_pages = _table(case, seed=6)
+    paged = PagedCache(case, R32, table, num_pages)
+    geom = _geom(case)
+    obuf = np.zeros(geom.total_bytes, dtype=np.uint8)
+    start = np.array([0, 20], dtype=np.int64)
+    kvb, kv = kv_for(case, 730, 100, anchor_is_base=False)
+    paged.append(0, 0, kvb, start)
+    oracle.append(obuf, geom, R, 0, 0, kv, start, chained=True, rotation="hadamard")
+    assert np.array_equal(paged.bytes_host(), oracle.paged_pool(obuf, geom, table, num_pages))
+    seq = start + 100
+    scale = 1.0 / math.sqrt(case.d)
+    worst = 0.0
+    for loop in (0, 4, 7):
+        qb, q = synth.queries(740 + loop, case.B, 4, case.d)
+        kvb_c, kv_c = kv_for(case, 750 + loop, 1, anchor_is_base=False)
+        if loop < 7:
+            out = paged.decode(0, 0, loop, qb, kvb_c[loop, 0, :, :, 0], kvb_c[loop, 1, :, :, 0], seq, scale)
+            ref = oracle.decode_attention(obuf, geom, R, 0, 0, loop, q, kv_c[loop, 0, :, :, 0],
+                                          kv_c[loop, 1, :, :, 0], seq, scale, chained=True)
+        else:
+            out = paged.decode_append(0, 0, qb, kvb_c[..., 0, :], seq, scale)
+            ref, ok = oracle.decode_attention_append(obuf, geom, R, 0, 0, q, kv_c[..., 0, :], seq, scale,
+                                                     chained=True, rotation="hadamard")
+            assert ok.all()
+        err = float(np.abs(out.cpu().numpy() - ref).max())
+        worst = max(worst, err)
+        assert err <= ATOL, f"loop {loop}: max |gpu - oracle| = {err:.3e}"
+    assert np.array_equal(paged.bytes_host(), oracle.paged_pool(obuf, geom, table, num_pages))
+    assert paged.status.tolist() == [0, 0, 0, 0]
+    print(f"paged + GQA + chained P=8 + Hadamard: worst max-abs error {worst:.3e}; pool bytes equal")
