@@ -170,9 +170,9 @@ __global__ void __launch_bounds__(kThreads) append_kernel(AppendArgs a) {
   __shared__ bool valid_s[kTok];
 
   // launched as a programmatic dependent: seq_lens and kv may come from the kernel
-  // ahead of this one; the next kernel is released once they are visible
+  // ahead of this one.  It writes the cache, so it does not release the next
+  // kernel early: that one starts once this kernel has finished.
   pdl_wait();
-  pdl_launch_dependents();
   const int start = a.seq_lens[b];
   if (start < 0 || start + a.n > a.g.Nmax) {
     if (blockIdx.x == 0 && h == 0 && blockIdx.z == 0 && tid == 0 && a.status) atomicExch(&a.status[1], 1);

@@ -140,10 +140,14 @@ __global__ void __launch_bounds__(kPrepThreads) qprep_kernel(DecodeArgs a) {
   // Launched as a programmatic dependent of whatever precedes the call on the
   // stream: everything else read here (q) or written (the packs, which the
   // previous call's decode kernel may still read) waits for that kernel.  The
-  // decode kernel is released only after this wait, so its own early reads
-  // (seq_lens, the cache) also follow it.
-  pdl_wait();
+  // decode kernel is released at once: while the previous call drains, it
+  // splits the work and starts its first cache copies.  What it reads before
+  // its own wait (seq_lens, the cache) no kernel of this library writes while
+  // released early: the kernels that write the cache (the append kernel, the
+  // anchor-loop merge with the token append) release their dependents only when
+  // they complete, and a caller's kernel does so too.
   pdl_launch_dependents();
+  pdl_wait();
   if (tid < D) q_s[tid] = __bfloat162float(a.q[(size_t)bh * D + tid]) * a.qscale;
   for (int i = tid; i < NG * kPackWords; i += kPrepThreads) img_s[i] = 0u;
   __syncthreads();
@@ -730,7 +734,9 @@ __global__ void __launch_bounds__(APPEND ? kAppendThreads : kMergeThreads, APPEN
   __shared__ float ml_s[2];
   __shared__ uint64_t r_bar;
   constexpr int UTOK = 2 * kTile;
-  pdl_launch_dependents();   // the next call's prep may start loading R; it waits for this kernel
+  // the next call's prep may start loading R (it waits for this kernel); the
+  // appending variant writes the cache, so its dependents wait for it to finish
+  if constexpr (!APPEND) pdl_launch_dependents();
   const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
   const int H = a.g.Hq, B = a.batch, Hkv = a.g.H;   // merge CTAs: one per (row, query head)
   // APPEND: CTAs [0, B*Hq) merge, the first query head of each KV head also coding
@@ -801,10 +807,11 @@ __global__ void __launch_bounds__(APPEND ? kAppendThreads : kMergeThreads, APPEN
   for (int w = 0; w < NT / 32; ++w) { s_cur += redf_s[w]; pre += redi_s[0][w]; U += redi_s[1][w]; }
   const int ntb = (clamp_len(a.seq_lens[b], a.g.Nmax) + UTOK - 1) / UTOK;
   if (ntb == 0) {   // empty cache: attention over the current token alone
-    for (int k = tid; k < D; k += NT)
-      a.out[(size_t)bh * D + k] = __bfloat162float(a.v_cur[(size_t)kvbh * D + k]);
     if (NRES > 0 && !hadamard) (void)mbar_wait_bounded(&r_bar, 0);   // the R copy lands before the CTA exits
     pdl_wait();   // completion of this kernel implies the decode kernel's
+    // written after the wait: the previous call's merge may still write its output
+    for (int k = tid; k < D; k += NT)
+      a.out[(size_t)bh * D + k] = __bfloat162float(a.v_cur[(size_t)kvbh * D + k]);
     if constexpr (APPEND)
       if (app_ok)
         token_append_store<D>(a.g, const_cast<uint8_t*>(a.base), a.layer, a.group, b, kvh, 0, app_pos, app_page,
