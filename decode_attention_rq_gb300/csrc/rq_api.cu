@@ -140,6 +140,7 @@ rq_status rq_cache_destroy(rq_cache* cache) {
 rq_status rq_append(rq_cache* cache, int32_t layer, int32_t group, int32_t batch, const void* kv,
                     const int32_t* seq_lens, int32_t n_tokens, int32_t* status, void* stream) {
   if (!cache || !kv || !seq_lens) return RQ_ERR_INVALID_ARG;
+  if (!on_cache_device(*cache)) return RQ_ERR_INVALID_ARG;
   const Geom& g = cache->geom;
   if (layer < 0 || layer >= g.L || group < 0 || group >= g.G || batch <= 0 || n_tokens < 0)
     return RQ_ERR_INVALID_ARG;
@@ -164,6 +165,7 @@ rq_status rq_decode_attention(rq_cache* cache, int32_t layer, int32_t group, int
                               void* workspace, size_t workspace_bytes, void* stream) {
   if (!cache || !q || !k_cur || !v_cur || !seq_lens || !out || !workspace)
     return RQ_ERR_INVALID_ARG;
+  if (!on_cache_device(*cache)) return RQ_ERR_INVALID_ARG;
   const Geom& g = cache->geom;
   if (layer < 0 || layer >= g.L || group < 0 || group >= g.G || loop < 0 || loop >= g.P ||
       batch <= 0)
@@ -188,6 +190,7 @@ rq_status rq_decode_attention_append(rq_cache* cache, int32_t layer, int32_t gro
                                      float softmax_scale, float* out, void* workspace,
                                      size_t workspace_bytes, void* stream) {
   if (!cache || !q || !kv_cur || !seq_lens || !out || !workspace) return RQ_ERR_INVALID_ARG;
+  if (!on_cache_device(*cache)) return RQ_ERR_INVALID_ARG;
   const Geom& g = cache->geom;
   if (layer < 0 || layer >= g.L || group < 0 || group >= g.G || batch <= 0) return RQ_ERR_INVALID_ARG;
   if (batch > g.Bmax) return RQ_ERR_CAPACITY;

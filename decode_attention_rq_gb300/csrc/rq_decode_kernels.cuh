@@ -5,6 +5,8 @@
 // parallel).  The design notes are at the top of rq_decode.cu.
 #pragma once
 
+#include <atomic>
+
 #include <cuda_fp8.h>
 #include "rq_internal.cuh"
 #include "rq_token_append.cuh"
@@ -919,12 +921,19 @@ cudaError_t launch_t(const DecodeArgs& a, int num_sms, cudaStream_t stream) {
       km_extra = a.batch * a.g.H;   // the V-coding CTAs, one per (row, KV head)
     }
   constexpr size_t merge_smem = NRES > 0 ? (size_t)D * D * sizeof(float) : 0;
-  static int per_sm = 0;   // resident decode CTAs per SM (registers and shared memory)
+  // Kernel attributes are per device: they are set, and the resident decode CTAs
+  // per SM (registers and shared memory) found, on the first call made with each
+  // device current.  Two threads racing on a first call both set the same values.
+  static std::atomic<int> per_sm_dev[kMaxDevices];
+  int dev = 0;
+  cudaError_t e0 = cudaGetDevice(&dev);
+  if (e0 != cudaSuccess) return e0;
+  if (dev < 0 || dev >= kMaxDevices) return cudaErrorInvalidDevice;
+  int per_sm = per_sm_dev[dev].load(std::memory_order_acquire);
   if (per_sm == 0) {
     // the stages and the kernel's own shared memory must fit one CTA's limit
-    int dev = 0, optin = 0;
-    cudaError_t e0 = cudaGetDevice(&dev);
-    if (e0 == cudaSuccess) e0 = cudaDeviceGetAttribute(&optin, cudaDevAttrMaxSharedMemoryPerBlockOptin, dev);
+    int optin = 0;
+    e0 = cudaDeviceGetAttribute(&optin, cudaDevAttrMaxSharedMemoryPerBlockOptin, dev);
     if (e0 != cudaSuccess) return e0;
     cudaFuncAttributes fa;
     e0 = cudaFuncGetAttributes(&fa, k);
@@ -955,6 +964,7 @@ cudaError_t launch_t(const DecodeArgs& a, int num_sms, cudaStream_t stream) {
     if (e != cudaSuccess) return e;
     if (occ < 1) return cudaErrorNotSupported;
     per_sm = occ < C::MINB ? occ : C::MINB;
+    per_sm_dev[dev].store(per_sm, std::memory_order_release);
   }
   const int grid = num_sms * per_sm;
   if (grid > kMaxContrib) return cudaErrorNotSupported;   // merge_kernel's contributor table

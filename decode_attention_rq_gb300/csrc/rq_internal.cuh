@@ -65,6 +65,18 @@ struct rq_cache {
 
 namespace rq {
 
+// Device ordinals the launchers keep per-device state for (kernel attributes,
+// the no-allocation workspace address).
+constexpr int kMaxDevices = 64;
+
+// True when the device current on the calling thread is the one the cache was
+// created on: the cache's memory, R and the caller's tensors live there, and a
+// kernel launched on another device would read addresses it cannot map.
+inline bool on_cache_device(const rq_cache& c) {
+  int dev = -1;
+  return cudaGetDevice(&dev) == cudaSuccess && dev == c.device;
+}
+
 // ---- launchers (one per translation unit) ----
 cudaError_t launch_append(const rq_cache& c, int layer, int group, int batch,
                           const __nv_bfloat16* kv, const int32_t* seq_lens, int n_tokens,

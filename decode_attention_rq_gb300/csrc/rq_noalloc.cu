@@ -32,7 +32,6 @@ static __device__ __align__(256) uint8_t g_noalloc_workspace[RQ_NOALLOC_WORKSPAC
 namespace rq {
 namespace {
 
-constexpr int kMaxDevices = 64;
 std::mutex g_noalloc_mutex;
 void* g_noalloc_ptr[kMaxDevices];   // device address of the array, per device ordinal
 
@@ -66,6 +65,7 @@ extern "C" rq_status rq_decode_attention_noalloc(rq_cache* cache, int32_t layer,
                                                  const int32_t* seq_lens, float softmax_scale,
                                                  float* out, int32_t* status, void* stream) {
   if (!cache || !q || !k_cur || !v_cur || !seq_lens || !out) return RQ_ERR_INVALID_ARG;
+  if (!on_cache_device(*cache)) return RQ_ERR_INVALID_ARG;
   const Geom& g = cache->geom;
   if (layer < 0 || layer >= g.L || group < 0 || group >= g.G || loop < 0 || loop >= g.P ||
       batch <= 0)

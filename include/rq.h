@@ -22,6 +22,9 @@
  *     return a status; nothing is launched then.  A failed launch returns
  *     RQ_ERR_CUDA.  Faults inside a kernel surface on a later CUDA call.
  *   - Device pointers must be 16-byte aligned (RQ_ERR_ALIGNMENT).
+ *   - A cache belongs to the device that was current when it was created;
+ *     a call on it made with another device current returns
+ *     RQ_ERR_INVALID_ARG (its memory is not addressable from there).
  *   - Supported shapes: head_dim in {96, 128}; group_size in {16, 32} dividing
  *     head_dim; loops_per_group in [1, 16]; num_query_heads a multiple of
  *     num_heads.  Others: RQ_ERR_UNSUPPORTED.
