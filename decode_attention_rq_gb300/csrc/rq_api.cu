@@ -150,7 +150,7 @@ rq_status rq_append(rq_cache* cache, int32_t layer, int32_t group, int32_t batch
   if (n_tokens == 0) return RQ_OK;
   cudaError_t e = launch_append(*cache, layer, group, batch, static_cast<const __nv_bfloat16*>(kv),
                                 seq_lens, n_tokens, status, static_cast<cudaStream_t>(stream));
-  return e == cudaSuccess ? RQ_OK : RQ_ERR_CUDA;
+  return e == cudaSuccess ? RQ_OK : (e == cudaErrorNotSupported ? RQ_ERR_UNSUPPORTED : RQ_ERR_CUDA);
 }
 
 size_t rq_decode_workspace_bytes(const rq_config* cfg, int32_t batch) {

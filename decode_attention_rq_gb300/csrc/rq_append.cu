@@ -325,6 +325,7 @@ cudaError_t launch_append(const rq_cache& c, int layer, int group, int batch,
   // aligned 16-position blocks touched by n tokens starting anywhere: at most ceil(n/16) + 1;
   // a short append in shared mode takes one CTA per (K/V, residual loop)
   const bool split = !(c.geom.mode & RQ_MODE_CHAINED) && c.geom.P > 1 && n_tokens <= kTok;
+  if ((int64_t)batch * c.geom.H > 65535) return cudaErrorNotSupported;   // grid.y holds (row, head)
   dim3 grid((n_tokens + kTok - 1) / kTok + 1, batch * c.geom.H, split ? 2 * (c.geom.P - 1) : 2);
   if (c.geom.d == 128) return launch_dependent(append_kernel<128>, grid, dim3(kThreads), 0, stream, a);
   if (c.geom.d == 96) return launch_dependent(append_kernel<96>, grid, dim3(kThreads), 0, stream, a);

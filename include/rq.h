@@ -190,7 +190,7 @@ rq_status rq_cache_destroy(rq_cache* cache);
  *   status    device int32[4] or NULL; see the status word under
  *             rq_decode_workspace_bytes (the workspace's first 16 bytes serve).
  * Errors: INVALID_ARG, CAPACITY (batch > max_batch or n_tokens > max_seq_len),
- * ALIGNMENT, CUDA. */
+ * ALIGNMENT, UNSUPPORTED (batch * num_heads > 65535), CUDA. */
 rq_status rq_append(rq_cache* cache, int32_t layer, int32_t group, int32_t batch,
                     const void* kv, const int32_t* seq_lens, int32_t n_tokens,
                     int32_t* status, void* stream);
