@@ -180,21 +180,22 @@ def test_decode_attention_append_writes_the_next_slot(chained):
     attention over the cache as it was; the token of every loop then reads back
     from slot seq_lens[b] within its quantization error (a wrong slot reads
     zeros, a wrong plane another loop); earlier slots and the next slot keep
-    their bytes; a row at capacity is attended but left untouched."""
-    d, g, H, B, P, cap = 64, 32, 2, 3, 4, 128
+    their bytes; a row with one free slot fills it; a row at capacity is
+    attended but left untouched."""
+    d, g, H, B, P, cap = 64, 32, 2, 4, 4, 128
     geom = Lo.Geometry(1, P, 1, H, d, g, B, cap)
     R = synth.rotation(d).astype(np.float32).astype(np.float64)
     w = synth.Workload("t", 1, P, 1, H, d, g, B, cap, synth.OURO_ALPHAS, True)
     _, kv = synth.looped_kv(5, w, batch=B, ntok=100)
     buf = np.zeros(geom.total_bytes, dtype=np.uint8)
-    oracle.append(buf, geom, R, 0, 0, kv, [0, 0, 28], chained)     # row 2 filled up to capacity
+    oracle.append(buf, geom, R, 0, 0, kv, [0, 0, 28, 27], chained)  # row 2 full, row 3 one slot short
     before = buf.copy()
     _, cur = synth.looped_kv(6, w, batch=B, ntok=1)
     kv_cur = cur[..., 0, :]                                          # [P, 2, B, H, d]
     q = np.random.default_rng(8).standard_normal((B, H, d))
-    seq = np.array([100, 37, cap])
+    seq = np.array([100, 37, cap, cap - 1])
     out, ok = oracle.decode_attention_append(buf, geom, R, 0, 0, q, kv_cur, seq, 0.125, chained=chained)
-    assert ok.tolist() == [True, True, False]
+    assert ok.tolist() == [True, True, False, True]
     ref = oracle.decode_attention(before, geom, R, 0, 0, P - 1, q, kv_cur[P - 1, 0], kv_cur[P - 1, 1], seq, 0.125,
                                   chained=chained)
     assert np.array_equal(out, ref)
@@ -203,15 +204,17 @@ def test_decode_attention_append_writes_the_next_slot(chained):
     # what compressing the token alone gives (its reconstruction per loop)
     recon = M.compress_group(kv_cur[..., None, :], R, g, chained=chained)["recon"][..., 0, :]
     worst = {}
-    for b in (0, 1):
+    for b in (0, 1, 3):
         n = int(seq[b])
+        m = min(n + 2, cap)
         for h in range(H):
             for loop in range(P):
-                K0, V0 = oracle.reconstruct(before, geom, R, 0, 0, b, h, loop, n + 2, chained)
-                K1, V1 = oracle.reconstruct(buf, geom, R, 0, 0, b, h, loop, n + 2, chained)
+                K0, V0 = oracle.reconstruct(before, geom, R, 0, 0, b, h, loop, m, chained)
+                K1, V1 = oracle.reconstruct(buf, geom, R, 0, 0, b, h, loop, m, chained)
                 for kvi, (X0, X1) in enumerate(((K0, K1), (V0, V1))):
                     assert np.array_equal(X1[:n], X0[:n])                 # earlier slots unchanged
-                    assert np.array_equal(X1[n + 1], X0[n + 1])          # the next slot too
+                    if n + 1 < cap:
+                        assert np.array_equal(X1[n + 1], X0[n + 1])      # the next slot too
                     assert np.array_equal(X1[n], recon[loop, kvi, b, h])    # this slot, this plane
                     x = kv_cur[loop, kvi, b, h]
                     rel = np.linalg.norm(X1[n] - x) / np.linalg.norm(x)

@@ -51,8 +51,14 @@ def test_quantizer_codes_are_exact_nearest_grid_points(bits):
     qmax = (1 << bits) - 1
     for trial in range(150):
         v = rng.standard_normal((4, g)).astype(np.float32).astype(np.float64)
-        if trial % 5 == 0:   # put some values exactly on grid midpoints
+        if trial % 5 == 0:   # put some values on a coarse grid
             v[1] = np.round(v[1] * 4) / 4
+        # a group whose scale and offset are E4M3-exact and whose inner values sit
+        # exactly halfway between grid points: the code must be the even neighbour
+        s_t = [0.25, 0.125, 0.5, 0.0625][trial % 4]
+        o_t = [0.0, -1.0, 0.5, -2.0][(trial // 4) % 4]
+        k_t = rng.integers(0, qmax, size=g - 2)
+        v[2] = np.concatenate([[o_t, o_t + qmax * s_t], o_t + (k_t + 0.5) * s_t])
         codes, s_b, o_b = M.quantize(v, bits, g)
         s = F.e4m3_decode(s_b)[:, 0]
         o = F.e4m3_decode(o_b)[:, 0]
@@ -278,6 +284,19 @@ def test_fma_f32_is_one_rounding_of_the_exact_value():
         if rem > Fraction(1, 2) or (rem == Fraction(1, 2) and fl % 2 == 1):
             fl += 1
         return sgn * float(fl * q)
+
+    # one rounding, not two: the exact a*b is halfway between two binary32 values
+    # and c is far below float64's precision there, so rounding a*b + c to float64
+    # first would land on the tie and send it to the even neighbour; the single
+    # rounding goes the way c points.  Both directions (even neighbour below, above).
+    tiny = float.fromhex("0x1p-80")
+    for a, b, c in [(1 + 2.0 ** -12, 1 + 2.0 ** -12, tiny), (1 + 2.0 ** -12, 1 + 3 * 2.0 ** -12, -tiny),
+                    (-(1 + 2.0 ** -12), 1 + 2.0 ** -12, -tiny)]:
+        a32, b32, c32 = np.float32(a), np.float32(b), np.float32(c)
+        assert float(a32) == a and float(b32) == b and float(c32) == c
+        want = rne32(Fraction(a) * Fraction(b) + Fraction(c))
+        assert float(F.fma_f32(a32, b32, c32)) == want
+        assert want != float(np.float32(np.float64(a) * np.float64(b) + np.float64(c)))   # the trap is real
 
     rng = np.random.default_rng(21)
     for i in range(6000):
