@@ -81,6 +81,16 @@ CASES = [
     ("f32-residual-sign", method.compress_group,
      [("e = fma_f32(-cb, ref, x[j])", "e = fma_f32(cb, ref, x[j])")],
      [lambda: TM.test_f32_and_f64_readings_agree_up_to_rounding(False)]),
+    ("chained-encoder-drops-c", method.compress_group,
+     [("enc_ref = fma_f32(cb, enc_ref, back).astype(np.float64)", "enc_ref = back.astype(np.float64)")],
+     [lambda: TM.test_f32_and_f64_readings_agree_up_to_rounding(True)]),
+    ("norm-ratio-in-least-squares-mode", method.compress_group,
+     [('c = ls_coefficient(x[j], ref) if scaling == "ls" else norm_ratio_coefficient(x[j], ref)',
+       'c = norm_ratio_coefficient(x[j], ref) if scaling == "ls" else ls_coefficient(x[j], ref)')],
+     [TM.test_residual_uses_bf16_coefficient_and_dequantized_anchor]),
+    ("f32-rotate-back-transposed", method.rotate_back_f32,
+     [("acc = fma_f32(R[k, :], r[..., k:k + 1], acc)", "acc = fma_f32(R[:, k], r[..., k:k + 1], acc)")],
+     [TM.test_f32_rotation_special_cases_and_error_bound]),
     ("f32-rotation-transposed", method.rotate_f32,
      [("u = fma_f32(R[:, k], e[..., k:k + 1], u)", "u = fma_f32(R[k, :], e[..., k:k + 1], u)")],
      [TM.test_f32_rotation_special_cases_and_error_bound]),
@@ -123,6 +133,14 @@ CASES = [
      [("byte_in_row = 4 * word + (q % 4)", "byte_in_row = 4 * word + q // per_byte"),
       ("slot = q // 4", "slot = q % per_byte")],
      [lambda: TL.test_channel_major_masks_give_consecutive_tokens(4)]),
+    ("writer-swaps-scale-and-offset", layout.pack_group,
+     [("buf[ma] = a_s[kv, b, h]\n                buf[ma + 1] = a_o[kv, b, h]",
+       "buf[ma] = a_o[kv, b, h]\n                buf[ma + 1] = a_s[kv, b, h]")],
+     [lambda: TL.test_decode_attention_append_writes_the_next_slot(False)]),
+    ("writer-c-big-endian", layout.pack_group,
+     [("buf[ca] = (cb & 0xFF).astype(np.uint8)\n                    buf[ca + 1] = (cb >> 8).astype(np.uint8)",
+       "buf[ca] = (cb >> 8).astype(np.uint8)\n                    buf[ca + 1] = (cb & 0xFF).astype(np.uint8)")],
+     [lambda: TL.test_decode_attention_append_writes_the_next_slot(False)]),
     ("storage-drops-coefficient", layout.bits_per_element,
      [("resid = 8.0 * (head_dim / 4 + 2 * ng + 2) / head_dim", "resid = 8.0 * (head_dim / 4 + 2 * ng) / head_dim")],
      [TL.test_storage_accounting_reproduces_the_pages]),
@@ -134,6 +152,12 @@ CASES = [
     ("rounding-ties-up", formats._round_to_format,
      [("k = np.rint(ax / quantum)", "k = np.floor(ax / quantum + 0.5)")],
      [TF.test_e4m3_midpoints_brute_force, TF.test_bf16_matches_torch_cast_from_fp32]),
+    ("e4m3-no-saturation", formats.e4m3_round,
+     [("np.clip(x, -E4M3_MAX, E4M3_MAX), _E4M3_MANT_BITS", "x, _E4M3_MANT_BITS"),
+      ("return np.clip(r, -E4M3_MAX, E4M3_MAX)", "return r")],
+     [lambda: TF.test_e4m3_fixed_points(500.0, 0x7E)]),
+    ("e4m3-negative-zero-loses-sign", formats.e4m3_encode, [("neg = np.signbit(x)", "neg = x < 0")],
+     [TF.test_e4m3_negative_underflow_keeps_sign]),
     ("e4m3-encode-bias", formats.e4m3_encode,
      [("norm_e = np.clip(e_unb + 7, 1, 15)", "norm_e = np.clip(e_unb + 8, 1, 15)")],
      [TF.test_e4m3_encode_matches_torch_cast_in_range]),
