@@ -83,23 +83,24 @@ def test_fused_call_equals_decode_then_append_and_the_oracle(d, g, P, chained, s
 
 
 def test_fused_call_empty_rows_and_capacity():
-    """An empty row gets its first token at slot 0; a row at capacity is attended
-    but not appended (status word [1] = 1, its bytes unchanged)."""
-    case = Case(L=1, P=4, G=1, H=2, d=128, g=32, B=3, Nmax=128, seed=61)
+    """An empty row gets its first token at slot 0; a row with one free slot fills
+    the last slot; a row at capacity is attended but not appended (status word
+    [1] = 1, its bytes unchanged)."""
+    case = Case(L=1, P=4, G=1, H=2, d=128, g=32, B=4, Nmax=128, seed=61)
     R32, R = rotation32(128)
     gpu = GpuCache(case, R32)
     geom = _geom(case)
     obuf = np.zeros(geom.total_bytes, dtype=np.uint8)
     kvb, kv = kv_for(case, 62, 100)
-    start = np.array([0, 0, 28], dtype=np.int64)     # row 2 fills the capacity
+    start = np.array([0, 0, 28, 27], dtype=np.int64)     # row 2 fills the capacity, row 3 all but one slot
     gpu.append(0, 0, kvb, start)
     oracle.append(obuf, geom, R, 0, 0, kv, start)
-    seq = np.array([0, 100, 128])
+    seq = np.array([0, 100, 128, 127])
     kvb_c, kv_c = kv_for(case, 63, 1)
-    qb, q = synth.queries(64, 3, 2, 128)
+    qb, q = synth.queries(64, 4, 2, 128)
     out = gpu.decode_append(0, 0, qb, kvb_c[..., 0, :], seq, 0.09).cpu().numpy()
     ref, ok = oracle.decode_attention_append(obuf, geom, R, 0, 0, q, kv_c[..., 0, :], seq, 0.09)
-    assert ok.tolist() == [True, True, False]
+    assert ok.tolist() == [True, True, False, True]
     assert np.abs(out - ref).max() <= ATOL
     assert np.array_equal(out[0], kv_c[3, 1, 0, :, 0].astype(np.float32))   # current token alone
     gbuf = gpu.bytes_host()
