@@ -5,7 +5,8 @@
     against the oracle;
   * the largest batch one decode call takes (RQ_MAX_DECODE_BATCH rows, ragged
     lengths including empty rows), plain and fused calls against the oracle;
-    one row more is refused with RQ_ERR_UNSUPPORTED before any launch.
+    one row more is refused with RQ_ERR_UNSUPPORTED before any launch;
+  * an append whose batch x heads passes its grid limit is refused the same way.
 """
 import math
 
@@ -97,3 +98,26 @@ def test_largest_decode_batch():
         gbig.decode(0, 0, 0, qb, kvb_b[0, 0, :MAX_BATCH + 1, :, 0], kvb_b[0, 1, :MAX_BATCH + 1, :, 0],
                     np.zeros(MAX_BATCH + 1), scale, batch=MAX_BATCH + 1)
     assert e.value.status == 6   # RQ_ERR_UNSUPPORTED
+
+
+def test_append_grid_limit_is_refused_before_any_launch():
+    """rq_append puts (row, head) pairs on a grid dimension of at most 65535: a
+    batch x heads above it returns RQ_ERR_UNSUPPORTED (nothing is launched, the
+    cache stays zero); one pair fewer is accepted."""
+    import torch
+    import decode_attention_rq_gb300 as rq
+    H, d, Nmax = 16, 128, 64
+    B = 65536 // H                                  # 4096 rows x 16 heads = 65536 pairs
+    case = Case(L=1, P=1, G=1, H=H, d=d, g=32, B=B, Nmax=Nmax, seed=3)
+    R32, _ = rotation32(d)
+    gpu = GpuCache(case, R32)
+    kv = torch.zeros((1, 2, B, H, 1, d), dtype=torch.bfloat16, device="cuda:0")
+    seq = torch.zeros(B, dtype=torch.int32, device="cuda:0")
+    with pytest.raises(rq.RqError) as e:
+        rq.rq_append(gpu.handle, 0, 0, B, kv, seq, 1, gpu.status)
+    assert e.value.status == 6   # RQ_ERR_UNSUPPORTED
+    torch.cuda.synchronize()
+    assert not gpu.buf.any()
+    rq.rq_append(gpu.handle, 0, 0, B - 1, kv[:, :, :B - 1].contiguous(), seq, 1, gpu.status)   # 65520 pairs: accepted
+    torch.cuda.synchronize()
+    assert gpu.status.tolist() == [0, 0, 0, 0]
