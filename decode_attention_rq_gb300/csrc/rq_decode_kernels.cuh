@@ -305,17 +305,25 @@ __global__ void __launch_bounds__(kThreads, (Cfg<D, GS, NRES>::MINB)) decode_ker
   const uint64_t pol = l2_evict_first_policy();   // the cache is read once per call
   // layout tiles of the producer's unit that hold tokens (the last unit of a row may have one)
   auto unit_tiles = [&]() { return min(C::UT, (sl_s[pc.b] - pc.t * C::UT * kTile + kTile - 1) / kTile); };
-  // paged layout: block-table entries of the next unit's tiles, loaded one unit
-  // ahead by the producer thread so that the copies never wait on them (kept in
-  // shared memory: the producer's state costs the other threads no registers)
+  // paged layout: block-table entries of the next unit's tiles, fetched one unit
+  // ahead by the producer thread with asynchronous copies, so that neither the
+  // copies nor the producer's own unit wait on them (kept in shared memory: the
+  // producer's state costs the other threads no registers)
   __shared__ int next_raw_s[C::UT];
   __shared__ int pu_s;   // unit the producer issues next
   auto fetch_pages = [&]() {
     const int nt = unit_tiles();
 #pragma unroll
-    for (int k = 0; k < C::UT; ++k) next_raw_s[k] = k < nt ? raw_page(a.g, pc.b, pc.t * C::UT + k) : 0;
+    for (int k = 0; k < C::UT; ++k) {
+      if (k < nt)
+        cp_async4(&next_raw_s[k], a.g.table + (size_t)pc.b * a.g.max_tiles + pc.t * C::UT + k);
+      else
+        next_raw_s[k] = 0;
+    }
+    cp_async_commit();
   };
   auto issue = [&](int stage) {
+    if constexpr (PAGED) cp_async_wait_all();   // this unit's entries (fetched an issue ago)
     const int t0 = pc.t * C::UT;
     const int ntile = unit_tiles();
     const int kvh = pc.h / a.g.qpk;
@@ -702,9 +710,11 @@ __global__ void __launch_bounds__(kThreads, (Cfg<D, GS, NRES>::MINB)) decode_ker
 
   if (aborted) {
     // let the copies still in flight land before the CTA exits (each wait bounded)
-    if (tid == 0)
+    if (tid == 0) {
       for (int v = fail_u; v < u1 && v < fail_u + STAGES; ++v)
         (void)mbar_wait_bounded(&full_bar[(v - u0) % STAGES], (uint32_t)(((v - u0) / STAGES) & 1));
+      if constexpr (PAGED) cp_async_wait_all();   // block-table entries fetched ahead
+    }
     __syncthreads();
     return;
   }
