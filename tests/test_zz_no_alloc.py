@@ -12,14 +12,16 @@ run every other test; it also passes when run on its own.
 """
 import math
 
+import numpy as np
 import pytest
 import torch
 
+import oracle
 from rq_harness import Case, GpuCache, kv_for, rotation32
 
 pytestmark = pytest.mark.gpu
 
-TOL = 1e-3   # the per-call bound the decode parity tests use for one kernel call
+ATOL = 2e-3   # against the oracle: the decode parity tests' bar
 
 
 def _inputs(case, seed):
@@ -32,10 +34,13 @@ def _inputs(case, seed):
 def test_noalloc_matches_workspace_call_twice_in_a_row():
     import decode_attention_rq_gb300 as rq
     case = Case(L=1, P=4, G=1, H=4, d=128, g=32, B=3, Nmax=768, seed=11)
-    R32, _ = rotation32(case.d)
+    R32, R = rotation32(case.d)
     gpu = GpuCache(case, R32)
-    kv, _ = kv_for(case, seed=case.seed, ntok=700)
-    gpu.append(0, 0, kv, [0] * case.B)
+    kvb, kv = kv_for(case, seed=case.seed, ntok=700)
+    gpu.append(0, 0, kvb, [0] * case.B)
+    geom = oracle.Geometry(case.L, case.P, case.G, case.H, case.d, case.g, case.B, case.Nmax)
+    obuf = np.zeros(geom.total_bytes, dtype=np.uint8)
+    oracle.append(obuf, geom, R, 0, 0, kv, np.zeros(case.B, dtype=np.int64))
     lens = [700, 129, 0]                       # several tiles, a ragged tail, an empty row
     sl = torch.tensor(lens, dtype=torch.int32, device="cuda")
     q, kc, vc = _inputs(case, 5)
@@ -43,13 +48,17 @@ def test_noalloc_matches_workspace_call_twice_in_a_row():
     status = torch.full((4,), -1, dtype=torch.int32, device="cuda")
     for loop in (1, 3):                        # a residual loop and the anchor loop
         ref = gpu.decode(0, 0, loop, q, kc, vc, lens, scale)
+        exact = oracle.decode_attention(obuf, geom, R, 0, 0, loop, q.double().cpu().numpy(),
+                                        kc.double().cpu().numpy(), vc.double().cpu().numpy(), lens, scale)
         for call in range(2):
             out = torch.full((case.B, case.H, case.d), float("nan"), device="cuda")
             rq.rq_decode_attention_noalloc(gpu.handle, 0, 0, loop, case.B, q, kc, vc, sl, scale, out,
                                            status)
             torch.cuda.synchronize()
-            err = (out - ref).abs().max().item()
-            assert err <= TOL, (loop, call, err)
+            # the same kernels on the same inputs: the same bits as the workspace call
+            assert torch.equal(out, ref), (loop, call, (out - ref).abs().max().item())
+            err = float(np.abs(out.cpu().numpy() - exact).max())
+            assert err <= ATOL, (loop, call, err)
             assert status.tolist() == [0, 0, 0, 0], (loop, call, status.tolist())
     gpu.close()
 
