@@ -9,8 +9,8 @@
 //
 // GB300 design
 //   * Three kernels per call.  qprep_kernel (one CTA per (row, head)) applies
-//     R to the query and turns q and R q into the fixed-point packs the
-//     scoring uses.  decode_kernel streams the cache and writes one partial
+//     R to the query and turns q and R q into the f16 operand images the
+//     scoring products use.  decode_kernel streams the cache and writes one partial
 //     softmax state per (CTA, segment).  merge_kernel (one CTA per (row,
 //     head)) combines the partials, adds the current BF16 token, applies R^T
 //     once and writes the output.  decode_kernel and merge_kernel are
@@ -32,14 +32,21 @@
 //   * Per group, q.x_hat = s * sum(q * code) + o * sum(q), and the value side
 //     keeps the offsets as one scalar per (unit, group): the work per code is
 //     one multiply-add against a small integer.
-//   * That multiply-add runs on the integer dot-product unit: the query (per
-//     group) and the softmax-times-scale weights (per unit and group) are
-//     taken to 16-bit fixed point as two int8 parts; dp4a sums 4 code x part
-//     products exactly.  Byte masks put the codes straight into dp4a operands:
-//     K rows are token-major (4 codes of one token per operand), V rows are
-//     channel-major (4 consecutive tokens of one channel per operand), so no
-//     shifts are needed.  The masks and the dot products run on separate
-//     pipes of the SM and overlap.
+//   * Those multiply-adds are f16 tensor-core products (mma.sync m16n8k16,
+//     f32 accumulation).  A code word masked with 0x000F000F, 0x00F000F0 or
+//     0x00030003 << 2m (after a shift by 8 for the other two bytes) is an f16
+//     pair whose bit patterns are small integers: values code * 2^-24 (times
+//     16 or 4^m), exact, with no conversion and no bias.  Scoring: tokens x
+//     channels against the query (q, and R q for the residual planes) split
+//     into two f16 pieces (about 22 bits) in the B operand, one column pair
+//     per channel group, so each lane's accumulator holds one group's dot
+//     products.  Values: channels x tokens against the softmax-times-scale
+//     weights of the unit, again two f16 pieces per weight, so every weight
+//     keeps its own relative precision (no fixed point relative to the
+//     unit's largest weight: a softmax that one key dominates loses nothing).
+//     The 16 / 4^m factors of the masked codes are divided out of the B
+//     operands.  The tokens of a lane's two score rows (t, t + 2) are the
+//     pair one B register of the value products holds.
 //   * Online softmax in base 2 (scale * log2(e) folded into q).
 //   * Variants: grouped-query attention runs the units, the prep and the merge
 //     over (row, query head), each query head reading its KV head's tiles;
@@ -84,7 +91,7 @@ static size_t partials_bytes(const Geom& g, int batch, int num_sms) {
 
 size_t decode_workspace_bytes(const Geom& g, int batch, int num_sms) {
   const size_t bh = (size_t)batch * g.Hq;
-  return 256 + partials_bytes(g, batch, num_sms) + bh * g.ng * kPackWords * sizeof(uint32_t);
+  return 256 + partials_bytes(g, batch, num_sms) + bh * kPackWords * sizeof(uint32_t);
 }
 
 cudaError_t launch_decode(const rq_cache& c, int layer, int group, int loop, int batch,

@@ -25,7 +25,7 @@ struct DecodeArgs {
   int32_t* status;
   const __nv_bfloat16* kv_all;   // [P][2][batch][H][d]: the anchor-loop call also appends it; else NULL
   float* partials;       // [(C + batch*H)][pstride]: (m, l, acc_anchor[d], acc_residual[d])
-  uint32_t* packs;       // [batch*H][NG][kPackWords]
+  uint32_t* packs;       // [batch*H][kPackWords]: query operands of the scoring products
   int pstride;
   int layer, group, batch, res0;   // res0: first residual plane this loop reads
   float qscale;                    // softmax_scale * log2(e)
@@ -34,6 +34,12 @@ struct DecodeArgs {
 // Chained calls that read 4 to 7 residual planes (rq_decode_chained.cu).
 cudaError_t launch_decode_long_chain(const DecodeArgs& a, int num_sms, int nres, cudaStream_t stream);
 
+// Query operands per (row, query head): a header (two scales, the per-group sums
+// of the query and of the rotated query) then the f16 B-operand images of the
+// scoring products, 8 lanes x (anchor + residual) registers.
+constexpr int kPackHeader = 32;
+constexpr int kPackWords = kPackHeader + 8 * 32;
+
 namespace {
 
 constexpr int kThreads = 256;
@@ -41,35 +47,79 @@ constexpr int kMaxCtasPerSm = 3;     // the workspace holds partials for this ma
 constexpr int kMaxRows = RQ_MAX_DECODE_BATCH;   // batch rows one call may cover
 constexpr int kMaxRes = 7;             // residual planes one call may read (chained, 8 loops)
 constexpr float kLog2e = 1.4426950408889634f;
-constexpr float kFix = 32767.f;        // 16-bit fixed point: values in [-32767, 32767]
-constexpr int kPackWords = 36;         // query pack per (row, head, group): anchor 16, residual 16, 4 scalars
 constexpr int kPrepThreads = 256;
 constexpr int kMergeThreads = 256;
 constexpr int kMaxContrib = 512;       // decode CTAs one merge can combine (the grid is smaller)
+// Value-weight image of one (plane, group): per value product m (8) and lane t
+// (4) the B registers b0, b1 (8 B), hi pieces at +0 and lo pieces at +kWPiece.
+// The strides put the pieces 8 banks apart and neighbouring images 2 banks
+// apart, so the lanes' stores and loads do not collide in shared memory.
+constexpr int kWPiece = 288;
+constexpr int kWItem = 648;
 
-
-__device__ __forceinline__ int dp4a_us(uint32_t a_u8, uint32_t b_s8, int c) {
-  int d;
-  asm("dp4a.u32.s32 %0, %1, %2, %3;" : "=r"(d) : "r"(a_u8), "r"(b_s8), "r"(c));
-  return d;
-}
-__device__ __forceinline__ int dp4a_uu(uint32_t a_u8, uint32_t b_u8, int c) {
-  int d;
-  asm("dp4a.u32.u32 %0, %1, %2, %3;" : "=r"(d) : "r"(a_u8), "r"(b_u8), "r"(c));
-  return d;
-}
-__device__ __forceinline__ int shl(int x, int s) { return (int)((uint32_t)x << s); }
-// 16-bit fixed point value x = 256*hi + lo, hi in [-128, 127] (int8), lo in [0, 255]
-__device__ __forceinline__ uint32_t fix_hi(int x) { return (uint32_t)(x >> 8) & 0xFFu; }
-__device__ __forceinline__ uint32_t fix_lo(int x) { return (uint32_t)x & 0xFFu; }
-__device__ __forceinline__ int to_fix(float x, float inv) {
-  int v = __float2int_rn(x * inv);
-  return max(-32767, min(32767, v));
-}
 __device__ __forceinline__ float2 meta2(const uint8_t* p) {   // (scale, offset)
   return e4m3x2_to_f32x2(*reinterpret_cast<const uint16_t*>(p));
 }
 __device__ __forceinline__ int clamp_len(int n, int nmax) { return n < 0 ? 0 : (n > nmax ? nmax : n); }
+
+// ---- f16 tensor-core products ------------------------------------------------
+// d += a b for one 16 x 8 x 16 tile: A 16 x 16 row-major f16, B 16 x 8 f16, D f32.
+// Fragments (lane = 4 g + t): a0 (row g, k 2t, 2t+1), a1 (row g+8, same k),
+// a2 (row g, k 2t+8, 2t+9), a3 (row g+8, those k); b0 (k 2t, 2t+1; col g),
+// b1 (k 2t+8, 2t+9; col g); d0 (row g, col 2t), d1 (row g, col 2t+1), d2, d3
+// (row g+8, cols 2t, 2t+1).
+__device__ __forceinline__ void mma16816(float (&d)[4], uint32_t a0, uint32_t a1, uint32_t a2, uint32_t a3,
+                                         uint32_t b0, uint32_t b1) {
+  asm("mma.sync.aligned.m16n8k16.row.col.f32.f16.f16.f32 {%0,%1,%2,%3}, {%4,%5,%6,%7}, {%8,%9}, {%0,%1,%2,%3};"
+      : "+f"(d[0]), "+f"(d[1]), "+f"(d[2]), "+f"(d[3])
+      : "r"(a0), "r"(a1), "r"(a2), "r"(a3), "r"(b0), "r"(b1));
+}
+// Codes as f16 operands.  An f16 whose bit pattern is an integer n < 2048 has the
+// value n * 2^-24 (subnormals, then the first normal binade, share the step
+// 2^-24), so masking a code word leaves exact f16 multiples of the codes: no
+// conversion and no bias.  The tensor core keeps such operands exactly.
+//
+// INT4 word (byte i = element 2i in bits 0-3, element 2i+1 in bits 4-7): four
+// f16x2 registers, r[k] half h = element k + 4h; odd k carry 16 x the code.
+__device__ __forceinline__ void int4_f16(uint32_t w, uint32_t (&r)[4]) {
+  const uint32_t w8 = w >> 8;
+  r[0] = w & 0x000F000Fu;
+  r[1] = w & 0x00F000F0u;
+  r[2] = w8 & 0x000F000Fu;
+  r[3] = w8 & 0x00F000F0u;
+}
+// INT2 word (byte i, bits 2m..2m+1 = element 4i + m): eight f16x2 registers,
+// r[2m + hb] half h = element 4 (hb + 2h) + m, carrying 4^m x the code.
+__device__ __forceinline__ void int2_f16(uint32_t w, uint32_t (&r)[8]) {
+  const uint32_t w8 = w >> 8;
+#pragma unroll
+  for (int m = 0; m < 4; ++m) {
+    r[2 * m] = w & (0x00030003u << (2 * m));
+    r[2 * m + 1] = w8 & (0x00030003u << (2 * m));
+  }
+}
+__device__ __forceinline__ uint32_t pack_f16x2(__half lo, __half hi) {
+  return (uint32_t)__half_as_ushort(lo) | ((uint32_t)__half_as_ushort(hi) << 16);
+}
+// x as two f16 pieces hi + lo (about 22 significant bits; magnitudes past the
+// f16 range clamp to +-65504)
+__device__ __forceinline__ void f16_pieces(float x, __half& hi, __half& lo) {
+  x = fminf(fmaxf(x, -65504.f), 65504.f);
+  hi = __float2half_rn(x);
+  lo = __float2half_rn(x - __half2float(hi));
+}
+// (x0, x1) rounded to f16, saturating at +-65504: x0 in the low half
+__device__ __forceinline__ uint32_t f16x2_sat(float x0, float x1) {
+  uint32_t r;
+  asm("cvt.rn.satfinite.f16x2.f32 %0, %1, %2;" : "=r"(r) : "f"(x1), "f"(x0));
+  return r;
+}
+// f16x2 pieces of (x0, x1): hi = the rounded pair, lo = the rounded remainders
+__device__ __forceinline__ void f16x2_pieces(float x0, float x1, uint32_t& hi, uint32_t& lo) {
+  hi = f16x2_sat(x0, x1);
+  const float2 h = __half22float2(*reinterpret_cast<const __half2*>(&hi));
+  lo = f16x2_sat(x0 - h.x, x1 - h.y);
+}
 
 // Balanced split of U units over C CTAs: CTA c takes [start(c), start(c+1)) with
 // start(c) = c*q + min(c, rem), q = U / C, rem = U % C (32-bit arithmetic only).
@@ -86,7 +136,6 @@ struct Split {
 template <int D, int GS, int NRES>
 struct Cfg {
   static constexpr int NG = D / GS;
-  static constexpr int NGP = NG <= 2 ? 2 : (NG <= 4 ? 4 : 8);   // groups padded to a power of two
   static constexpr int A_CODES = kTile * D / 2;
   static constexpr int R_CODES = kTile * D / 4;
   static constexpr int META = kTile * NG * 2;
@@ -96,34 +145,109 @@ struct Cfg {
   static constexpr int UT = 2;                                    // layout tiles per work unit
   static constexpr int UTOK = UT * kTile;                         // tokens per work unit
   static constexpr int STAGE = UT * SUB;
-  static constexpr int STAGES = 2;
-  // CTAs per SM: three (24 warps) while the registers allow it; the chained
-  // variants with more residual planes keep two, or one from four planes up
-  // (their two stages alone take most of the shared memory)
+  // CTAs per SM: two while the registers allow; one from four residual planes up
   static constexpr int MINB = NRES <= 1 ? 3 : (NRES <= 3 ? 2 : 1);
-  static constexpr int PPT = UTOK * NGP / kThreads;               // (token, group) pairs per thread
-  static constexpr int AW = GS / 8;              // 32-bit words of INT4 codes per (token, group)
-  static constexpr int RW = GS / 16;             // 32-bit words of INT2 codes per (token, group)
-  static constexpr int NITEM = NG * (1 + NRES);  // (kind, group) value-weight items per unit
-  static constexpr int WQ = 2 * UTOK + 16;       // weight bytes per item: hi by token, lo by token, pad
-  static constexpr int SMEM = STAGES * STAGE;
+  static constexpr int NITEM = NG * (1 + NRES);  // (plane, group) value-weight images
+  static constexpr int WIMG = NITEM * kWItem + 256;              // + a zero block for idle lanes
+  static constexpr int STAGES = (MINB * (3 * STAGE + WIMG) + MINB * 8192 <= 224 * 1024) ? 3 : 2;
+  static constexpr int SMEM = STAGES * STAGE + WIMG;
+  // ---- scoring products (tokens x channels), per warp 16 tokens ----
+  // anchor K: lane t holds words [t WA, (t+1) WA) of a token row (8 channels each);
+  // product j takes registers 2j, 2j+1 of the lane (word j/2)
+  static constexpr int WA = D / 32;
+  static constexpr int NMA = 2 * WA;
+  // residual K: lanes t < TR hold words 2t, 2t+1 (16 channels each); product j
+  // takes registers 2j, 2j+1 (word j/4)
+  static constexpr int TR = D / 32;
+  static constexpr int NMR = 8;
+  static constexpr int NIMG = 2 * NMA + (NRES > 0 ? 2 * NMR : 0);   // B-operand registers per lane
+  static_assert(kPackHeader + 8 * NIMG <= kPackWords, "query pack");
+  // channel group of the anchor / residual product j for lane t
+  static constexpr int ga(int t, int j) { return (t * WA + j / 2) * 8 / GS; }
+  static constexpr int gr(int t, int j) { return (2 * t + j / 4) * 16 / GS; }
+  // Products whose lanes all see the same groups share an accumulator: each
+  // lane's channels land in its own column pair, so an accumulator holds, per
+  // lane, the partial dot product of one group.  own: bit 4 a + t set when
+  // (accumulator a, lane t) is the first to hold its group (it adds the group's
+  // offset term).
+  struct AccMap {
+    int acc[8];   // accumulator of product j
+    int rep[8];   // a product of accumulator a
+    int n;        // accumulators
+    unsigned own;
+  };
+  static constexpr AccMap make_map(bool res) {
+    AccMap m{};
+    const int nj = res ? NMR : NMA, nt = res ? TR : 4;
+    for (int j = 0; j < nj; ++j) {
+      int found = -1;
+      for (int a = 0; a < m.n && found < 0; ++a) {
+        bool same = true;
+        for (int t = 0; t < nt; ++t)
+          if ((res ? gr(t, j) : ga(t, j)) != (res ? gr(t, m.rep[a]) : ga(t, m.rep[a]))) same = false;
+        if (same) found = a;
+      }
+      if (found < 0) {
+        found = m.n;
+        m.rep[m.n++] = j;
+      }
+      m.acc[j] = found;
+    }
+    for (int a = 0; a < m.n; ++a)
+      for (int t = 0; t < nt; ++t) {
+        const int g = res ? gr(t, m.rep[a]) : ga(t, m.rep[a]);
+        bool first = true;
+        for (int a2 = 0; a2 <= a; ++a2)
+          for (int t2 = 0; t2 < nt; ++t2) {
+            if (a2 == a && t2 >= t) continue;
+            if ((res ? gr(t2, m.rep[a2]) : ga(t2, m.rep[a2])) == g) first = false;
+          }
+        if (first) m.own |= 1u << (4 * a + t);
+      }
+    return m;
+  }
+  static constexpr int NACA = make_map(false).n;
+  static constexpr int NACR = make_map(true).n;
+  // ---- value products (channels x tokens), per warp 16 channels ----
+  static constexpr int VW = D / 16;   // warps with a 16-channel tile
+  static constexpr int NGW = (NG + 3) / 4;   // weight groups per lane: t, t + 4
 };
 
-// Query packs of one (row, head): for each group, the 16-bit fixed-point query
-// as int8 (hi, lo) parts laid out as the dp4a operands of the scoring, their
-// scales and sums.  Words of pack (bh, group):
-//   [4w + k], w < GS/8        anchor word w: k = 0 even-channel hi, 1 even lo,
-//                             2 odd hi, 3 odd lo (channels 8w + 2i (+1), i = byte)
-//   [16 + 8w + 2m + p]        residual word w, 2-bit field m: p = 0 hi, 1 lo
-//                             (channels 16w + 4i + m, i = byte)
-//   [32..35]                  sig_a, sum(q), sig_r, sum(R q) of the group (float bits)
+// Byte offset of token t's slot in a value-weight image (within a piece), and
+// the power of two the weight is scaled by so that it cancels the code's own
+// factor (16 for the high nibbles of INT4 words, 4^m for field m of INT2 words).
+// In both layouts an f16x2 operand holds tokens t and t + 2 (t mod 4 < 2): the
+// pair shares one 4-byte slot, low half first, and one factor.
+__device__ __forceinline__ void int4_slot(int tok, int& off, float& sc) {
+  const int tau = tok >> 6, tp = tok & 63, w = tp >> 3, i = tp & 7;
+  const int lane = w >> 1, e = w & 1;
+  const int k = 2 * (i & 1) + ((i >> 2) & 1), h = (i >> 1) & 1;
+  const int rho = 4 * (2 * tau + e) + k;
+  off = ((rho >> 1) * 4 + lane) * 8 + (rho & 1) * 4 + h * 2;
+  sc = (k & 1) ? 0.0625f : 1.f;
+}
+__device__ __forceinline__ void int2_slot(int tok, int& off, float& sc) {
+  const int tau = tok >> 6, tp = tok & 63, lane = tp >> 4, q = tp & 15;
+  const int m = q >> 2, i = q & 3, hb = i & 1, h = i >> 1;
+  const int rho = 8 * tau + 2 * m + hb;
+  off = ((rho >> 1) * 4 + lane) * 8 + (rho & 1) * 4 + h * 2;
+  sc = m == 0 ? 1.f : (m == 1 ? 0.25f : (m == 2 ? 0.0625f : 0.015625f));
+}
+
+// Query prep: one CTA per (row, query head).  Applies R to the query and writes
+// the B operands of the scoring products: for q (anchor plane) and R q (residual
+// planes), a power-of-two scale 2^k bringing max |x| into [2^14, 2^15), each
+// channel as two f16 pieces of x 2^k (divided by the code factor of its slot),
+// placed in the register order of the lane that holds the matching codes.
 template <int D, int GS, int NRES>
 __global__ void __launch_bounds__(kPrepThreads) qprep_kernel(DecodeArgs a) {
-  constexpr int NG = D / GS;
+  using C = Cfg<D, GS, NRES>;
+  constexpr int NG = C::NG, NMA = C::NMA, NIMG = C::NIMG;
   constexpr int RPW = 16;                  // rows of R per warp (D / 8 <= 16; the rest padded)
   __shared__ __align__(16) float q_s[D];
   __shared__ float qr_s[D];
-  __shared__ __align__(16) uint32_t img_s[NG * kPackWords];   // the packs of this (row, head)
+  __shared__ float red_s[2][kPrepThreads / 32];
+  __shared__ __align__(16) uint32_t pack_s[kPackWords];
   const int bh = blockIdx.x, tid = threadIdx.x;
   // R first (R stays unchanged while the cache is used), before waiting for the
   // kernel ahead of this one.  Warp w holds rows w, w+8, ...; lane l columns
@@ -151,7 +275,7 @@ __global__ void __launch_bounds__(kPrepThreads) qprep_kernel(DecodeArgs a) {
   pdl_launch_dependents();
   pdl_wait();
   if (tid < D) q_s[tid] = __bfloat162float(a.q[(size_t)bh * D + tid]) * a.qscale;
-  for (int i = tid; i < NG * kPackWords; i += kPrepThreads) img_s[i] = 0u;
+  if (tid < kPackHeader) pack_s[tid] = 0u;
   __syncthreads();
   if (NRES > 0 && hadamard) {   // R q = H q / sqrt(128); qr_s serves as the butterflies' scratch
     float v[1] = {tid < D ? q_s[tid] : 0.f};
@@ -181,77 +305,95 @@ __global__ void __launch_bounds__(kPrepThreads) qprep_kernel(DecodeArgs a) {
     if ((lane & 1) == 0 && row < D) qr_s[row] = pv[0];
     __syncthreads();
   }
-  // Each pack byte is written by the thread of its channel: thread k < D holds
-  // channel k of q and of R q.  A group's GS channels sit in GS consecutive lanes
-  // of one warp, so group maxima and sums are lane reductions.
-  uint8_t* img = reinterpret_cast<uint8_t*>(img_s);
-  if (tid < D) {
-    const int k = tid, gi = k / GS, j = k % GS;
-    const float x = q_s[k];
-    float mx = fabsf(x), s1 = x;
+  // max |x| of each plane, and the per-group sums of x (header)
+  {
+    const float x0 = tid < D ? q_s[tid] : 0.f;
+    const float x1 = (NRES > 0 && tid < D) ? qr_s[tid] : 0.f;
+    float m0 = fabsf(x0), m1 = fabsf(x1), s0 = x0, s1 = x1;
 #pragma unroll
-    for (int off = GS / 2; off > 0; off >>= 1) {
-      mx = fmaxf(mx, __shfl_xor_sync(0xffffffffu, mx, off));
+    for (int off = GS / 2; off > 0; off >>= 1) {   // group sums: GS consecutive lanes
+      s0 += __shfl_xor_sync(0xffffffffu, s0, off);
       s1 += __shfl_xor_sync(0xffffffffu, s1, off);
     }
-    const int v = to_fix(x, mx > 0.f ? kFix / mx : 0.f);
-    const int w = j >> 3, i = (j & 7) >> 1, odd = j & 1;
-    uint8_t* wb = img + 4 * (gi * kPackWords + 4 * w + 2 * odd) + i;
-    wb[0] = (uint8_t)fix_hi(v);
-    wb[4] = (uint8_t)fix_lo(v);
-    if (j == 0) {
-      img_s[gi * kPackWords + 32] = __float_as_uint(mx / (kFix * 16.f));   // anchor sums carry 16
-      img_s[gi * kPackWords + 33] = __float_as_uint(s1);
+    if (tid < D && tid % GS == 0) {
+      pack_s[4 + tid / GS] = __float_as_uint(s0);
+      pack_s[4 + NG + tid / GS] = __float_as_uint(s1);
     }
-  }
-  if (NRES > 0 && tid < D) {
-    const int k = tid, gi = k / GS, j = k % GS;
-    const float x = qr_s[k];
-    float mr = fabsf(x), s2 = x;
 #pragma unroll
-    for (int off = GS / 2; off > 0; off >>= 1) {
-      mr = fmaxf(mr, __shfl_xor_sync(0xffffffffu, mr, off));
-      s2 += __shfl_xor_sync(0xffffffffu, s2, off);
+    for (int off = 16; off > 0; off >>= 1) {
+      m0 = fmaxf(m0, __shfl_xor_sync(0xffffffffu, m0, off));
+      m1 = fmaxf(m1, __shfl_xor_sync(0xffffffffu, m1, off));
     }
-    const int v = to_fix(x, mr > 0.f ? kFix / mr : 0.f);
-    const int w = j >> 4, i = (j & 15) >> 2, m = j & 3;
-    uint8_t* wb = img + 4 * (gi * kPackWords + 16 + 8 * w + 2 * m) + i;
-    wb[0] = (uint8_t)fix_hi(v);
-    wb[4] = (uint8_t)fix_lo(v);
-    if (j == 0) {
-      img_s[gi * kPackWords + 34] = __float_as_uint(mr / (kFix * 64.f));   // residual sums carry 64
-      img_s[gi * kPackWords + 35] = __float_as_uint(s2);
-    }
+    if (lane == 0) { red_s[0][warp] = m0; red_s[1][warp] = m1; }
   }
   __syncthreads();
-  uint4* dst = reinterpret_cast<uint4*>(a.packs + (size_t)bh * NG * kPackWords);
-  const uint4* src = reinterpret_cast<const uint4*>(img_s);
-  for (int i = tid; i < NG * kPackWords / 4; i += kPrepThreads) dst[i] = src[i];
+  float scl[2];   // 2^k per plane
+#pragma unroll
+  for (int p = 0; p < 2; ++p) {
+    float mx = 0.f;
+#pragma unroll
+    for (int w = 0; w < kPrepThreads / 32; ++w) mx = fmaxf(mx, red_s[p][w]);
+    int e = 0;
+    (void)frexpf(mx, &e);                  // mx = f 2^e, f in [0.5, 1)
+    const int k = mx > 0.f ? 15 - e : 0;
+    scl[p] = ldexpf(1.f, k);
+    if (tid == 0) pack_s[p] = __float_as_uint(ldexpf(1.f, 24 - k));   // sum(code x) = D 2^(24 - k)
+  }
+  // the images: one thread per (piece, lane, register)
+  for (int i = tid; i < 8 * NIMG; i += kPrepThreads) {
+    const int piece = i / (4 * NIMG), t = (i / NIMG) % 4, rho = i % NIMG;
+    uint32_t v = 0u;
+    int ch[2] = {-1, -1};
+    float sc = 1.f;
+    bool res = false;
+    if (rho < 2 * NMA) {             // anchor: word rho / 4 of the lane, register k
+      const int k = rho & 3, wd = t * C::WA + (rho >> 2);
+      ch[0] = 8 * wd + k;
+      ch[1] = 8 * wd + k + 4;
+      sc = (k & 1) ? 0.0625f : 1.f;
+    } else if (t < C::TR) {          // residual: word (rho - 2 NMA) / 8 of the lane, register 2m + hb
+      const int r = rho - 2 * NMA, wd = 2 * t + (r >> 3), m = (r & 7) >> 1, hb = r & 1;
+      ch[0] = 16 * wd + 4 * hb + m;
+      ch[1] = 16 * wd + 4 * hb + m + 8;
+      sc = m == 0 ? 1.f : (m == 1 ? 0.25f : (m == 2 ? 0.0625f : 0.015625f));
+      res = true;
+    }
+    if (ch[0] >= 0) {
+      const float* xs = res ? qr_s : q_s;
+      const float s = scl[res ? 1 : 0] * sc;
+      __half h0, l0, h1, l1;
+      f16_pieces(xs[ch[0]] * s, h0, l0);
+      f16_pieces(xs[ch[1]] * s, h1, l1);
+      v = piece == 0 ? pack_f16x2(h0, h1) : pack_f16x2(l0, l1);
+    }
+    pack_s[kPackHeader + i] = v;
+  }
+  __syncthreads();
+  uint4* dst = reinterpret_cast<uint4*>(a.packs + (size_t)bh * kPackWords);
+  const uint4* src = reinterpret_cast<const uint4*>(pack_s);
+  for (int i = tid; i < (kPackHeader + 8 * NIMG) / 4; i += kPrepThreads) dst[i] = src[i];
 }
 
 // PAGED: the cache uses the block-table layout (tile addresses through the table).
 template <int D, int GS, int NRES, bool PAGED>
 __global__ void __launch_bounds__(kThreads, (Cfg<D, GS, NRES>::MINB)) decode_kernel(DecodeArgs a) {
   using C = Cfg<D, GS, NRES>;
-  constexpr int NG = C::NG, NGP = C::NGP, AW = C::AW, RW = C::RW, STAGES = C::STAGES;
-  constexpr int NITEM = C::NITEM, UTOK = C::UTOK, PPT = C::PPT, WQ = C::WQ;
+  constexpr int NG = C::NG, STAGES = C::STAGES, NITEM = C::NITEM, UTOK = C::UTOK;
+  constexpr int NMA = C::NMA, NMR = C::NMR, NACA = C::NACA, NACR = C::NACR, NIMG = C::NIMG, NGW = C::NGW;
+  constexpr typename C::AccMap MA = C::make_map(false), MR = C::make_map(true);
   extern __shared__ __align__(128) uint8_t smem[];
   __shared__ uint64_t full_bar[STAGES];
   __shared__ int pre_s[kMaxRows + 1];
   __shared__ int nt_s[kMaxRows + 1];        // work units (128-token) per row; then a sentinel
   __shared__ int sl_s[kMaxRows];
-  // per-unit scratch; the first two are double-buffered by unit parity
-  __shared__ float red_s[2][kThreads / 32];        // per-warp score maxima
-  __shared__ uint32_t tmax_s[2][NITEM];            // max |value weight| per item, float bits
-  // value weights of the unit in 16-bit fixed point, per item: the hi bytes indexed by token,
-  // then the lo bytes.  V rows put four consecutive tokens of a channel in the bytes of a
-  // masked code word, so one 32-bit load here is the matching dp4a operand.
-  __shared__ __align__(16) uint8_t wq_s[NITEM][WQ];
+  __shared__ __align__(16) float red_s[2][kThreads / 32];   // per-warp score maxima, by unit parity
   __shared__ float wsum_s[kThreads / 32][NITEM + 1];   // per-warp partials of off_s
   __shared__ float off_s[NITEM + 1];               // per-segment offset sums; [NITEM] = softmax sum
+  uint8_t* wimg = smem + STAGES * C::STAGE;        // value-weight images, then a zero block
 
   pdl_launch_dependents();   // the merge kernel may start staging R
   const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
+  const int gid = lane >> 2, tig = lane & 3;
   const int H = a.g.Hq, B = a.batch;   // units run over (row, query head); query head h reads KV head h / qpk
   const int Cn = gridDim.x, cta = blockIdx.x;
 
@@ -364,7 +506,8 @@ __global__ void __launch_bounds__(kThreads, (Cfg<D, GS, NRES>::MINB)) decode_ker
     for (int s = 0; s < STAGES; ++s) mbar_init(&full_bar[s], 1);
     fence_mbar_init();
   }
-  for (int i = tid; i < 2 * NITEM; i += kThreads) (&tmax_s[0][0])[i] = 0u;
+  // the zero block that idle lanes read their value B operands from
+  for (int i = tid; i < 64; i += kThreads) reinterpret_cast<uint32_t*>(wimg + NITEM * kWItem)[i] = 0u;
   __syncthreads();
   if (tid == 0) {
     if constexpr (PAGED) {
@@ -376,39 +519,50 @@ __global__ void __launch_bounds__(kThreads, (Cfg<D, GS, NRES>::MINB)) decode_ker
   Cursor cc = locate(u0);   // consumer cursor
   pdl_wait();               // the query packs of qprep_kernel are complete
 
-  // ---- per-thread state ----
-  const int gi1 = tid % NGP;              // phase-1 group of this thread (same for every pair)
-  const bool g_ok = gi1 < NG;
-  // query packs: anchor [AW words][E.hi, E.lo, O.hi, O.lo], residual [RW words][m][hi, lo]
-  uint32_t qa[AW][4];
-  uint32_t qrp[RW][4][2];
-  float sig_a = 0.f, sig_r = 0.f, qsum = 0.f, qrsum = 0.f;
-  float acc = 0.f;          // phase-2 accumulator: (channel, anchor|residual)
+  // ---- per-thread constants ----
+  // scoring: rows gid and gid + 8 of the warp's products are tokens tk0 and tk0 + 2
+  // (tk0 = 16 warp + 4 (gid / 2) + gid % 2; rows r0, r0 + 2 of tile tau), the pair
+  // that one f16x2 operand of the value products holds
+  const int tk0 = 16 * warp + 4 * (gid >> 1) + (gid & 1), tau = warp >> 2, r0 = tk0 & (kTile - 1);
+  // value-weight slot of the pair in the INT4 (anchor) and INT2 (residual) images
+  int so4, so2;
+  float sc4, sc2;
+  int4_slot(tk0, so4, sc4);
+  int2_slot(tk0, so2, sc2);
+  const bool bq_lane = (gid >> 1) == tig;   // lanes whose scoring B operands are not zero
+  // value products: channels vc0 = 16 warp + gid, vc1 = vc0 + 8 of group vg
+  const bool v_act = warp < C::VW;
+  const int vc0 = 16 * warp + gid, vg = (16 * warp) / GS;
+  const uint8_t* vzero = wimg + NITEM * kWItem;
+
+  // ---- per-segment state ----
+  uint32_t bq[NIMG];                 // B operands of the scoring products (query, rotated query)
+  float sig_a = 0.f, sig_r = 0.f;
+  float qa_own[NACA], qr_own[NACR];  // the offset sums of the groups this lane adds
+  float acc_a[4], acc_r[4];          // value accumulators (d0..d3 of the value products)
   float m_run = -INFINITY;
-  float off_part[1 + NRES]; // partial offset sums of this thread's group: anchor, residual planes
-  float l_part = 0.f;       // partial softmax denominator (threads of group 0)
-#pragma unroll
-  for (int j = 0; j <= NRES; ++j) off_part[j] = 0.f;
+  float off_part[1 + NRES][NGW];     // partial offset sums of this lane's weight groups
+  float l_part = 0.f;                // partial softmax denominator (lanes tig == 0)
   int cur_bh = -1;
   bool aborted = false;
   int fail_u = 0;
 
-  const int p2_ch = tid < D ? tid : tid - D;
-  const bool p2_anchor = tid < D;
-  const bool p2_active = tid < (NRES > 0 ? 2 * D : D);
-
   auto flush = [&](int bh) {
-    // finish the segment's partials: offset sums per item and the softmax denominator,
-    // per warp, then over the warps in a fixed order (repeated calls give equal bits)
+    // finish the segment's partials: offset sums per item and the softmax
+    // denominator, per warp, then over the warps in a fixed order (repeated calls
+    // give equal bits)
 #pragma unroll
-    for (int j = 0; j <= NRES; ++j) {
-      float x = off_part[j];
-      for (int off = NGP; off < 32; off <<= 1) x += __shfl_xor_sync(0xffffffffu, x, off);
-      if (lane < NGP && g_ok) wsum_s[warp][j * NG + gi1] = x;
-    }
+    for (int j = 0; j <= NRES; ++j)
+#pragma unroll
+      for (int s = 0; s < NGW; ++s) {
+        float x = off_part[j][s];
+        for (int off = 4; off < 32; off <<= 1) x += __shfl_xor_sync(0xffffffffu, x, off);
+        const int g = tig + 4 * s;
+        if (gid == 0 && g < NG) wsum_s[warp][j * NG + g] = x;
+      }
     {
       float x = l_part;
-      for (int off = 16; off > 0; off >>= 1) x += __shfl_xor_sync(0xffffffffu, x, off);
+      for (int off = 4; off < 32; off <<= 1) x += __shfl_xor_sync(0xffffffffu, x, off);
       if (lane == 0) wsum_s[warp][NITEM] = x;
     }
     __syncthreads();
@@ -425,49 +579,43 @@ __global__ void __launch_bounds__(kThreads, (Cfg<D, GS, NRES>::MINB)) decode_ker
       part[0] = m_run;
       part[1] = off_s[NITEM];
     }
-    if (p2_active) {
-      const int gi = p2_ch / GS;
-      float v = acc;
-      if (p2_anchor) {
-        v += off_s[gi];
-      } else {
+    if (v_act && tig == 0) {
+      float oa = off_s[vg], orr = 0.f;
 #pragma unroll
-        for (int r = 0; r < NRES; ++r) v += off_s[(1 + r) * NG + gi];
+      for (int r = 0; r < NRES; ++r) orr += off_s[(1 + r) * NG + vg];
+      part[2 + vc0] = fmaf(acc_a[0] + acc_a[1], 16777216.f, oa);
+      part[2 + vc0 + 8] = fmaf(acc_a[2] + acc_a[3], 16777216.f, oa);
+      if (NRES > 0) {
+        part[2 + D + vc0] = fmaf(acc_r[0] + acc_r[1], 16777216.f, orr);
+        part[2 + D + vc0 + 8] = fmaf(acc_r[2] + acc_r[3], 16777216.f, orr);
       }
-      part[2 + (p2_anchor ? 0 : D) + p2_ch] = v;
     }
   };
 
   auto begin_segment = [&](int bh) {
-    // this thread's group's query packs (written by qprep_kernel; read through L2)
-    const int gq = g_ok ? gi1 : 0;
-    const uint4* pk = reinterpret_cast<const uint4*>(a.packs + ((size_t)bh * NG + gq) * kPackWords);
-    uint32_t w[kPackWords];
+    const uint32_t* pk = a.packs + (size_t)bh * kPackWords;
+    sig_a = __uint_as_float(__ldcg(pk + 0));
+    sig_r = __uint_as_float(__ldcg(pk + 1));
 #pragma unroll
-    for (int i = 0; i < kPackWords / 4; ++i) {
-      const uint4 v = __ldcg(pk + i);
-      w[4 * i] = v.x; w[4 * i + 1] = v.y; w[4 * i + 2] = v.z; w[4 * i + 3] = v.w;
+    for (int ac = 0; ac < NACA; ++ac) qa_own[ac] = __uint_as_float(__ldcg(pk + 4 + C::ga(tig, MA.rep[ac])));
+#pragma unroll
+    for (int ac = 0; ac < NACR; ++ac)
+      qr_own[ac] = tig < C::TR ? __uint_as_float(__ldcg(pk + 4 + NG + C::gr(tig, MR.rep[ac]))) : 0.f;
+    // the image of this lane (piece gid & 1, lane tig), when it is one of the eight non-zero ones
+    const uint4* img = reinterpret_cast<const uint4*>(pk + kPackHeader + ((gid & 1) * 4 + tig) * NIMG);
+#pragma unroll
+    for (int i = 0; i < NIMG / 4; ++i) {
+      const uint4 v = bq_lane ? __ldcg(img + i) : make_uint4(0u, 0u, 0u, 0u);
+      bq[4 * i] = v.x; bq[4 * i + 1] = v.y; bq[4 * i + 2] = v.z; bq[4 * i + 3] = v.w;
     }
-#pragma unroll
-    for (int x = 0; x < AW; ++x)
-#pragma unroll
-      for (int k = 0; k < 4; ++k) qa[x][k] = w[4 * x + k];
-#pragma unroll
-    for (int x = 0; x < RW; ++x)
-#pragma unroll
-      for (int m = 0; m < 4; ++m) {
-        qrp[x][m][0] = w[16 + 8 * x + 2 * m];
-        qrp[x][m][1] = w[16 + 8 * x + 2 * m + 1];
-      }
-    sig_a = __uint_as_float(w[32]);
-    qsum = __uint_as_float(w[33]);
-    sig_r = __uint_as_float(w[34]);
-    qrsum = __uint_as_float(w[35]);
     m_run = -INFINITY;
     l_part = 0.f;
 #pragma unroll
-    for (int j = 0; j <= NRES; ++j) off_part[j] = 0.f;
-    acc = 0.f;
+    for (int j = 0; j <= NRES; ++j)
+#pragma unroll
+      for (int s = 0; s < NGW; ++s) off_part[j][s] = 0.f;
+#pragma unroll
+    for (int i = 0; i < 4; ++i) { acc_a[i] = 0.f; acc_r[i] = 0.f; }
     cur_bh = bh;
   };
 
@@ -483,81 +631,117 @@ __global__ void __launch_bounds__(kThreads, (Cfg<D, GS, NRES>::MINB)) decode_ker
     if (!mbar_wait_bounded(&full_bar[stage], (uint32_t)((it / STAGES) & 1))) aborted = true;
 
     const uint8_t* st = smem + stage * C::STAGE;
+    const uint8_t* sub = st + tau * C::SUB;   // the layout tile of this lane's tokens
 
-    // ---- phase 1: score of each token; a token's NGP groups sit in adjacent lanes ----
-    float wmax = -INFINITY;
-    float sc[PPT];            // scores of this thread's tokens (every lane of a token has it)
+    // ---- scores of tokens tk0, tk1: tensor-core products over the K planes ----
+    float sc0, sc1;
+    {
+      // anchor: this lane's words of the two token rows
+      uint32_t wa0[C::WA], wa1[C::WA];
+      const uint8_t* ak = sub + r0 * (D / 2) + tig * (D / 8);
+      if constexpr (C::WA == 4) {
+        const uint4 x0 = *reinterpret_cast<const uint4*>(ak);
+        const uint4 x1 = *reinterpret_cast<const uint4*>(ak + 2 * (D / 2));
+        wa0[0] = x0.x; wa0[1] = x0.y; wa0[2] = x0.z; wa0[3] = x0.w;
+        wa1[0] = x1.x; wa1[1] = x1.y; wa1[2] = x1.z; wa1[3] = x1.w;
+      } else {
 #pragma unroll
-    for (int pp = 0; pp < PPT; ++pp) {
-      const int tok = (tid + pp * kThreads) / NGP;
-      const uint8_t* sub = st + (tok >> 6) * C::SUB;   // layout tile of this token
-      const int row = tok & (kTile - 1);
-      float score = 0.f;
-      if (g_ok && !aborted && tok < n_valid) {
-        const int gi = gi1;
-        const uint8_t* AK = sub;
-        // anchor: INT4 token-major; masks give the even / (16 x) odd channels as bytes
-        uint32_t aw[4];
-        if (AW == 4) {
-          uint4 v = *reinterpret_cast<const uint4*>(AK + row * (D / 2) + gi * (GS / 2));
-          aw[0] = v.x; aw[1] = v.y; aw[2] = v.z; aw[3] = v.w;
-        } else {
-          uint2 v = *reinterpret_cast<const uint2*>(AK + row * (D / 2) + gi * (GS / 2));
-          aw[0] = v.x; aw[1] = v.y; aw[2] = 0u; aw[3] = 0u;
-        }
-        int eh = 0, el = 0, oh = 0, ol = 0;
-#pragma unroll
-        for (int w = 0; w < AW; ++w) {
-          const uint32_t lo4 = aw[w] & 0x0F0F0F0Fu, hi4 = aw[w] & 0xF0F0F0F0u;
-          eh = dp4a_us(lo4, qa[w][0], eh);
-          el = dp4a_uu(lo4, qa[w][1], el);
-          oh = dp4a_us(hi4, qa[w][2], oh);
-          ol = dp4a_uu(hi4, qa[w][3], ol);
-        }
-        const int ta = shl(shl(eh, 8) + el, 4) + shl(oh, 8) + ol;     // 16 x sum(q_fix * code)
-        const float2 ma = meta2(AK + C::A_CODES + row * NG * 2 + gi * 2);
-        const float score_a = fmaf(ma.x, (float)ta * sig_a, ma.y * qsum);
-        score = score_a;
-        if (NRES > 0) {
-          float cprod = 1.f, sres = 0.f;
-#pragma unroll
-          for (int r = 0; r < NRES; ++r) {
-            const uint8_t* RK = sub + 2 * C::A_TILE + 2 * r * C::R_TILE;
-            uint32_t rw[2];
-            if (RW == 2) {
-              uint2 v = *reinterpret_cast<const uint2*>(RK + row * (D / 4) + gi * (GS / 4));
-              rw[0] = v.x; rw[1] = v.y;
-            } else {
-              rw[0] = *reinterpret_cast<const uint32_t*>(RK + row * (D / 4) + gi * (GS / 4));
-              rw[1] = 0u;
-            }
-            int hm[4] = {0, 0, 0, 0}, lm[4] = {0, 0, 0, 0};
-#pragma unroll
-            for (int w = 0; w < RW; ++w)
-#pragma unroll
-              for (int m = 0; m < 4; ++m) {
-                const uint32_t bm = rw[w] & (0x03030303u << (2 * m));
-                hm[m] = dp4a_us(bm, qrp[w][m][0], hm[m]);
-                lm[m] = dp4a_uu(bm, qrp[w][m][1], lm[m]);
-              }
-            const int tr = shl(shl(hm[0], 8) + lm[0], 6) + shl(shl(hm[1], 8) + lm[1], 4) +
-                           shl(shl(hm[2], 8) + lm[2], 2) + (shl(hm[3], 8) + lm[3]);   // 64 x dot
-            const float2 mr = meta2(RK + C::R_CODES + row * NG * 2 + gi * 2);
-            const float cr = bf16_bits_to_f32(*reinterpret_cast<const uint16_t*>(RK + C::R_CODES + C::META + row * 2));
-            // chained: plane r weighs the product of the coefficients before it
-            sres = fmaf(cprod, fmaf(mr.x, (float)tr * sig_r, mr.y * qrsum), sres);
-            cprod *= cr;
-          }
-          score = fmaf(cprod, score_a, sres);
+        for (int k = 0; k < C::WA; ++k) {
+          wa0[k] = *reinterpret_cast<const uint32_t*>(ak + 4 * k);
+          wa1[k] = *reinterpret_cast<const uint32_t*>(ak + 2 * (D / 2) + 4 * k);
         }
       }
+      float da[NACA][4];
 #pragma unroll
-      for (int off = 1; off < NGP; off <<= 1) score += __shfl_xor_sync(0xffffffffu, score, off);
-      if (tok >= n_valid) score = -INFINITY;
-      sc[pp] = score;
-      wmax = fmaxf(wmax, score);
+      for (int ac = 0; ac < NACA; ++ac) da[ac][0] = da[ac][1] = da[ac][2] = da[ac][3] = 0.f;
+#pragma unroll
+      for (int k = 0; k < C::WA; ++k) {
+        uint32_t x0[4], x1[4];
+        int4_f16(wa0[k], x0);
+        int4_f16(wa1[k], x1);
+#pragma unroll
+        for (int jj = 0; jj < 2; ++jj) {
+          const int j = 2 * k + jj;
+          mma16816(da[MA.acc[j]], x0[2 * jj], x1[2 * jj], x0[2 * jj + 1], x1[2 * jj + 1], bq[2 * j], bq[2 * j + 1]);
+        }
+      }
+      // anchor score per token: sum over this lane's accumulators of s * (dot product) + o * sum(q)
+      float sa0 = 0.f, sa1 = 0.f;
+      const uint8_t* am = sub + C::A_CODES + r0 * NG * 2;
+#pragma unroll
+      for (int ac = 0; ac < NACA; ++ac) {
+        const int g = C::ga(tig, MA.rep[ac]);
+        const float2 m0 = meta2(am + g * 2), m1 = meta2(am + 2 * NG * 2 + g * 2);
+        const bool own = (MA.own >> (4 * ac + tig)) & 1u;
+        sa0 = fmaf(m0.x, (da[ac][0] + da[ac][1]) * sig_a, own ? fmaf(m0.y, qa_own[ac], sa0) : sa0);
+        sa1 = fmaf(m1.x, (da[ac][2] + da[ac][3]) * sig_a, own ? fmaf(m1.y, qa_own[ac], sa1) : sa1);
+      }
+      sc0 = sa0;
+      sc1 = sa1;
+      if constexpr (NRES > 0) {
+        float cp0 = 1.f, cp1 = 1.f, sr0 = 0.f, sr1 = 0.f;
+#pragma unroll
+        for (int r = 0; r < NRES; ++r) {
+          const uint8_t* rk = sub + 2 * C::A_TILE + 2 * r * C::R_TILE;
+          float dr[NACR][4];
+#pragma unroll
+          for (int ac = 0; ac < NACR; ++ac) dr[ac][0] = dr[ac][1] = dr[ac][2] = dr[ac][3] = 0.f;
+          // lanes without residual words (d = 96: lane 3) take part with zero operands:
+          // the products are warp-wide
+          uint32_t w0[2] = {0u, 0u}, w1[2] = {0u, 0u};
+          if (tig < C::TR) {
+            const uint8_t* rr = rk + r0 * (D / 4) + tig * 8;
+            const uint2 y0 = *reinterpret_cast<const uint2*>(rr);
+            const uint2 y1 = *reinterpret_cast<const uint2*>(rr + 2 * (D / 4));
+            w0[0] = y0.x; w0[1] = y0.y; w1[0] = y1.x; w1[1] = y1.y;
+          }
+#pragma unroll
+          for (int k = 0; k < 2; ++k) {
+            uint32_t x0[8], x1[8];
+            int2_f16(w0[k], x0);
+            int2_f16(w1[k], x1);
+#pragma unroll
+            for (int jj = 0; jj < 4; ++jj) {
+              const int j = 4 * k + jj;
+              mma16816(dr[MR.acc[j]], x0[2 * jj], x1[2 * jj], x0[2 * jj + 1], x1[2 * jj + 1],
+                       bq[2 * NMA + 2 * j], bq[2 * NMA + 2 * j + 1]);
+            }
+          }
+          float s0 = 0.f, s1 = 0.f;
+          if (tig < C::TR) {
+            const uint8_t* rm = rk + C::R_CODES + r0 * NG * 2;
+#pragma unroll
+            for (int ac = 0; ac < NACR; ++ac) {
+              const int g = C::gr(tig, MR.rep[ac]);
+              const float2 m0 = meta2(rm + g * 2), m1 = meta2(rm + 2 * NG * 2 + g * 2);
+              const bool own = (MR.own >> (4 * ac + tig)) & 1u;
+              s0 = fmaf(m0.x, (dr[ac][0] + dr[ac][1]) * sig_r, own ? fmaf(m0.y, qr_own[ac], s0) : s0);
+              s1 = fmaf(m1.x, (dr[ac][2] + dr[ac][3]) * sig_r, own ? fmaf(m1.y, qr_own[ac], s1) : s1);
+            }
+          }
+          const uint8_t* rc = rk + C::R_CODES + C::META + r0 * 2;
+          const float c0 = bf16_bits_to_f32(*reinterpret_cast<const uint16_t*>(rc));
+          const float c1 = bf16_bits_to_f32(*reinterpret_cast<const uint16_t*>(rc + 4));
+          // chained: plane r weighs the product of the coefficients before it
+          sr0 = fmaf(cp0, s0, sr0);
+          sr1 = fmaf(cp1, s1, sr1);
+          cp0 *= c0;
+          cp1 *= c1;
+        }
+        sc0 = fmaf(cp0, sa0, sr0);
+        sc1 = fmaf(cp1, sa1, sr1);
+      }
+      // the token's score: the sum over the four lanes of its row
+      sc0 += __shfl_xor_sync(0xffffffffu, sc0, 1);
+      sc1 += __shfl_xor_sync(0xffffffffu, sc1, 1);
+      sc0 += __shfl_xor_sync(0xffffffffu, sc0, 2);
+      sc1 += __shfl_xor_sync(0xffffffffu, sc1, 2);
     }
-    for (int off = 16; off > 0; off >>= 1) wmax = fmaxf(wmax, __shfl_xor_sync(0xffffffffu, wmax, off));
+    const bool ok0 = !aborted && tk0 < n_valid, ok1 = !aborted && tk0 + 2 < n_valid;
+    if (!ok0) sc0 = -INFINITY;
+    if (!ok1) sc1 = -INFINITY;
+    float wmax = fmaxf(sc0, sc1);
+    for (int off = 4; off < 32; off <<= 1) wmax = fmaxf(wmax, __shfl_xor_sync(0xffffffffu, wmax, off));
     if (lane == 0) red_s[buf][warp] = wmax;
     if (__syncthreads_or(aborted)) {                   // B1: per-warp score maxima are in red_s
       fail_u = u;
@@ -568,144 +752,105 @@ __global__ void __launch_bounds__(kThreads, (Cfg<D, GS, NRES>::MINB)) decode_ker
     // every warp has finished the previous unit: its stage can be refilled
     if (tid == 0 && it >= 1 && u - 1 + STAGES < u1) issue((it - 1) % STAGES);
 
-    float m_tile = red_s[buf][0];
-#pragma unroll
-    for (int w = 1; w < kThreads / 32; ++w) m_tile = fmaxf(m_tile, red_s[buf][w]);
+    const float4 ma4 = reinterpret_cast<const float4*>(red_s[buf])[0], mb4 = reinterpret_cast<const float4*>(red_s[buf])[1];
+    const float m_tile = fmaxf(fmaxf(fmaxf(ma4.x, ma4.y), fmaxf(ma4.z, ma4.w)), fmaxf(fmaxf(mb4.x, mb4.y), fmaxf(mb4.z, mb4.w)));
     const float m_new = fmaxf(m_run, m_tile);
     const float alpha = ex2_fast(m_run - m_new);   // 0 on the first unit (m_run = -inf)
     m_run = m_new;
 
-    // the maxima of the other parity were last read before B1: clear them for the next unit
-    if (tid < NITEM) tmax_s[buf ^ 1][tid] = 0u;
-
-    // ---- value weights of this thread's (token, group) pairs: p * coefficients * scale,
-    //      and the offset terms p * coefficients * offset summed on the fly ----
-    float wv[PPT][1 + NRES];
+    // ---- value weights p * coefficients * scale of this lane's (token, group)
+    //      pairs as f16 pieces into the images; offsets p * coefficients * offset ----
+    const float p0 = ex2_fast(sc0 - m_new), p1 = ex2_fast(sc1 - m_new);   // 0 for masked tokens
+    if (tig == 0) l_part = fmaf(l_part, alpha, p0 + p1);
 #pragma unroll
-    for (int j = 0; j <= NRES; ++j) off_part[j] *= alpha;
+    for (int j = 0; j <= NRES; ++j)
 #pragma unroll
-    for (int pp = 0; pp < PPT; ++pp) {
-      const int tok = (tid + pp * kThreads) / NGP;
-      const float pt = ex2_fast(sc[pp] - m_new);       // 0 for masked tokens
-      if (gi1 == 0) l_part = fmaf(l_part, pp == 0 ? alpha : 1.f, pt);
+      for (int s = 0; s < NGW; ++s) off_part[j][s] *= alpha;
 #pragma unroll
-      for (int j = 0; j <= NRES; ++j) wv[pp][j] = 0.f;
-      if (g_ok && tok < n_valid) {
-        const uint8_t* sub = st + (tok >> 6) * C::SUB;
-        const int row = tok & (kTile - 1);
-        float cprod = pt;   // p times the coefficients of the planes before the current one
+    for (int s = 0; s < NGW; ++s) {
+      const int g = tig + 4 * s;
+      if (g < NG) {
+        float cp0 = p0, cp1 = p1;   // p times the coefficients of the planes before the current one
 #pragma unroll
         for (int r = 0; r < NRES; ++r) {
-          const uint8_t* RV = sub + 2 * C::A_TILE + (2 * r + 1) * C::R_TILE;
-          const float2 mv = meta2(RV + C::R_CODES + row * NG * 2 + gi1 * 2);
-          wv[pp][1 + r] = cprod * mv.x;
-          off_part[1 + r] = fmaf(cprod, mv.y, off_part[1 + r]);
-          cprod *= bf16_bits_to_f32(*reinterpret_cast<const uint16_t*>(RV + C::R_CODES + C::META + row * 2));
+          const uint8_t* rv = sub + 2 * C::A_TILE + (2 * r + 1) * C::R_TILE + C::R_CODES;
+          const float2 v0 = meta2(rv + r0 * NG * 2 + g * 2), v1 = meta2(rv + (r0 + 2) * NG * 2 + g * 2);
+          if (ok0) off_part[1 + r][s] = fmaf(cp0, v0.y, off_part[1 + r][s]);
+          if (ok1) off_part[1 + r][s] = fmaf(cp1, v1.y, off_part[1 + r][s]);
+          uint32_t hi, lo;
+          f16x2_pieces(ok0 ? cp0 * v0.x * sc2 : 0.f, ok1 ? cp1 * v1.x * sc2 : 0.f, hi, lo);
+          uint8_t* im = wimg + ((1 + r) * NG + g) * kWItem + so2;
+          *reinterpret_cast<uint32_t*>(im) = hi;
+          *reinterpret_cast<uint32_t*>(im + kWPiece) = lo;
+          const uint8_t* rc = rv + C::META + r0 * 2;
+          if (ok0) cp0 *= bf16_bits_to_f32(*reinterpret_cast<const uint16_t*>(rc));
+          if (ok1) cp1 *= bf16_bits_to_f32(*reinterpret_cast<const uint16_t*>(rc + 4));
         }
-        const float2 ma = meta2(sub + C::A_TILE + C::A_CODES + row * NG * 2 + gi1 * 2);
-        wv[pp][0] = cprod * ma.x;
-        off_part[0] = fmaf(cprod, ma.y, off_part[0]);
+        const uint8_t* am = sub + C::A_TILE + C::A_CODES;
+        const float2 a0 = meta2(am + r0 * NG * 2 + g * 2), a1 = meta2(am + (r0 + 2) * NG * 2 + g * 2);
+        if (ok0) off_part[0][s] = fmaf(cp0, a0.y, off_part[0][s]);
+        if (ok1) off_part[0][s] = fmaf(cp1, a1.y, off_part[0][s]);
+        uint32_t hi, lo;
+        f16x2_pieces(ok0 ? cp0 * a0.x * sc4 : 0.f, ok1 ? cp1 * a1.x * sc4 : 0.f, hi, lo);
+        uint8_t* im = wimg + g * kWItem + so4;
+        *reinterpret_cast<uint32_t*>(im) = hi;
+        *reinterpret_cast<uint32_t*>(im + kWPiece) = lo;
       }
     }
-    // per-item max |w|: lanes of one group, then one shared atomic per warp and item
-    // (|w| >= 0 orders like its bit pattern)
-#pragma unroll
-    for (int j = 0; j <= NRES; ++j) {
-      float mx = 0.f;
-#pragma unroll
-      for (int pp = 0; pp < PPT; ++pp) mx = fmaxf(mx, fabsf(wv[pp][j]));
-      for (int off = NGP; off < 32; off <<= 1) mx = fmaxf(mx, __shfl_xor_sync(0xffffffffu, mx, off));
-      if (lane < NGP && g_ok) atomicMax(&tmax_s[buf][j * NG + gi1], __float_as_uint(mx));
-    }
-    __syncthreads();                                   // B2: per-item maxima are final
-    if (g_ok) {
-#pragma unroll
-      for (int j = 0; j <= NRES; ++j) {
-        const float mx = __uint_as_float(tmax_s[buf][j * NG + gi1]);
-        // any scale near kFix / mx works: the weights are clamped to the 16-bit
-        // range and dequantized with mx / kFix
-        const float inv = mx > 0.f ? __fdividef(kFix, mx) : 0.f;
-        uint8_t* wq = wq_s[j * NG + gi1];
-#pragma unroll
-        for (int pp = 0; pp < PPT; ++pp) {
-          const int tok = (tid + pp * kThreads) / NGP;
-          const int v = to_fix(wv[pp][j], inv);
-          wq[tok] = (uint8_t)fix_hi(v);
-          wq[UTOK + tok] = (uint8_t)fix_lo(v);
-        }
-      }
-    }
-    __syncthreads();                                   // B3: weight operands are in wq_s
+    __syncthreads();                                   // B2: the weight images are complete
 
-    // ---- phase 2: value accumulation, thread = (channel, anchor | residual) ----
-    if (p2_active) {
-      const int gi = p2_ch / GS;
-      float add = 0.f;
-      if (p2_anchor) {
-        const uint8_t* wq = wq_s[gi];
-        int eh = 0, el = 0, oh = 0, ol = 0;
+    // ---- value products: channels vc0, vc0 + 8 against the weights of the 128 tokens ----
+    if (v_act) {
+      const uint8_t* vb = gid < 2 ? wimg + vg * kWItem + gid * kWPiece + tig * 8 : vzero + tig * 8;
+      float dv[4] = {0.f, 0.f, 0.f, 0.f};
 #pragma unroll
-        for (int sb = 0; sb < C::UT; ++sb) {
-          const uint4* row = reinterpret_cast<const uint4*>(st + sb * C::SUB + C::A_TILE + p2_ch * (kTile / 2));
+      for (int t2 = 0; t2 < C::UT; ++t2) {
+        const uint8_t* av = st + t2 * C::SUB + C::A_TILE + vc0 * (kTile / 2) + tig * 8;
+        const uint2 y0 = *reinterpret_cast<const uint2*>(av);
+        const uint2 y1 = *reinterpret_cast<const uint2*>(av + 8 * (kTile / 2));
+        const uint32_t w0[2] = {y0.x, y0.y}, w1[2] = {y1.x, y1.y};
 #pragma unroll
-          for (int h2 = 0; h2 < 2; ++h2) {
-            const uint4 x4 = row[h2];
-            const uint32_t xs[4] = {x4.x, x4.y, x4.z, x4.w};
+        for (int e = 0; e < 2; ++e) {
+          uint32_t x0[4], x1[4];
+          int4_f16(w0[e], x0);
+          int4_f16(w1[e], x1);
 #pragma unroll
-            for (int q2 = 0; q2 < 2; ++q2) {
-              // code words w, w+1 hold tokens 8w .. 8w+15; the low nibbles of word w are
-              // tokens 8w .. 8w+3, the high nibbles 8w+4 .. 8w+7
-              const int w = sb * 8 + h2 * 4 + q2 * 2;
-              const uint4 wh = *reinterpret_cast<const uint4*>(wq + 8 * w);
-              const uint4 wl = *reinterpret_cast<const uint4*>(wq + UTOK + 8 * w);
-              const uint32_t a0 = xs[2 * q2], a1 = xs[2 * q2 + 1];
-              eh = dp4a_us(a0 & 0x0F0F0F0Fu, wh.x, eh);
-              el = dp4a_uu(a0 & 0x0F0F0F0Fu, wl.x, el);
-              oh = dp4a_us(a0 & 0xF0F0F0F0u, wh.y, oh);
-              ol = dp4a_uu(a0 & 0xF0F0F0F0u, wl.y, ol);
-              eh = dp4a_us(a1 & 0x0F0F0F0Fu, wh.z, eh);
-              el = dp4a_uu(a1 & 0x0F0F0F0Fu, wl.z, el);
-              oh = dp4a_us(a1 & 0xF0F0F0F0u, wh.w, oh);
-              ol = dp4a_uu(a1 & 0xF0F0F0F0u, wl.w, ol);
+          for (int jj = 0; jj < 2; ++jj) {
+            const int m = 2 * (2 * t2 + e) + jj;
+            const uint2 bb = *reinterpret_cast<const uint2*>(vb + m * 32);
+            mma16816(dv, x0[2 * jj], x1[2 * jj], x0[2 * jj + 1], x1[2 * jj + 1], bb.x, bb.y);
+          }
+        }
+      }
+#pragma unroll
+      for (int i = 0; i < 4; ++i) acc_a[i] = fmaf(acc_a[i], alpha, dv[i]);
+      if constexpr (NRES > 0) {
+        float dr[4] = {0.f, 0.f, 0.f, 0.f};
+#pragma unroll
+        for (int r = 0; r < NRES; ++r) {
+          const uint8_t* vbr = gid < 2 ? wimg + ((1 + r) * NG + vg) * kWItem + gid * kWPiece + tig * 8 : vzero + tig * 8;
+#pragma unroll
+          for (int t2 = 0; t2 < C::UT; ++t2) {
+            const uint8_t* rvp = st + t2 * C::SUB + 2 * C::A_TILE + (2 * r + 1) * C::R_TILE + vc0 * (kTile / 4) + tig * 4;
+            const uint32_t y0 = *reinterpret_cast<const uint32_t*>(rvp);
+            const uint32_t y1 = *reinterpret_cast<const uint32_t*>(rvp + 8 * (kTile / 4));
+            uint32_t x0[8], x1[8];
+            int2_f16(y0, x0);
+            int2_f16(y1, x1);
+#pragma unroll
+            for (int jj = 0; jj < 4; ++jj) {
+              const int m = 4 * t2 + jj;
+              const uint2 bb = *reinterpret_cast<const uint2*>(vbr + m * 32);
+              mma16816(dr, x0[2 * jj], x1[2 * jj], x0[2 * jj + 1], x1[2 * jj + 1], bb.x, bb.y);
             }
           }
         }
-        const int t = shl(shl(eh, 8) + el, 4) + shl(oh, 8) + ol;        // 16 x sum(w_fix * code)
-        add = (float)t * (__uint_as_float(tmax_s[buf][gi]) * (1.f / (16.f * kFix)));
-      } else {
 #pragma unroll
-        for (int r = 0; r < NRES; ++r) {
-          const int item = (1 + r) * NG + gi;
-          const uint8_t* wq = wq_s[item];
-          int hm[4] = {0, 0, 0, 0}, lm[4] = {0, 0, 0, 0};
-#pragma unroll
-          for (int sb = 0; sb < C::UT; ++sb) {
-            const uint4 x4 = *reinterpret_cast<const uint4*>(st + sb * C::SUB + 2 * C::A_TILE +
-                                                             (2 * r + 1) * C::R_TILE + p2_ch * (kTile / 4));
-            const uint32_t xs[4] = {x4.x, x4.y, x4.z, x4.w};
-#pragma unroll
-            for (int j = 0; j < 4; ++j) {
-              // word j: mask 3 << 2m leaves tokens 16j + 4m .. 16j + 4m + 3
-              const int t0 = sb * kTile + 16 * j;
-              const uint4 wh = *reinterpret_cast<const uint4*>(wq + t0);
-              const uint4 wl = *reinterpret_cast<const uint4*>(wq + UTOK + t0);
-              const uint32_t b0 = xs[j] & 0x03030303u, b1 = xs[j] & 0x0C0C0C0Cu;
-              const uint32_t b2 = xs[j] & 0x30303030u, b3 = xs[j] & 0xC0C0C0C0u;
-              hm[0] = dp4a_us(b0, wh.x, hm[0]); lm[0] = dp4a_uu(b0, wl.x, lm[0]);
-              hm[1] = dp4a_us(b1, wh.y, hm[1]); lm[1] = dp4a_uu(b1, wl.y, lm[1]);
-              hm[2] = dp4a_us(b2, wh.z, hm[2]); lm[2] = dp4a_uu(b2, wl.z, lm[2]);
-              hm[3] = dp4a_us(b3, wh.w, hm[3]); lm[3] = dp4a_uu(b3, wl.w, lm[3]);
-            }
-          }
-          const int t = shl(shl(hm[0], 8) + lm[0], 6) + shl(shl(hm[1], 8) + lm[1], 4) +
-                        shl(shl(hm[2], 8) + lm[2], 2) + (shl(hm[3], 8) + lm[3]);   // 64 x sum
-          add = fmaf((float)t, __uint_as_float(tmax_s[buf][item]) * (1.f / (64.f * kFix)), add);
-        }
+        for (int i = 0; i < 4; ++i) acc_r[i] = fmaf(acc_r[i], alpha, dr[i]);
       }
-      acc = fmaf(acc, alpha, add);
     }
-    // no barrier here: the next unit writes wq_s only after its B2 and clears this
-    // parity's maxima only after its B1, and its stage is refilled after the next B1
+    // no barrier here: the next unit writes the images only after its B1, and its
+    // stage is refilled after the next B1
   }
 
   if (aborted) {
@@ -720,6 +865,7 @@ __global__ void __launch_bounds__(kThreads, (Cfg<D, GS, NRES>::MINB)) decode_ker
   }
   __syncthreads();
   if (cur_bh >= 0) flush(cur_bh);
+  (void)NMR;
 }
 
 // Combines the partial softmax states of (row, head) blockIdx.x: the CTAs that

@@ -14,6 +14,7 @@ pins on the CPU that each pattern reaches its edge):
     the data are not O(1) (E4M3 saturation, values past +-448) the bar is
     2e-3 times the largest |output| of the (row, head), i.e. the same relative
     precision;
+  * a softmax that one key dominates, or two keys share, with queries x 8;
   * ragged lengths 1, 2, 31, 32, 33, 255 in one call.
 
 Sources: the explainer "ResidualQuant stores looped-Transformer KV caches as
@@ -178,6 +179,36 @@ def test_residual_edges_through_an_exact_rotation(d, g):
     worst = _decode_all_loops(gpu, obuf, geom, R, case, seq, 82, False, scaled=True)
     assert gpu.status.tolist() == [0, 0, 0, 0]
     print(f"exact-rotation residual edges d={d} g={g}: decode {worst:.2e} (relative); bytes equal")
+
+
+@pytest.mark.parametrize("d,g", [(128, 32), (96, 32), (128, 16)])
+def test_peaky_softmax(d, g):
+    """Queries x 8 (a few keys carry the softmax); one row whose query is aligned
+    with one cached key (that key takes almost all the weight) and one whose
+    query points between two keys (they share it)."""
+    case = Case(L=1, P=4, G=1, H=2, d=d, g=g, B=3, Nmax=320, seed=83)
+    n = 300
+    kvb, kv = kv_for(case, 84, n)
+    gpu, geom, obuf, R = _fill(case, kv, np.zeros(3, dtype=np.int64))
+    seq = np.array([300, 257, 129])
+    scale = 1.0 / math.sqrt(d)
+    worst = 0.0
+    for loop in range(4):
+        qb, q = synth.queries(85 + loop, 3, 2, d)
+        q8 = (qb.float() * 8).to(torch.bfloat16)
+        # row 1, head 0: aligned with key 77; row 2, head 1: between keys 10 and 100
+        q8[1, 0] = (0.5 * torch.from_numpy(kv[loop, 0, 1, 0, 77])).to(torch.bfloat16)
+        q8[2, 1] = (0.25 * torch.from_numpy(kv[loop, 0, 2, 1, 10] + kv[loop, 0, 2, 1, 100])).to(torch.bfloat16)
+        qf = q8.double().numpy()
+        cb, cur = synth.looped_kv(86 + loop, case.workload(), batch=3, ntok=1)
+        out = gpu.decode(0, 0, loop, q8, cb[loop, 0, :, :, 0], cb[loop, 1, :, :, 0], seq, scale).cpu().numpy()
+        ref = oracle.decode_attention(obuf, geom, R, 0, 0, loop, qf, cur[loop, 0, :, :, 0], cur[loop, 1, :, :, 0],
+                                      seq, scale)
+        err = float(np.abs(out - ref).max())
+        worst = max(worst, err)
+        assert err <= ATOL, f"loop {loop}: max abs err {err:.3e}"
+    assert gpu.status.tolist() == [0, 0, 0, 0]
+    print(f"peaky softmax d={d} g={g}: worst {worst:.2e}")
 
 
 def test_ragged_lengths_with_edge_vectors():
