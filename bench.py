@@ -88,8 +88,13 @@ class ClockSampler:
             self.proc = subprocess.Popen(["nvidia-smi", "-i", str(self.gpu), f"--query-gpu={q}",
                                           "--format=csv,noheader,nounits", "-lms", "50"],
                                          stdout=subprocess.PIPE, stderr=subprocess.DEVNULL, text=True)
+            self.first = threading.Event()
             self.t = threading.Thread(target=self._read, daemon=True)
             self.t.start()
+            # the timed region starts once the sampler delivers (its start-up takes a while);
+            # the samples kept are the ones taken from then on
+            self.first.wait(timeout=5.0)
+            self.lines = []
         except Exception:
             self.proc = None
         return self
@@ -97,6 +102,7 @@ class ClockSampler:
     def _read(self):
         for line in self.proc.stdout:
             self.lines.append(line.strip())
+            self.first.set()
 
     def __exit__(self, *a):
         if self.proc:
@@ -248,7 +254,7 @@ def _l2_note(w, chained=False):
 def main():
     ap = argparse.ArgumentParser()
     ap.add_argument("--gpus", type=int, default=1)
-    ap.add_argument("--steps", type=int, default=100)
+    ap.add_argument("--steps", type=int, default=300)
     ap.add_argument("--warmup", type=int, default=5)
     ap.add_argument("--impl", default="rq", choices=["rq", "reference"])
     ap.add_argument("--workload", default="ouro8k", choices=sorted(synth.WORKLOADS))
@@ -257,6 +263,9 @@ def main():
     ap.add_argument("--no-bf16", action="store_true", help="skip the BF16 comparator")
     ap.add_argument("--no-cpu", action="store_true", help="skip the CPU-oracle baseline")
     ap.add_argument("--no-e2e", action="store_true")
+    ap.add_argument("--no-configs", action="store_true",
+                    help="time only the main workload (the default run also times " + ", ".join(
+                        ("ouro16k_b2", "ouro16k_b4", "huginn")) + " as sub-records)")
     ap.add_argument("--ref-budget", type=float, default=None,
                     help="seconds of oracle work per reference step (default: about 150 s per run)")
     ap.add_argument("--quiet", action="store_true")
@@ -281,27 +290,24 @@ def main():
     run_rq(args, w)
 
 
-def run_rq(args, w):
+def _time_step(args, w, dev, rank, world, chained=False, hadamard=False, paged=False, query_heads=None):
+    """Builds a cache of workload w on dev, fills it (prefill), captures one decode
+    step in a CUDA graph and times args.steps replays (after args.warmup), then
+    each kind of call on its own.  Returns the measurements and the live objects
+    (graph, stream, per-step tensors, cache handle) for the end-to-end leg;
+    _release frees them."""
     import torch
-    world = int(os.environ.get("WORLD_SIZE", "1"))
-    rank = int(os.environ.get("RANK", "0"))
-    local = int(os.environ.get("LOCAL_RANK", "0"))
-    torch.cuda.set_device(local)
-    dev = torch.device("cuda", local)
-    if world > 1:
-        import torch.distributed as dist
-        dist.init_process_group("nccl")
     import decode_attention_rq_gb300 as rq
 
     L, P, G, H, d, g, B, N = (w.num_layers, w.loops_per_group, w.num_groups, w.num_heads, w.head_dim,
                               w.group_size, w.batch, w.context)
     gen = torch.Generator(device=dev)
     gen.manual_seed(1234 + rank)
-    R32 = None if args.hadamard else torch.from_numpy(synth.rotation(d).astype(np.float32)).to(dev)
-    Hq = args.query_heads or H   # grouped-query attention when Hq > H (the pages' models: Hq = H)
-    cfg = rq.rq_config(L, P, G, H, d, g, B, N + 64, (rq.RQ_MODE_CHAINED if args.chained else rq.RQ_MODE_SHARED)
-                       | (rq.RQ_MODE_HADAMARD if args.hadamard else 0), Hq)
-    if args.paged:
+    R32 = None if hadamard else torch.from_numpy(synth.rotation(d).astype(np.float32)).to(dev)
+    Hq = query_heads or H   # grouped-query attention when Hq > H (the pages' models: Hq = H)
+    cfg = rq.rq_config(L, P, G, H, d, g, B, N + 64, (rq.RQ_MODE_CHAINED if chained else rq.RQ_MODE_SHARED)
+                       | (rq.RQ_MODE_HADAMARD if hadamard else 0), Hq)
+    if paged:
         # every row's tiles on pages of a shuffled table (the pool holds exactly those pages)
         ntiles = -(-(N + 64) // 64)
         num_pages = B * ntiles
@@ -311,6 +317,7 @@ def run_rq(args, w):
         cache_buf = torch.empty(nbytes, dtype=torch.uint8, device=dev)
         handle = rq.rq_cache_create_paged(cfg, num_pages, cache_buf, nbytes, table, ntiles, R32)
     else:
+        table = None
         nbytes = rq.rq_cache_bytes(cfg)
         cache_buf = torch.empty(nbytes, dtype=torch.uint8, device=dev)
         handle = rq.rq_cache_create(cfg, cache_buf, nbytes, R32)
@@ -349,18 +356,17 @@ def run_rq(args, w):
             rq.rq_decode_attention(handle, layer, grp, lp, B, q_all[i], t[lp, 0, :, :, 0], t[lp, 1, :, :, 0],
                                    seq, scale, out_all[i], ws, ws_bytes, s.cuda_stream)
 
-    def step(stream=None):
+    def step():
         for i in range(ncalls):
             call(i)
 
-    launches_per_step = 3 * ncalls   # a call is qprep + decode + merge kernels (the append runs in the merge)
     torch.cuda.synchronize()
     with torch.cuda.stream(s):
-        step(s.cuda_stream)   # eager once (also sets kernel attributes before capture)
+        step()   # eager once (also sets kernel attributes before capture)
     torch.cuda.synchronize()
     graph = torch.cuda.CUDAGraph()
     with torch.cuda.graph(graph, stream=s):
-        step(s.cuda_stream)
+        step()
     torch.cuda.synchronize()
 
     # warm-up (replay() launches on the current stream: make it s, where the events are)
@@ -370,7 +376,7 @@ def run_rq(args, w):
     torch.cuda.synchronize()
     # timed region
     e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
-    with ClockSampler(local) as clk:
+    with ClockSampler(dev.index) as clk:
         if world > 1:
             torch.distributed.barrier()
         torch.cuda.synchronize()
@@ -393,7 +399,7 @@ def run_rq(args, w):
     # changes (a run of residual-loop calls, a run of anchor-loop calls): inside a run the
     # calls keep their programmatic-dependent overlap, as in the step, and a run's time
     # divided by its calls is the time per call.
-    byts = algorithmic_bytes_per_step(w, B, N, args.chained)
+    byts = algorithmic_bytes_per_step(w, B, N, chained)
     kinds = [lp < P - 1 for (lp, _, _) in order]
     bounds = [0] + [i for i in range(1, ncalls) if kinds[i] != kinds[i - 1]] + [ncalls]
     ev = [torch.cuda.Event(enable_timing=True) for _ in bounds]
@@ -416,55 +422,126 @@ def run_rq(args, w):
                     bytes_res += sum(byts["per_loop"][order[i][0]] for i in range(bounds[k], bounds[k + 1]))
                 else:
                     t_anchor, n_anchor = t_anchor + ms, n_anchor + n
+    peak, peak_kind = _peaks()
     # the dominant launch: a residual-loop call (shared: anchor + one residual plane;
     # chained: anchor + the planes down to the loop), bytes and time summed over those calls
     per_launch_bytes = bytes_res / n_res
     avg_launch_ms = t_res / n_res
-    peak, peak_kind = _peaks()
     achieved = per_launch_bytes / (avg_launch_ms / 1e3) / 1e9
     anchor_ms = t_anchor / n_anchor
     anchor_gbs = byts["call_anchor"] / (anchor_ms / 1e3) / 1e9
+    step_gbs = byts["step"] / (ms_step / 1e3) / 1e9
+    return {
+        "ms_step": ms_step, "clocks": clk.summary(), "prefill_s": prefill_s, "step_gbs": step_gbs,
+        "peak": peak, "peak_kind": peak_kind, "calls": ncalls,
+        "roofline": {"bound": "hbm", "achieved": achieved, "peak": peak, "unit": "GB/s", "frac": achieved / peak,
+                     "avg_launch_ms": avg_launch_ms, "bytes_per_launch": per_launch_bytes,
+                     "anchor_loop_call": {"avg_ms": anchor_ms, "bytes": byts["call_anchor"],
+                                          "includes_token_append": True, "achieved": anchor_gbs,
+                                          "frac": anchor_gbs / peak}},
+        "launches_per_step": 3 * ncalls,   # a call is qprep + decode + merge kernels (the append runs in the merge)
+        "gen": gen, "scale": scale,
+        "live": {"graph": graph, "stream": s, "q_all": q_all, "temp_all": temp_all, "out_all": out_all,
+                 "handle": handle, "cache_buf": cache_buf, "ws": ws, "table": table, "R": R32},
+    }
+
+
+def _release(t):
+    import torch
+    import decode_attention_rq_gb300 as rq
+    live = t.pop("live")
+    torch.cuda.synchronize()
+    rq.rq_cache_destroy(live["handle"])
+    live.clear()
+    torch.cuda.empty_cache()
+
+
+# The configurations the default run also times, each as a sub-record of the
+# JSON line: the two 16k-context batches of the Ouro throughput comparison and
+# the Huginn shape (head width 96, 55 heads, 8 loop groups of 4).
+EXTRA_CONFIGS = ("ouro16k_b2", "ouro16k_b4", "huginn")
+
+
+def _sub_record(args, name, dev, rank, world):
+    w = synth.WORKLOADS[name]
+    t = _time_step(args, w, dev, rank, world)
+    rec = {"config": _config(w), "ms_per_step": t["ms_step"],
+           "tokens_per_s": job_throughput(world, w.batch, t["ms_step"]),
+           "effective_gbps": t["step_gbs"], "frac_of_hbm_peak": t["step_gbs"] / t["peak"],
+           "roofline": dict(t["roofline"], kernel="rq_decode_attention, residual-loop call",
+                            peak_source=f"MEASURED_PEAKS.json hbm_gbs ({t['peak_kind']})"),
+           "gpu_launches": t["launches_per_step"] * args.steps, "clocks": t["clocks"]}
+    gen, scale = t["gen"], t["scale"]
+    _release(t)
+    if not args.no_bf16:
+        rec["bf16_comparator"] = bench_bf16(args, w, dev, gen, scale)
+        rec["speedup_vs_bf16"] = rec["bf16_comparator"]["ms_per_step_attention"] / rec["ms_per_step"]
+    return rec
+
+
+def run_rq(args, w):
+    import torch
+    world = int(os.environ.get("WORLD_SIZE", "1"))
+    rank = int(os.environ.get("RANK", "0"))
+    local = int(os.environ.get("LOCAL_RANK", "0"))
+    torch.cuda.set_device(local)
+    dev = torch.device("cuda", local)
+    if world > 1:
+        import torch.distributed as dist
+        dist.init_process_group("nccl")
+
+    B = w.batch
+    t = _time_step(args, w, dev, rank, world, args.chained, args.hadamard, args.paged, args.query_heads)
+    ms_step = t["ms_step"]
     traffic = None
     tp = os.path.join(ROOT, "profiles", "traffic_per_launch.json")
     if os.path.exists(tp):
         try:
             tj = json.load(open(tp))
-            if (tj.get("workload") == w.name and tj.get("batch") == B and tj.get("group_size") == g
+            if (tj.get("workload") == w.name and tj.get("batch") == B and tj.get("group_size") == w.group_size
                     and not args.chained and not args.hadamard and not args.paged and not args.query_heads
                     and tj.get("kernel_source_hash") == _kernel_hash()):
                 traffic = tj.get("bytes_per_launch")
         except Exception:
             traffic = None
 
-    step_gbs = byts["step"] / (ms_step / 1e3) / 1e9
+    peak = t["peak"]
     value = job_throughput(world, B, ms_step)
+    roof = t["roofline"]
     line = {
         "metric": METRIC, "value": value, "unit": "tokens/s", "n_gpus": world, "steps": args.steps,
         "warmup": args.warmup, "ms_per_step": ms_step, "higher_is_better": True, "scaling": "weak",
-        "vs_baseline": None, "dtype": "int32/fp32", "data": "synthetic", "config": _config(w, args.chained, args.hadamard, args.paged, args.query_heads),
-        "effective_gbps": step_gbs, "frac_of_hbm_peak": step_gbs / peak,
-        "roofline": {"bound": "hbm", "achieved": achieved, "peak": peak, "unit": "GB/s",
-                     "frac": achieved / peak, "traffic": traffic,
+        "vs_baseline": None, "dtype": "int32/fp32", "data": "synthetic",
+        "config": _config(w, args.chained, args.hadamard, args.paged, args.query_heads),
+        "effective_gbps": t["step_gbs"], "frac_of_hbm_peak": t["step_gbs"] / peak,
+        "roofline": {"bound": "hbm", "achieved": roof["achieved"], "peak": peak, "unit": "GB/s",
+                     "frac": roof["frac"], "traffic": traffic,
                      "kernel": "rq_decode_attention, residual-loop call (qprep_kernel + "
                                "decode_kernel<d, g, 1> + merge_kernel)",
-                     "peak_source": f"MEASURED_PEAKS.json hbm_gbs ({peak_kind})",
-                     "avg_launch_ms": avg_launch_ms, "bytes_per_launch": per_launch_bytes,
-                     "anchor_loop_call": {"avg_ms": anchor_ms, "bytes": byts["call_anchor"], "includes_token_append": True,
-                                          "achieved": anchor_gbs, "frac": anchor_gbs / peak}},
-        "gpu_launches": launches_per_step * args.steps,
-        "clocks": clk.summary(),
-        "prefill_s": prefill_s,
+                     "peak_source": f"MEASURED_PEAKS.json hbm_gbs ({t['peak_kind']})",
+                     "avg_launch_ms": roof["avg_launch_ms"], "bytes_per_launch": roof["bytes_per_launch"],
+                     "anchor_loop_call": roof["anchor_loop_call"]},
+        "gpu_launches": t["launches_per_step"] * args.steps,
+        "clocks": t["clocks"],
+        "prefill_s": t["prefill_s"],
     }
-    # BF16 comparator: the same 96 calls over uncompressed K/V
+    if not args.no_e2e:
+        live = t["live"]
+        line["e2e"] = bench_e2e(args, live["graph"], live["stream"], live["q_all"], live["temp_all"],
+                                live["out_all"], B)
+    gen, scale = t["gen"], t["scale"]
+    _release(t)
+    # BF16 comparator: the same calls over uncompressed K/V
     if not args.no_bf16 and not args.query_heads:   # the BF16 comparator is multi-head
         line["bf16_comparator"] = bench_bf16(args, w, dev, gen, scale)
         # whole compressed step (appends included) against the BF16 attention calls alone
         line["speedup_vs_bf16"] = line["bf16_comparator"]["ms_per_step_attention"] / ms_step
-    if not args.no_e2e:
-        line["e2e"] = bench_e2e(args, graph, s, q_all, temp_all, out_all, B)
+    if not args.no_configs and w.name == "ouro8k" and not (args.batch or args.group_size or args.layers
+                                                          or args.chained or args.hadamard or args.paged
+                                                          or args.query_heads):
+        line["configs"] = {name: _sub_record(args, name, dev, rank, world) for name in EXTRA_CONFIGS}
     if rank == 0 and not args.no_cpu and world == 1:
-        line["cpu_baseline"] = cpu_baseline(w, B, N, budget_s=15.0)
-    rq.rq_cache_destroy(handle)
+        line["cpu_baseline"] = cpu_baseline(w, B, w.context, budget_s=15.0)
     if rank == 0:
         print(json.dumps(line))
 
