@@ -259,8 +259,9 @@ rq_status rq_decode_attention_append(rq_cache* cache, int32_t layer, int32_t gro
 
 /* Size of the workspace built into the library for rq_decode_attention_noalloc
  * (2 MiB of device memory, held on every device that loads the library until
- * the process exits).  With 152 SMs, head_dim 128 and group size 32 it
- * covers batch * num_heads up to about 1100 (row, head) pairs. */
+ * the process exits).  With 152 SMs and head_dim 128 it covers batch *
+ * num_query_heads up to about 740 (row, head) pairs (split-K partials of
+ * 1040 B and a query pack of 1152 B per pair, plus 456 CTA partials). */
 #define RQ_NOALLOC_WORKSPACE_BYTES (2u * 1024u * 1024u)
 
 /* rq_decode_attention for callers that cannot allocate device memory.
@@ -280,7 +281,13 @@ rq_status rq_decode_attention_append(rq_cache* cache, int32_t layer, int32_t gro
  * `stream` before its kernel, then runs the same kernel as
  * rq_decode_attention.  All calls share the one array: calls that overlap
  * on the GPU (other streams, other host threads) race and give wrong
- * results, so serialize them.
+ * results, so serialize them.  On one stream the clear is an ordinary
+ * stream operation: it starts after the previous call's kernels have
+ * finished, so consecutive noalloc calls do not overlap their start with
+ * the previous call's tail the way rq_decode_attention calls with
+ * workspaces do.  The status copied to `status` is the current call's only
+ * (the clear zeroes the word first); a caller that wants to know whether
+ * any of several calls failed ORs the words it receives. */
  * Errors: as rq_decode_attention; WORKSPACE when the call needs more than
  * RQ_NOALLOC_WORKSPACE_BYTES (too many rows x heads for the built-in array;
  * use rq_decode_attention with a workspace of rq_decode_workspace_bytes). */
