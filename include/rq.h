@@ -287,7 +287,7 @@ rq_status rq_decode_attention_append(rq_cache* cache, int32_t layer, int32_t gro
  * the previous call's tail the way rq_decode_attention calls with
  * workspaces do.  The status copied to `status` is the current call's only
  * (the clear zeroes the word first); a caller that wants to know whether
- * any of several calls failed ORs the words it receives. */
+ * any of several calls failed ORs the words it receives.
  * Errors: as rq_decode_attention; WORKSPACE when the call needs more than
  * RQ_NOALLOC_WORKSPACE_BYTES (too many rows x heads for the built-in array;
  * use rq_decode_attention with a workspace of rq_decode_workspace_bytes). */
