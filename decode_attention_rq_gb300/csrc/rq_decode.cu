@@ -83,12 +83,19 @@ int pstride_for(int d) { return ((2 + 2 * d) + 3) / 4 * 4; }
 
 int decode_max_chained_loops() { return kMaxRes + 1; }
 
-// Workspace: status word (256 B slot) | partials (C + batch*H) x pstride floats | query packs.
+// Query heads per work unit: grouped-query caches take the heads of a KV head in
+// groups of 4 (or 2) through the multi-query kernel (rq_decode_gqa.cu).
+static int decode_qh(const Geom& g) { return g.qpk % 4 == 0 ? 4 : (g.qpk % 2 == 0 ? 2 : 1); }
+
+// Partial rows: the per-head kernel writes row cta + bh (at most 3 CTAs per SM);
+// the multi-query kernel row (cta + group) * qh + h (at most 2 CTAs per SM).
 static size_t partials_bytes(const Geom& g, int batch, int num_sms) {
-  const size_t C = (size_t)num_sms * kMaxCtasPerSm, bh = (size_t)batch * g.Hq;
+  const int qh = decode_qh(g);
+  const size_t C = (size_t)num_sms * (kMaxCtasPerSm > 2 * qh ? kMaxCtasPerSm : 2 * qh), bh = (size_t)batch * g.Hq;
   return ((C + bh) * pstride_for(g.d) * sizeof(float) + 255) / 256 * 256;
 }
 
+// Workspace: status word (256 B slot) | partials (C + batch*Hq) x pstride floats | query packs.
 size_t decode_workspace_bytes(const Geom& g, int batch, int num_sms) {
   const size_t bh = (size_t)batch * g.Hq;
   return 256 + partials_bytes(g, batch, num_sms) + bh * kPackWords * sizeof(uint32_t);
@@ -123,8 +130,16 @@ cudaError_t launch_decode(const rq_cache& c, int layer, int group, int loop, int
   a.group = group;
   a.batch = batch;
   a.res0 = loop;
+  a.qh = 1;
   a.qscale = scale * kLog2e;
   const int d = c.geom.d, gs = c.geom.g, n = c.num_sms;
+  // grouped-query attention: the query heads of a KV head in groups of 4 (or 2)
+  // per pass over its tiles
+  const int qh = decode_qh(c.geom);
+  if (qh > 1 && nres <= 1) {
+    a.qh = qh;
+    return launch_decode_gqa(a, n, nres, stream);
+  }
   if (d == 128 && gs == 32) return launch_d<128, 32>(a, n, nres, stream);
   if (d == 128 && gs == 16) return launch_d<128, 16>(a, n, nres, stream);
   if (d == 96 && gs == 32) return launch_d<96, 32>(a, n, nres, stream);

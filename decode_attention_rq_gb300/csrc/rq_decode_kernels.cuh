@@ -28,11 +28,15 @@ struct DecodeArgs {
   uint32_t* packs;       // [batch*H][kPackWords]: query operands of the scoring products
   int pstride;
   int layer, group, batch, res0;   // res0: first residual plane this loop reads
+  int qh;                          // query heads a work unit covers (1; grouped-query: 2 or 4)
   float qscale;                    // softmax_scale * log2(e)
 };
 
 // Chained calls that read 4 to 7 residual planes (rq_decode_chained.cu).
 cudaError_t launch_decode_long_chain(const DecodeArgs& a, int num_sms, int nres, cudaStream_t stream);
+// Grouped-query calls reading at most one residual plane, a.qh (2 or 4) query
+// heads per work unit (rq_decode_gqa.cu).
+cudaError_t launch_decode_gqa(const DecodeArgs& a, int num_sms, int nres, cudaStream_t stream);
 
 // Query operands per (row, query head): a header (two scales, the per-group sums
 // of the query and of the rotated query) then the f16 B-operand images of the
@@ -949,8 +953,8 @@ __global__ void __launch_bounds__(APPEND ? kAppendThreads : kMergeThreads, APPEN
   int before = 0, total = 0;
   for (int r = tid; r < B; r += NT) {
     const int nt = (clamp_len(a.seq_lens[r], a.g.Nmax) + UTOK - 1) / UTOK;
-    total += H * nt;
-    if (r < b) before += H * nt;
+    total += (H / a.qh) * nt;
+    if (r < b) before += (H / a.qh) * nt;
   }
   for (int off = 16; off > 0; off >>= 1) {
     sc += __shfl_xor_sync(0xffffffffu, sc, off);
@@ -977,7 +981,7 @@ __global__ void __launch_bounds__(APPEND ? kAppendThreads : kMergeThreads, APPEN
     return;
   }
   const Split split{U / Cn, U % Cn};
-  const int s0 = pre + h * ntb, s1 = s0 + ntb;
+  const int s0 = pre + (h / a.qh) * ntb, s1 = s0 + ntb;   // the units of h's head group
   const int c_lo = split.owner(s0), c_hi = split.owner(s1 - 1);
   const int nc = min(c_hi - c_lo + 1, kMaxContrib);
 
@@ -991,15 +995,20 @@ __global__ void __launch_bounds__(APPEND ? kAppendThreads : kMergeThreads, APPEN
   // warp 0 reads the (m, l) pairs
   constexpr int PF = 8;
   const bool acc_thread = tid < (NRES > 0 ? 2 * D : D);   // NT covers them (static_assert above)
-  const float* pc = a.partials + (size_t)(c_lo + bh) * a.pstride + 2 + tid;
+  // contributor i's partial for this head: row (c_lo + i + group) * qh + (h mod qh),
+  // group = the head's (row, head group) index (qh = 1: row c_lo + i + bh)
+  const int hgq = b * (H / a.qh) + h / a.qh;
+  const float* pbase = a.partials + ((size_t)(c_lo + hgq) * a.qh + h % a.qh) * a.pstride;
+  const size_t cstride = (size_t)a.qh * a.pstride;
+  const float* pc = pbase + 2 + tid;
   float xa[PF];
 #pragma unroll
-  for (int k = 0; k < PF; ++k) xa[k] = (acc_thread && k < nc) ? __ldcg(pc + (size_t)k * a.pstride) : 0.f;
+  for (int k = 0; k < PF; ++k) xa[k] = (acc_thread && k < nc) ? __ldcg(pc + (size_t)k * cstride) : 0.f;
   if (warp == 0) {
     // (m, l) of each contributor, read once: m parked in w_s, l in l_s
     float M = s_cur;
     for (int i = lane; i < nc; i += 32) {
-      const float2 ml = __ldcg(reinterpret_cast<const float2*>(a.partials + (size_t)(c_lo + i + bh) * a.pstride));
+      const float2 ml = __ldcg(reinterpret_cast<const float2*>(pbase + (size_t)i * cstride));
       w_s[i] = ml.x;
       l_s[i] = ml.y;
       M = fmaxf(M, ml.x);
@@ -1022,7 +1031,7 @@ __global__ void __launch_bounds__(APPEND ? kAppendThreads : kMergeThreads, APPEN
 #pragma unroll
     for (int k = 0; k < PF; ++k)
       if (k < nc) v = fmaf(w_s[k], xa[k], v);
-    for (int i = PF; i < nc; ++i) v = fmaf(w_s[i], __ldcg(pc + (size_t)i * a.pstride), v);
+    for (int i = PF; i < nc; ++i) v = fmaf(w_s[i], __ldcg(pc + (size_t)i * cstride), v);
     if (tid < D) va_s[tid] = fmaf(exp2f(s_cur - M), __bfloat162float(a.v_cur[(size_t)kvbh * D + tid]), v);
     else vr_s[tid - D] = v;
   }

@@ -22,7 +22,12 @@ pytestmark = pytest.mark.gpu
 ATOL = 2e-3
 
 
-@pytest.mark.parametrize("d,g,H,Hq,chained", [(128, 32, 2, 4, False), (128, 32, 2, 8, False), (96, 16, 3, 6, True)])
+# Hq / H = 2 and 4 run the multi-query kernel with two and four heads per work
+# unit, 8 with four heads in two groups; the chained case's loops 0 and 1 (three
+# and two residual planes) take the per-head kernel, its loops 2 and 3 the
+# multi-query one.
+@pytest.mark.parametrize("d,g,H,Hq,chained", [(128, 32, 2, 4, False), (128, 32, 2, 8, False), (96, 16, 3, 6, True),
+                                              (128, 16, 1, 8, False), (96, 32, 2, 8, False), (128, 32, 3, 6, True)])
 def test_grouped_query_attention(d, g, H, Hq, chained):
     case = Case(L=1, P=4, G=1, H=H, d=d, g=g, B=2, Nmax=256, seed=90, chained=chained, Hq=Hq)
     mha = Case(L=1, P=4, G=1, H=Hq, d=d, g=g, B=2, Nmax=256, seed=90, chained=chained)
