@@ -149,6 +149,11 @@ struct Cfg {
   static constexpr int UT = 2;                                    // layout tiles per work unit
   static constexpr int UTOK = UT * kTile;                         // tokens per work unit
   static constexpr int STAGE = UT * SUB;
+  // A stage holds each plane's UT tiles together: K anchor, V anchor, then per
+  // residual plane K and V (PA, PR bytes per plane); the unit's tiles of a plane
+  // are neighbours in the cache too, so one copy moves them
+  static constexpr int PA = UT * A_TILE;
+  static constexpr int PR = UT * R_TILE;
   // CTAs per SM: two while the registers allow; one from four residual planes up
   static constexpr int MINB = NRES <= 1 ? 3 : (NRES <= 3 ? 2 : 1);
   static constexpr int NITEM = NG * (1 + NRES);  // (plane, group) value-weight images
@@ -476,29 +481,35 @@ __global__ void __launch_bounds__(kThreads, (Cfg<D, GS, NRES>::MINB)) decode_ker
     const uint8_t* region = PAGED ? a.base : a.base + a.g.region_offset(a.layer, a.group, pc.b, kvh);
     uint8_t* dst = smem + stage * C::STAGE;
     mbar_arrive_expect_tx(&full_bar[stage], (uint32_t)(ntile * C::SUB));
-    for (int k = 0; k < ntile; ++k) {
-      uint8_t* d = dst + k * C::SUB;
-      const int tile = t0 + k;
-      const uint8_t* blk = region;   // paged: this head's block of the tile's page
-      if constexpr (PAGED) {
+    // plane slots of the stage: K anchor, V anchor, then K and V of each residual plane
+    auto slot = [&](bool anchor, int r, int kv) {
+      return dst + (anchor ? kv * C::PA : 2 * C::PA + (2 * r + kv) * C::PR);
+    };
+    if constexpr (PAGED) {
+      for (int k = 0; k < ntile; ++k) {   // a tile per page: one copy per plane and tile
         const int page = max(checked_page(a.g, next_raw_s[k], a.status), 0);   // a bad entry reads page 0
-        blk = a.base + (((int64_t)a.layer * a.g.G + a.group) * a.g.num_pages + page) * a.g.page_bytes +
-              (int64_t)kvh * a.g.head_block;
+        // this head's block of the tile's page (same offsets as Geom::tile_offset, sizes as constants)
+        const uint8_t* blk = a.base + (((int64_t)a.layer * a.g.G + a.group) * a.g.num_pages + page) * a.g.page_bytes +
+                             (int64_t)kvh * a.g.head_block;
+        bulk_g2s_hint(slot(true, 0, 0) + k * C::A_TILE, blk, C::A_TILE, &full_bar[stage], pol);
+        bulk_g2s_hint(slot(true, 0, 1) + k * C::A_TILE, blk + C::A_TILE, C::A_TILE, &full_bar[stage], pol);
+#pragma unroll
+        for (int r = 0; r < NRES; ++r) {
+          const uint8_t* rb = blk + 2 * C::A_TILE + 2 * (a.res0 + r) * C::R_TILE;
+          bulk_g2s_hint(slot(false, r, 0) + k * C::R_TILE, rb, C::R_TILE, &full_bar[stage], pol);
+          bulk_g2s_hint(slot(false, r, 1) + k * C::R_TILE, rb + C::R_TILE, C::R_TILE, &full_bar[stage], pol);
+        }
       }
-      auto src = [&](bool anchor, int j, int kv) {
-        if constexpr (PAGED)   // same offsets as Geom::tile_offset, with the tile sizes as constants
-          return blk + (anchor ? kv * C::A_TILE : 2 * C::A_TILE + (2 * j + kv) * C::R_TILE);
-        else
-          return region + (anchor ? a.g.anchor_plane(kv) : a.g.res_plane(j, kv)) +
-                 (int64_t)tile * (anchor ? C::A_TILE : C::R_TILE);
-      };
-      bulk_g2s_hint(d, src(true, 0, 0), C::A_TILE, &full_bar[stage], pol);
-      bulk_g2s_hint(d + C::A_TILE, src(true, 0, 1), C::A_TILE, &full_bar[stage], pol);
+    } else {   // the unit's tiles of a plane are contiguous: one copy per plane
+      const uint32_t na = (uint32_t)(ntile * C::A_TILE), nr = (uint32_t)(ntile * C::R_TILE);
+      bulk_g2s_hint(slot(true, 0, 0), region + a.g.anchor_plane(0) + (int64_t)t0 * C::A_TILE, na, &full_bar[stage], pol);
+      bulk_g2s_hint(slot(true, 0, 1), region + a.g.anchor_plane(1) + (int64_t)t0 * C::A_TILE, na, &full_bar[stage], pol);
 #pragma unroll
       for (int r = 0; r < NRES; ++r) {
-        uint8_t* d0 = d + 2 * C::A_TILE + 2 * r * C::R_TILE;
-        bulk_g2s_hint(d0, src(false, a.res0 + r, 0), C::R_TILE, &full_bar[stage], pol);
-        bulk_g2s_hint(d0 + C::R_TILE, src(false, a.res0 + r, 1), C::R_TILE, &full_bar[stage], pol);
+        bulk_g2s_hint(slot(false, r, 0), region + a.g.res_plane(a.res0 + r, 0) + (int64_t)t0 * C::R_TILE, nr,
+                      &full_bar[stage], pol);
+        bulk_g2s_hint(slot(false, r, 1), region + a.g.res_plane(a.res0 + r, 1) + (int64_t)t0 * C::R_TILE, nr,
+                      &full_bar[stage], pol);
       }
     }
     advance(pc);
@@ -635,14 +646,17 @@ __global__ void __launch_bounds__(kThreads, (Cfg<D, GS, NRES>::MINB)) decode_ker
     if (!mbar_wait_bounded(&full_bar[stage], (uint32_t)((it / STAGES) & 1))) aborted = true;
 
     const uint8_t* st = smem + stage * C::STAGE;
-    const uint8_t* sub = st + tau * C::SUB;   // the layout tile of this lane's tokens
+    // this lane's tokens: tile tau of each plane
+    const uint8_t* sak = st + tau * C::A_TILE;             // K anchor
+    const uint8_t* sav = st + C::PA + tau * C::A_TILE;     // V anchor
+    const uint8_t* sres = st + 2 * C::PA + tau * C::R_TILE;   // + (2 r + kv) PR: residual plane r
 
     // ---- scores of tokens tk0, tk1: tensor-core products over the K planes ----
     float sc0, sc1;
     {
       // anchor: this lane's words of the two token rows
       uint32_t wa0[C::WA], wa1[C::WA];
-      const uint8_t* ak = sub + r0 * (D / 2) + tig * (D / 8);
+      const uint8_t* ak = sak + r0 * (D / 2) + tig * (D / 8);
       if constexpr (C::WA == 4) {
         const uint4 x0 = *reinterpret_cast<const uint4*>(ak);
         const uint4 x1 = *reinterpret_cast<const uint4*>(ak + 2 * (D / 2));
@@ -671,7 +685,7 @@ __global__ void __launch_bounds__(kThreads, (Cfg<D, GS, NRES>::MINB)) decode_ker
       }
       // anchor score per token: sum over this lane's accumulators of s * (dot product) + o * sum(q)
       float sa0 = 0.f, sa1 = 0.f;
-      const uint8_t* am = sub + C::A_CODES + r0 * NG * 2;
+      const uint8_t* am = sak + C::A_CODES + r0 * NG * 2;
 #pragma unroll
       for (int ac = 0; ac < NACA; ++ac) {
         const int g = C::ga(tig, MA.rep[ac]);
@@ -686,7 +700,7 @@ __global__ void __launch_bounds__(kThreads, (Cfg<D, GS, NRES>::MINB)) decode_ker
         float cp0 = 1.f, cp1 = 1.f, sr0 = 0.f, sr1 = 0.f;
 #pragma unroll
         for (int r = 0; r < NRES; ++r) {
-          const uint8_t* rk = sub + 2 * C::A_TILE + 2 * r * C::R_TILE;
+          const uint8_t* rk = sres + 2 * r * C::PR;
           float dr[NACR][4];
 #pragma unroll
           for (int ac = 0; ac < NACR; ++ac) dr[ac][0] = dr[ac][1] = dr[ac][2] = dr[ac][3] = 0.f;
@@ -777,7 +791,7 @@ __global__ void __launch_bounds__(kThreads, (Cfg<D, GS, NRES>::MINB)) decode_ker
         float cp0 = p0, cp1 = p1;   // p times the coefficients of the planes before the current one
 #pragma unroll
         for (int r = 0; r < NRES; ++r) {
-          const uint8_t* rv = sub + 2 * C::A_TILE + (2 * r + 1) * C::R_TILE + C::R_CODES;
+          const uint8_t* rv = sres + (2 * r + 1) * C::PR + C::R_CODES;
           const float2 v0 = meta2(rv + r0 * NG * 2 + g * 2), v1 = meta2(rv + (r0 + 2) * NG * 2 + g * 2);
           if (ok0) off_part[1 + r][s] = fmaf(cp0, v0.y, off_part[1 + r][s]);
           if (ok1) off_part[1 + r][s] = fmaf(cp1, v1.y, off_part[1 + r][s]);
@@ -790,7 +804,7 @@ __global__ void __launch_bounds__(kThreads, (Cfg<D, GS, NRES>::MINB)) decode_ker
           if (ok0) cp0 *= bf16_bits_to_f32(*reinterpret_cast<const uint16_t*>(rc));
           if (ok1) cp1 *= bf16_bits_to_f32(*reinterpret_cast<const uint16_t*>(rc + 4));
         }
-        const uint8_t* am = sub + C::A_TILE + C::A_CODES;
+        const uint8_t* am = sav + C::A_CODES;
         const float2 a0 = meta2(am + r0 * NG * 2 + g * 2), a1 = meta2(am + (r0 + 2) * NG * 2 + g * 2);
         if (ok0) off_part[0][s] = fmaf(cp0, a0.y, off_part[0][s]);
         if (ok1) off_part[0][s] = fmaf(cp1, a1.y, off_part[0][s]);
@@ -809,7 +823,7 @@ __global__ void __launch_bounds__(kThreads, (Cfg<D, GS, NRES>::MINB)) decode_ker
       float dv[4] = {0.f, 0.f, 0.f, 0.f};
 #pragma unroll
       for (int t2 = 0; t2 < C::UT; ++t2) {
-        const uint8_t* av = st + t2 * C::SUB + C::A_TILE + vc0 * (kTile / 2) + tig * 8;
+        const uint8_t* av = st + C::PA + t2 * C::A_TILE + vc0 * (kTile / 2) + tig * 8;
         const uint2 y0 = *reinterpret_cast<const uint2*>(av);
         const uint2 y1 = *reinterpret_cast<const uint2*>(av + 8 * (kTile / 2));
         const uint32_t w0[2] = {y0.x, y0.y}, w1[2] = {y1.x, y1.y};
@@ -835,7 +849,7 @@ __global__ void __launch_bounds__(kThreads, (Cfg<D, GS, NRES>::MINB)) decode_ker
           const uint8_t* vbr = gid < 2 ? wimg + ((1 + r) * NG + vg) * kWItem + gid * kWPiece + tig * 8 : vzero + tig * 8;
 #pragma unroll
           for (int t2 = 0; t2 < C::UT; ++t2) {
-            const uint8_t* rvp = st + t2 * C::SUB + 2 * C::A_TILE + (2 * r + 1) * C::R_TILE + vc0 * (kTile / 4) + tig * 4;
+            const uint8_t* rvp = st + 2 * C::PA + (2 * r + 1) * C::PR + t2 * C::R_TILE + vc0 * (kTile / 4) + tig * 4;
             const uint32_t y0 = *reinterpret_cast<const uint32_t*>(rvp);
             const uint32_t y1 = *reinterpret_cast<const uint32_t*>(rvp + 8 * (kTile / 4));
             uint32_t x0[8], x1[8];
@@ -1031,7 +1045,16 @@ __global__ void __launch_bounds__(APPEND ? kAppendThreads : kMergeThreads, APPEN
 #pragma unroll
     for (int k = 0; k < PF; ++k)
       if (k < nc) v = fmaf(w_s[k], xa[k], v);
-    for (int i = PF; i < nc; ++i) v = fmaf(w_s[i], __ldcg(pc + (size_t)i * cstride), v);
+    // the rest in batches of PF independent loads (one L2 round trip per batch),
+    // summed in contributor order as above
+    for (int i0 = PF; i0 < nc; i0 += PF) {
+      float x[PF];
+#pragma unroll
+      for (int k = 0; k < PF; ++k) x[k] = i0 + k < nc ? __ldcg(pc + (size_t)(i0 + k) * cstride) : 0.f;
+#pragma unroll
+      for (int k = 0; k < PF; ++k)
+        if (i0 + k < nc) v = fmaf(w_s[i0 + k], x[k], v);
+    }
     if (tid < D) va_s[tid] = fmaf(exp2f(s_cur - M), __bfloat162float(a.v_cur[(size_t)kvbh * D + tid]), v);
     else vr_s[tid - D] = v;
   }
