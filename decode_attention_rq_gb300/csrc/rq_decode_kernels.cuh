@@ -385,7 +385,10 @@ __global__ void __launch_bounds__(kPrepThreads) qprep_kernel(DecodeArgs a) {
 
 // PAGED: the cache uses the block-table layout (tile addresses through the table).
 template <int D, int GS, int NRES, bool PAGED>
-__global__ void __launch_bounds__(kThreads, (Cfg<D, GS, NRES>::MINB)) decode_kernel(DecodeArgs a) {
+// Anchor-only calls: at most 72 registers, so that an append CTA of the merge
+// kernel (64 registers) fits beside three decode CTAs on an SM
+__global__ void __launch_bounds__(kThreads, (Cfg<D, GS, NRES>::MINB)) __maxnreg__(NRES == 0 ? 72 : 80)
+    decode_kernel(DecodeArgs a) {
   using C = Cfg<D, GS, NRES>;
   constexpr int NG = C::NG, STAGES = C::STAGES, NITEM = C::NITEM, UTOK = C::UTOK;
   constexpr int NMA = C::NMA, NMR = C::NMR, NACA = C::NACA, NACR = C::NACR, NIMG = C::NIMG, NGW = C::NGW;
@@ -891,10 +894,10 @@ __global__ void __launch_bounds__(kThreads, (Cfg<D, GS, NRES>::MINB)) decode_ker
 // APPEND (anchor-loop call only): the grid has two CTAs per (row, head); they
 // also compress the current token's K (first CTA, which also merges) and V
 // (second CTA) into the cache at position seq_lens[row] (rq_token_append.cuh).
-// They run 128 threads of at most 32 registers, small enough to sit beside the
-// decode kernel's CTAs and do that work while those stream.
+// They run 128 threads of at most 64 registers: one such CTA fits beside three
+// anchor-call decode CTAs (72 registers each) and does that work while they stream.
 template <int D, int NRES, bool APPEND>
-__global__ void __launch_bounds__(APPEND ? kAppendThreads : kMergeThreads, APPEND ? 16 : 0)
+__global__ void __launch_bounds__(APPEND ? kAppendThreads : kMergeThreads, APPEND ? 8 : 0)
     merge_kernel(DecodeArgs a, int Cn) {
   static_assert(!APPEND || NRES == 0, "append runs in the anchor-loop merge");
   constexpr int NT = APPEND ? kAppendThreads : kMergeThreads;

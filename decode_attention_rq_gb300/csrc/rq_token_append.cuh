@@ -134,7 +134,7 @@ __device__ __forceinline__ void rotate_chunk(const TokenAppendSmem& s, const flo
   }
 #pragma unroll
   for (int t = 0; t < NJ; ++t) u[t] = 0.f;
-#pragma unroll 4
+#pragma unroll 8
   for (int k4 = 0; k4 < D / 4; ++k4) {
     const float4 r = __ldg(Rrow + k4);
 #pragma unroll
