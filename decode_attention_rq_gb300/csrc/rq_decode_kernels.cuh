@@ -149,13 +149,25 @@ struct Cfg {
   static constexpr int UT = 2;                                    // layout tiles per work unit
   static constexpr int UTOK = UT * kTile;                         // tokens per work unit
   static constexpr int STAGE = UT * SUB;
-  // A stage holds each plane's UT tiles together: K anchor, V anchor, then per
-  // residual plane K and V (PA, PR bytes per plane); the unit's tiles of a plane
-  // are neighbours in the cache too, so one copy moves them
+  // Stage layout.  Contiguous cache: each plane's UT tiles together (K anchor,
+  // V anchor, then K and V of each residual plane; PA, PR bytes per plane), as
+  // a unit's tiles of a plane are neighbours in the cache: one copy per plane.
+  // Paged cache: tile by tile (SUB bytes), each tile's anchor pair and its
+  // residual planes being neighbours in the tile's page: two copies per tile.
   static constexpr int PA = UT * A_TILE;
   static constexpr int PR = UT * R_TILE;
+  template <bool PAGED> struct Lay {
+    static constexpr int TA = PAGED ? SUB : A_TILE;          // tile stride, anchor planes
+    static constexpr int AV = PAGED ? A_TILE : PA;           // V anchor of tile 0
+    static constexpr int RB = PAGED ? 2 * A_TILE : 2 * PA;   // K of residual plane 0, tile 0
+    static constexpr int TR = PAGED ? SUB : R_TILE;          // tile stride, residual planes
+    static constexpr int PL = PAGED ? R_TILE : PR;           // K to V, and plane to plane: 2 PL
+  };
   // CTAs per SM: two while the registers allow; one from four residual planes up
   static constexpr int MINB = NRES <= 1 ? 3 : (NRES <= 3 ? 2 : 1);
+  // registers a thread: the share of MINB CTAs (a multiple of 8, at most 255); anchor-only
+  // calls 72, leaving room for a token-append CTA of the merge kernel beside three CTAs
+  static constexpr int MAXREG = NRES == 0 ? 72 : (65536 / (256 * MINB) / 8 * 8 > 255 ? 255 : 65536 / (256 * MINB) / 8 * 8);
   static constexpr int NITEM = NG * (1 + NRES);  // (plane, group) value-weight images
   static constexpr int WIMG = NITEM * kWItem + 256;              // + a zero block for idle lanes
   static constexpr int STAGES = (MINB * (3 * STAGE + WIMG) + MINB * 8192 <= 224 * 1024) ? 3 : 2;
@@ -387,9 +399,10 @@ __global__ void __launch_bounds__(kPrepThreads) qprep_kernel(DecodeArgs a) {
 template <int D, int GS, int NRES, bool PAGED>
 // Anchor-only calls: at most 72 registers, so that an append CTA of the merge
 // kernel (64 registers) fits beside three decode CTAs on an SM
-__global__ void __launch_bounds__(kThreads, (Cfg<D, GS, NRES>::MINB)) __maxnreg__(NRES == 0 ? 72 : 80)
+__global__ void __launch_bounds__(kThreads, (Cfg<D, GS, NRES>::MINB)) __maxnreg__((Cfg<D, GS, NRES>::MAXREG))
     decode_kernel(DecodeArgs a) {
   using C = Cfg<D, GS, NRES>;
+  using LY = typename C::template Lay<PAGED>;
   constexpr int NG = C::NG, STAGES = C::STAGES, NITEM = C::NITEM, UTOK = C::UTOK;
   constexpr int NMA = C::NMA, NMR = C::NMR, NACA = C::NACA, NACR = C::NACR, NIMG = C::NIMG, NGW = C::NGW;
   constexpr typename C::AccMap MA = C::make_map(false), MR = C::make_map(true);
@@ -489,19 +502,16 @@ __global__ void __launch_bounds__(kThreads, (Cfg<D, GS, NRES>::MINB)) __maxnreg_
       return dst + (anchor ? kv * C::PA : 2 * C::PA + (2 * r + kv) * C::PR);
     };
     if constexpr (PAGED) {
-      for (int k = 0; k < ntile; ++k) {   // a tile per page: one copy per plane and tile
+      for (int k = 0; k < ntile; ++k) {   // a tile per page: anchor pair, then the residual planes read
         const int page = max(checked_page(a.g, next_raw_s[k], a.status), 0);   // a bad entry reads page 0
         // this head's block of the tile's page (same offsets as Geom::tile_offset, sizes as constants)
         const uint8_t* blk = a.base + (((int64_t)a.layer * a.g.G + a.group) * a.g.num_pages + page) * a.g.page_bytes +
                              (int64_t)kvh * a.g.head_block;
-        bulk_g2s_hint(slot(true, 0, 0) + k * C::A_TILE, blk, C::A_TILE, &full_bar[stage], pol);
-        bulk_g2s_hint(slot(true, 0, 1) + k * C::A_TILE, blk + C::A_TILE, C::A_TILE, &full_bar[stage], pol);
-#pragma unroll
-        for (int r = 0; r < NRES; ++r) {
-          const uint8_t* rb = blk + 2 * C::A_TILE + 2 * (a.res0 + r) * C::R_TILE;
-          bulk_g2s_hint(slot(false, r, 0) + k * C::R_TILE, rb, C::R_TILE, &full_bar[stage], pol);
-          bulk_g2s_hint(slot(false, r, 1) + k * C::R_TILE, rb + C::R_TILE, C::R_TILE, &full_bar[stage], pol);
-        }
+        uint8_t* d = dst + k * C::SUB;
+        bulk_g2s_hint(d, blk, 2 * C::A_TILE, &full_bar[stage], pol);
+        if constexpr (NRES > 0)
+          bulk_g2s_hint(d + 2 * C::A_TILE, blk + 2 * C::A_TILE + 2 * a.res0 * C::R_TILE, 2 * NRES * C::R_TILE,
+                        &full_bar[stage], pol);
       }
     } else {   // the unit's tiles of a plane are contiguous: one copy per plane
       const uint32_t na = (uint32_t)(ntile * C::A_TILE), nr = (uint32_t)(ntile * C::R_TILE);
@@ -650,9 +660,9 @@ __global__ void __launch_bounds__(kThreads, (Cfg<D, GS, NRES>::MINB)) __maxnreg_
 
     const uint8_t* st = smem + stage * C::STAGE;
     // this lane's tokens: tile tau of each plane
-    const uint8_t* sak = st + tau * C::A_TILE;             // K anchor
-    const uint8_t* sav = st + C::PA + tau * C::A_TILE;     // V anchor
-    const uint8_t* sres = st + 2 * C::PA + tau * C::R_TILE;   // + (2 r + kv) PR: residual plane r
+    const uint8_t* sak = st + tau * LY::TA;                 // K anchor
+    const uint8_t* sav = st + LY::AV + tau * LY::TA;        // V anchor
+    const uint8_t* sres = st + LY::RB + tau * LY::TR;       // + (2 r + kv) PL: residual plane r
 
     // ---- scores of tokens tk0, tk1: tensor-core products over the K planes ----
     float sc0, sc1;
@@ -703,7 +713,7 @@ __global__ void __launch_bounds__(kThreads, (Cfg<D, GS, NRES>::MINB)) __maxnreg_
         float cp0 = 1.f, cp1 = 1.f, sr0 = 0.f, sr1 = 0.f;
 #pragma unroll
         for (int r = 0; r < NRES; ++r) {
-          const uint8_t* rk = sres + 2 * r * C::PR;
+          const uint8_t* rk = sres + 2 * r * LY::PL;
           float dr[NACR][4];
 #pragma unroll
           for (int ac = 0; ac < NACR; ++ac) dr[ac][0] = dr[ac][1] = dr[ac][2] = dr[ac][3] = 0.f;
@@ -794,7 +804,7 @@ __global__ void __launch_bounds__(kThreads, (Cfg<D, GS, NRES>::MINB)) __maxnreg_
         float cp0 = p0, cp1 = p1;   // p times the coefficients of the planes before the current one
 #pragma unroll
         for (int r = 0; r < NRES; ++r) {
-          const uint8_t* rv = sres + (2 * r + 1) * C::PR + C::R_CODES;
+          const uint8_t* rv = sres + (2 * r + 1) * LY::PL + C::R_CODES;
           const float2 v0 = meta2(rv + r0 * NG * 2 + g * 2), v1 = meta2(rv + (r0 + 2) * NG * 2 + g * 2);
           if (ok0) off_part[1 + r][s] = fmaf(cp0, v0.y, off_part[1 + r][s]);
           if (ok1) off_part[1 + r][s] = fmaf(cp1, v1.y, off_part[1 + r][s]);
@@ -826,7 +836,7 @@ __global__ void __launch_bounds__(kThreads, (Cfg<D, GS, NRES>::MINB)) __maxnreg_
       float dv[4] = {0.f, 0.f, 0.f, 0.f};
 #pragma unroll
       for (int t2 = 0; t2 < C::UT; ++t2) {
-        const uint8_t* av = st + C::PA + t2 * C::A_TILE + vc0 * (kTile / 2) + tig * 8;
+        const uint8_t* av = st + LY::AV + t2 * LY::TA + vc0 * (kTile / 2) + tig * 8;
         const uint2 y0 = *reinterpret_cast<const uint2*>(av);
         const uint2 y1 = *reinterpret_cast<const uint2*>(av + 8 * (kTile / 2));
         const uint32_t w0[2] = {y0.x, y0.y}, w1[2] = {y1.x, y1.y};
@@ -852,7 +862,7 @@ __global__ void __launch_bounds__(kThreads, (Cfg<D, GS, NRES>::MINB)) __maxnreg_
           const uint8_t* vbr = gid < 2 ? wimg + ((1 + r) * NG + vg) * kWItem + gid * kWPiece + tig * 8 : vzero + tig * 8;
 #pragma unroll
           for (int t2 = 0; t2 < C::UT; ++t2) {
-            const uint8_t* rvp = st + 2 * C::PA + (2 * r + 1) * C::PR + t2 * C::R_TILE + vc0 * (kTile / 4) + tig * 4;
+            const uint8_t* rvp = st + LY::RB + (2 * r + 1) * LY::PL + t2 * LY::TR + vc0 * (kTile / 4) + tig * 4;
             const uint32_t y0 = *reinterpret_cast<const uint32_t*>(rvp);
             const uint32_t y1 = *reinterpret_cast<const uint32_t*>(rvp + 8 * (kTile / 4));
             uint32_t x0[8], x1[8];
