@@ -165,13 +165,16 @@ struct Cfg {
   };
   // CTAs per SM: two while the registers allow; one from four residual planes up
   static constexpr int MINB = NRES <= 1 ? 3 : (NRES <= 3 ? 2 : 1);
-  // registers a thread: the share of MINB CTAs (a multiple of 8, at most 255); anchor-only
-  // calls 72, leaving room for a token-append CTA of the merge kernel beside three CTAs
-  static constexpr int MAXREG = NRES == 0 ? 72 : (65536 / (256 * MINB) / 8 * 8 > 255 ? 255 : 65536 / (256 * MINB) / 8 * 8);
   static constexpr int NITEM = NG * (1 + NRES);  // (plane, group) value-weight images
   static constexpr int WIMG = NITEM * kWItem + 256;              // + a zero block for idle lanes
   static constexpr int STAGES = (MINB * (3 * STAGE + WIMG) + MINB * 8192 <= 224 * 1024) ? 3 : 2;
   static constexpr int SMEM = STAGES * STAGE + WIMG;
+  // CTAs per SM that the shared memory allows (MINB, or one fewer when MINB
+  // copies of SMEM and the static part do not fit)
+  static constexpr int FIT = (MINB * (SMEM + 8192) <= 228 * 1024 || MINB == 1) ? MINB : MINB - 1;
+  // registers a thread: the share of FIT CTAs (a multiple of 8, at most 255); anchor-only
+  // calls 72, leaving room for a token-append CTA of the merge kernel beside three CTAs
+  static constexpr int MAXREG = NRES == 0 ? 72 : (65536 / (256 * FIT) / 8 * 8 > 255 ? 255 : 65536 / (256 * FIT) / 8 * 8);
   // ---- scoring products (tokens x channels), per warp 16 tokens ----
   // anchor K: lane t holds words [t WA, (t+1) WA) of a token row (8 channels each);
   // product j takes registers 2j, 2j+1 of the lane (word j/2)
@@ -399,7 +402,7 @@ __global__ void __launch_bounds__(kPrepThreads) qprep_kernel(DecodeArgs a) {
 template <int D, int GS, int NRES, bool PAGED>
 // Anchor-only calls: at most 72 registers, so that an append CTA of the merge
 // kernel (64 registers) fits beside three decode CTAs on an SM
-__global__ void __launch_bounds__(kThreads, (Cfg<D, GS, NRES>::MINB)) __maxnreg__((Cfg<D, GS, NRES>::MAXREG))
+__global__ void __launch_bounds__(kThreads, (Cfg<D, GS, NRES>::FIT)) __maxnreg__((Cfg<D, GS, NRES>::MAXREG))
     decode_kernel(DecodeArgs a) {
   using C = Cfg<D, GS, NRES>;
   using LY = typename C::template Lay<PAGED>;
@@ -468,7 +471,9 @@ __global__ void __launch_bounds__(kThreads, (Cfg<D, GS, NRES>::MINB)) __maxnreg_
       }
     }
   };
-  Cursor pc = locate(u0);   // producer cursor (thread 0 only)
+  // producer cursor (thread 0 only), in shared memory: it costs the other threads no registers
+  __shared__ Cursor pc;
+  if (tid == 0) pc = locate(u0);
   const uint64_t pol = l2_evict_first_policy();   // the cache is read once per call
   // layout tiles of the producer's unit that hold tokens (the last unit of a row may have one)
   auto unit_tiles = [&]() { return min(C::UT, (sl_s[pc.b] - pc.t * C::UT * kTile + kTile - 1) / kTile); };
