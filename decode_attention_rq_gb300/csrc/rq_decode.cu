@@ -25,7 +25,11 @@
 //   * A unit's plane slices (anchor K/V, the residual K/V planes this loop
 //     reads) are contiguous and 16-byte aligned: one thread issues 1-D TMA
 //     bulk copies into a shared-memory ring tracked by mbarriers (bounded
-//     waits); all other threads only compute.
+//     waits).  Contiguous cache: a stage holds each plane's two tiles
+//     together, one copy per plane; paged cache: tile by tile, two copies per
+//     tile (the anchor pair, the residual planes read), neighbours in the
+//     tile's page.  Fewer copies matter: the issuing thread, also a consumer,
+//     stalls while the SM's copy engine is busy.
 //   * Scores use the rotated query: q.(c a_hat + R^T r_hat) = c (q.a_hat) +
 //     (R q).r_hat.  The value side accumulates the anchor part and the
 //     rotated residual part apart; R^T is applied once, in the merge.
@@ -48,8 +52,10 @@
 //     operands.  The tokens of a lane's two score rows (t, t + 2) are the
 //     pair one B register of the value products holds.
 //   * Online softmax in base 2 (scale * log2(e) folded into q).
-//   * Variants: grouped-query attention runs the units, the prep and the merge
-//     over (row, query head), each query head reading its KV head's tiles;
+//   * Variants: grouped-query attention runs the multi-query kernel
+//     (rq_decode_gqa.cu: a unit is (row, head group, 128 tokens), the tiles
+//     staged once for 2 or 4 query heads) for calls reading at most one
+//     residual plane, and per query head otherwise;
 //     the paged layout (decode_kernel<..., PAGED>) takes each tile's address
 //     from the block table, fetched one unit ahead by the producer thread;
 //     the Walsh-Hadamard mode replaces R q and R^T acc by the fast transform;
