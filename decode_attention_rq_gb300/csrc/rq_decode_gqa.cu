@@ -210,7 +210,7 @@ __global__ void __launch_bounds__(kThreads, 2) decode_gqa_kernel(DecodeArgs a) {
   // ---- per-segment state ----
   float m_run[QH], l_part[QH];
   float off_part[QH][1 + NRES][NGW];
-  float acc_a[4], acc_r[4];   // value accumulators of head tig (zero columns for tig >= QH)
+  float acc_a[4] = {0.f, 0.f, 0.f, 0.f}, acc_r[4] = {0.f, 0.f, 0.f, 0.f};   // head tig's value accumulators (zero columns for tig >= QH)
   int cur_bh = -1;            // current (row, head group)
   bool aborted = false;
   int fail_u = 0;

@@ -572,7 +572,7 @@ __global__ void __launch_bounds__(kThreads, (Cfg<D, GS, NRES>::FIT)) __maxnreg__
   uint32_t bq[NIMG];                 // B operands of the scoring products (query, rotated query)
   float sig_a = 0.f, sig_r = 0.f;
   float qa_own[NACA], qr_own[NACR];  // the offset sums of the groups this lane adds
-  float acc_a[4], acc_r[4];          // value accumulators (d0..d3 of the value products)
+  float acc_a[4] = {0.f, 0.f, 0.f, 0.f}, acc_r[4] = {0.f, 0.f, 0.f, 0.f};   // value accumulators (d0..d3 of the value products)
   float m_run = -INFINITY;
   float off_part[1 + NRES][NGW];     // partial offset sums of this lane's weight groups
   float l_part = 0.f;                // partial softmax denominator (lanes tig == 0)
