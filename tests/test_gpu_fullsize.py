@@ -48,6 +48,24 @@ def _cases():
     }
 
 
+def _gqa_cases():
+    """Grouped-query heads at the Ouro 8k batch-4 size: Hq query heads over the
+    16 KV heads (the multi-query kernel, 2 or 4 query heads per unit); samples
+    (layer, group, row, KV head, query head) with the query head on that KV head."""
+    W = synth.WORKLOADS
+    return {
+        "ouro8k_hq32": (W["ouro8k"], 32, [(0, 0, 1, 5, 11), (0, 0, 3, 12, 24)], 107),
+        "ouro8k_hq64": (W["ouro8k"], 64, [(0, 0, 0, 9, 39), (0, 0, 2, 15, 60)], 108),
+    }
+
+
+def _q_inputs(w, Hq, seed):
+    """Per loop: queries [B, Hq, d] (bf16, float64) and the current token's K/V per KV head."""
+    B, H, d = w.batch, w.num_heads, w.head_dim
+    return [(synth.queries(seed * 10 + loop, B, Hq, d), synth.queries(seed * 10 + 1000 + loop, B, H, d),
+             synth.queries(seed * 10 + 2000 + loop, B, H, d)) for loop in range(w.loops_per_group)]
+
+
 def _inputs(w, seed):
     """Per loop: queries and the current token's K/V for every (row, head): bf16 and float64."""
     B, H, d = w.batch, w.num_heads, w.head_dim
@@ -78,6 +96,16 @@ def oracle_results():
             args = (w, seed, layer, group, b, h, w.context, w.context + 64, int(seq[b]), chained, q, kc, vc,
                     synth.softmax_scale(w.head_dim))
             res[(name, layer, group, b, h)] = pool.apply_async(slice_job, (args,))
+    for name, (w, Hq, samples, seed) in _gqa_cases().items():
+        ins = _q_inputs(w, Hq, seed)
+        seq = _seq_lens(w)
+        for (layer, group, b, h, qh) in samples:
+            q = np.stack([ins[l][0][1][b, qh] for l in range(w.loops_per_group)])
+            kc = np.stack([ins[l][1][1][b, h] for l in range(w.loops_per_group)])
+            vc = np.stack([ins[l][2][1][b, h] for l in range(w.loops_per_group)])
+            args = (w, seed, layer, group, b, h, w.context, w.context + 64, int(seq[b]), False, q, kc, vc,
+                    synth.softmax_scale(w.head_dim))
+            res[(name, layer, group, b, h, qh)] = pool.apply_async(slice_job, (args,))
     pool.close()
     yield res
     pool.terminate()
@@ -159,3 +187,76 @@ def test_fullsize_sampled_parity(name, oracle_results):
             assert err <= ATOL, f"{name} {s} loop {loop}: max |gpu - oracle| = {err:.3e}"
     print(f"{name}: worst max-abs error {worst:.3e} over {len(samples)} slices x {w.loops_per_group} loops; "
           f"cache bytes equal")
+
+
+def _gqa_device_case(w, Hq, samples, seed):
+    import decode_attention_rq_gb300 as rq
+    dev = "cuda:0"
+    P, H, d, g, B, N = w.loops_per_group, w.num_heads, w.head_dim, w.group_size, w.batch, w.context
+    cap = N + 64
+    cfg = rq.rq_config(1, P, 1, H, d, g, B, cap, rq.RQ_MODE_SHARED, Hq)
+    nbytes = rq.rq_cache_bytes(cfg)
+    buf = torch.zeros(nbytes, dtype=torch.uint8, device=dev)
+    R = torch.from_numpy(synth.rotation(d).astype(np.float32)).to(dev)
+    handle = rq.rq_cache_create(cfg, buf, nbytes, R)
+    ws_bytes = rq.rq_decode_workspace_bytes(cfg, B)
+    ws = torch.zeros(ws_bytes, dtype=torch.uint8, device=dev)
+    status = ws[:16].view(torch.int32)
+    gen = torch.Generator(device=dev)
+    gen.manual_seed(seed)
+    slices = {s[:4]: synth.looped_kv_slice(seed, w, N, *s[:4])[0].to(dev) for s in samples}
+    for c0 in range(0, N, CHUNK):
+        n = min(CHUNK, N - c0)
+        kv = synth.looped_kv_torch(gen, w, B, n, dev)
+        for (layer, gg, b, h), t in slices.items():
+            kv[:, :, b, h] = t[:, :, c0:c0 + n]
+        seq = torch.full((B,), c0, dtype=torch.int32, device=dev)
+        rq.rq_append(handle, 0, 0, B, kv, seq, n, status)
+        del kv
+    torch.cuda.synchronize()
+    sl = torch.as_tensor(_seq_lens(w).astype(np.int32), device=dev)
+    scale = synth.softmax_scale(d)
+    ins = _q_inputs(w, Hq, seed)
+    kv_all = torch.stack([torch.stack([ins[l][1][0], ins[l][2][0]]) for l in range(P)]).to(dev).contiguous()
+    outs = {}
+    for loop in range(P):
+        (q, _), (kc, _), (vc, _) = ins[loop]
+        out = torch.empty((B, Hq, d), dtype=torch.float32, device=dev)
+        if loop < P - 1:
+            rq.rq_decode_attention(handle, 0, 0, loop, B, q.to(dev), kc.to(dev), vc.to(dev), sl, scale, out, ws,
+                                   ws_bytes)
+        else:
+            rq.rq_decode_attention_append(handle, 0, 0, B, q.to(dev), kv_all, sl, scale, out, ws, ws_bytes)
+        outs[loop] = out.cpu().numpy()
+    torch.cuda.synchronize()
+    assert status.tolist() == [0, 0, 0, 0]
+    geom = oracle.Geometry(1, P, 1, H, d, g, B, cap)
+    regions = {}
+    for s in samples:
+        off = geom.region_offset(*s[:4])
+        regions[s] = buf[off: off + geom.region].cpu().numpy()
+    rq.rq_cache_destroy(handle)
+    del buf, ws
+    torch.cuda.empty_cache()
+    return regions, outs
+
+
+@pytest.mark.parametrize("name", list(_gqa_cases()))
+def test_fullsize_grouped_query_sampled_parity(name, oracle_results):
+    """The multi-query kernel at the benchmark's size (every CTA takes several
+    units and crosses head-group boundaries): sampled (row, query head) outputs
+    of every loop within 2e-3 of the oracle, the KV head's region byte-equal
+    (the appended slot included)."""
+    w, Hq, samples, seed = _gqa_cases()[name]
+    regions, outs = _gqa_device_case(w, Hq, samples, seed)
+    worst = 0.0
+    for s in samples:
+        layer, group, b, h, qh = s
+        obuf, oout = oracle_results[(name,) + s].get(timeout=1800)
+        diff = int((regions[s] != obuf).sum())
+        assert diff == 0, f"{name} {s}: {diff} of {obuf.size} cache bytes differ"
+        for loop in range(w.loops_per_group):
+            err = float(np.abs(outs[loop][b, qh] - oout[loop]).max())
+            worst = max(worst, err)
+            assert err <= ATOL, f"{name} {s} loop {loop}: max |gpu - oracle| = {err:.3e}"
+    print(f"{name}: worst max-abs error {worst:.3e} over {len(samples)} slices x {w.loops_per_group} loops")

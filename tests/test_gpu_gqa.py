@@ -70,3 +70,4 @@ def test_grouped_query_attention(d, g, H, Hq, chained):
     assert np.array_equal(gbuf, obuf), f"{int((gbuf != obuf).sum())} cache bytes differ"
     assert gqa_dev.status.tolist() == [0, 0, 0, 0]
     print(f"GQA H={H} Hq={Hq} d={d} chained={chained}: worst max-abs error {worst:.3e}; cache bytes equal")
+
