@@ -1024,8 +1024,11 @@ __global__ void __launch_bounds__(APPEND ? kAppendThreads : kMergeThreads, APPEN
                             app_smem);
 
   // this thread's element of the first contributors' accumulators, loaded while
-  // warp 0 reads the (m, l) pairs
-  constexpr int PF = 8;
+  // warp 0 reads the (m, l) pairs.  16 in flight: a (row, head) of 128 units (16k
+  // tokens) at batch 2 has about 15 contributors, which then take one L2 round
+  // trip instead of two (8 in flight: ouro16k b2 step 3.25 ms, 16: 3.14 ms;
+  // 32 gave 3.21 ms, its registers costing more than the batch it saves).
+  constexpr int PF = 16;
   const bool acc_thread = tid < (NRES > 0 ? 2 * D : D);   // NT covers them (static_assert above)
   // contributor i's partial for this head: row (c_lo + i + group) * qh + (h mod qh),
   // group = the head's (row, head group) index (qh = 1: row c_lo + i + bh)
