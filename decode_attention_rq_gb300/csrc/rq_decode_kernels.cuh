@@ -976,6 +976,8 @@ __global__ void __launch_bounds__(APPEND ? kAppendThreads : kMergeThreads, APPEN
     mbar_arrive_expect_tx(&r_bar, (uint32_t)(D * D * sizeof(float)));
     bulk_g2s(R_s, a.R, (uint32_t)(D * D * sizeof(float)), &r_bar);
   }
+  // the current token's value element of this thread (an input: read before the wait)
+  const float vcur = tid < D ? __bfloat162float(a.v_cur[(size_t)kvbh * D + tid]) : 0.f;
   // current token's score (base 2)
   float sc = 0.f;
   for (int k = tid; k < D; k += NT)
@@ -1004,8 +1006,7 @@ __global__ void __launch_bounds__(APPEND ? kAppendThreads : kMergeThreads, APPEN
     if (NRES > 0 && !hadamard) (void)mbar_wait_bounded(&r_bar, 0);   // the R copy lands before the CTA exits
     pdl_wait();   // completion of this kernel implies the decode kernel's
     // written after the wait: the previous call's merge may still write its output
-    for (int k = tid; k < D; k += NT)
-      a.out[(size_t)bh * D + k] = __bfloat162float(a.v_cur[(size_t)kvbh * D + k]);
+    if (tid < D) a.out[(size_t)bh * D + tid] = vcur;
     if constexpr (APPEND)
       if (app_ok)
         token_append_store<D>(a.g, const_cast<uint8_t*>(a.base), a.layer, a.group, b, kvh, 0, app_pos, app_page,
@@ -1076,7 +1077,7 @@ __global__ void __launch_bounds__(APPEND ? kAppendThreads : kMergeThreads, APPEN
       for (int k = 0; k < PF; ++k)
         if (i0 + k < nc) v = fmaf(w_s[i0 + k], x[k], v);
     }
-    if (tid < D) va_s[tid] = fmaf(exp2f(s_cur - M), __bfloat162float(a.v_cur[(size_t)kvbh * D + tid]), v);
+    if (tid < D) va_s[tid] = fmaf(exp2f(s_cur - M), vcur, v);
     else vr_s[tid - D] = v;
   }
   __syncthreads();

@@ -17,7 +17,13 @@
  *     the library never allocates or frees device memory and never
  *     synchronizes the device.  Host pointers are marked "host".
  *   - `stream` is a cudaStream_t passed as void* (NULL = legacy default
- *     stream).  Work is enqueued asynchronously on it.
+ *     stream).  Work is enqueued asynchronously on it.  The decode calls
+ *     launch their kernels as programmatic dependents of the work before
+ *     them on the stream, and those kernels read their inputs (queries,
+ *     current K/V, seq_lens, cache) before waiting for it: a caller's
+ *     kernel that releases its dependents early (griddepcontrol.launch_
+ *     dependents) must have written those inputs before it does.  Kernels
+ *     launched without that release are complete before a call starts.
  *   - Argument errors are found on the host before anything is enqueued and
  *     return a status; nothing is launched then.  A failed launch returns
  *     RQ_ERR_CUDA.  Faults inside a kernel surface on a later CUDA call.
