@@ -288,16 +288,16 @@ __global__ void __launch_bounds__(kPrepThreads) qprep_kernel(DecodeArgs a) {
     }
   }
   // Launched as a programmatic dependent of whatever precedes the call on the
-  // stream: everything else read here (q) or written (the packs, which the
-  // previous call's decode kernel may still read) waits for that kernel.  The
-  // decode kernel is released at once: while the previous call drains, it
-  // splits the work and starts its first cache copies.  What it reads before
-  // its own wait (seq_lens, the cache) no kernel of this library writes while
-  // released early: the kernels that write the cache (the append kernel, the
-  // anchor-loop merge with the token append) release their dependents only when
-  // they complete, and a caller's kernel does so too.
+  // stream.  The query and R are inputs, complete before that work releases
+  // this kernel (the contract in rq.h), so the whole pack is built before the
+  // wait, while the previous call drains; only its write to the workspace
+  // (which the previous call's decode kernel may still read) waits.  The
+  // decode kernel is released at once: it splits the work and starts its
+  // first cache copies.  What it reads before its own wait (seq_lens, the
+  // cache) no kernel of this library writes while released early: the kernels
+  // that write the cache (the append kernel, the anchor-loop merge with the
+  // token append) release their dependents only when they complete.
   pdl_launch_dependents();
-  pdl_wait();
   if (tid < D) q_s[tid] = __bfloat162float(a.q[(size_t)bh * D + tid]) * a.qscale;
   if (tid < kPackHeader) pack_s[tid] = 0u;
   __syncthreads();
@@ -393,6 +393,7 @@ __global__ void __launch_bounds__(kPrepThreads) qprep_kernel(DecodeArgs a) {
     pack_s[kPackHeader + i] = v;
   }
   __syncthreads();
+  pdl_wait();   // the workspace's packs are free once the kernel ahead has finished
   uint4* dst = reinterpret_cast<uint4*>(a.packs + (size_t)bh * kPackWords);
   const uint4* src = reinterpret_cast<const uint4*>(pack_s);
   for (int i = tid; i < (kPackHeader + 8 * NIMG) / 4; i += kPrepThreads) dst[i] = src[i];
