@@ -919,14 +919,14 @@ __global__ void __launch_bounds__(APPEND ? kAppendThreads : kMergeThreads, APPEN
   constexpr int NT = APPEND ? kAppendThreads : kMergeThreads;
   static_assert(NRES == 0 ? NT >= D : NT >= 2 * D, "a thread per accumulator element");
   extern __shared__ __align__(16) float R_s[];   // [D][D] when NRES > 0; the append's scratch with APPEND
-  __shared__ float w_s[kMaxContrib];
-  __shared__ float l_s[kMaxContrib];
+  __shared__ float w_s[APPEND ? 1 : kMaxContrib];   // contributor weights (merge without the append)
+  __shared__ float l_s[APPEND ? 1 : kMaxContrib];
+  __shared__ float ml_s[2];
   __shared__ float va_s[D];
-  __shared__ float vr_s[D];
+  __shared__ __align__(16) float vr_s[D];
   __shared__ float rt_s[D];
   __shared__ float redf_s[NT / 32];
   __shared__ int redi_s[2][NT / 32];
-  __shared__ float ml_s[2];
   __shared__ uint64_t r_bar;
   constexpr int UTOK = 2 * kTile;
   // the next call's prep may start loading R (it waits for this kernel); the
@@ -1025,11 +1025,10 @@ __global__ void __launch_bounds__(APPEND ? kAppendThreads : kMergeThreads, APPEN
       token_append_store<D>(a.g, const_cast<uint8_t*>(a.base), a.layer, a.group, b, kvh, 0, app_pos, app_page,
                             app_smem);
 
-  // this thread's element of the first contributors' accumulators, loaded while
-  // warp 0 reads the (m, l) pairs.  16 in flight: a (row, head) of 128 units (16k
-  // tokens) at batch 2 has about 15 contributors, which then take one L2 round
-  // trip instead of two (8 in flight: ouro16k b2 step 3.25 ms, 16: 3.14 ms;
-  // 32 gave 3.21 ms, its registers costing more than the batch it saves).
+  // The combine, in batches of PF contributors (one L2 round trip per batch).
+  // PF = 16: a (row, head) of 128 units (16k tokens) at batch 2 has about 15
+  // contributors, one batch (8 in flight took two round trips there: ouro16k b2
+  // step 3.25 against 3.14 ms; 32 gave 3.21 ms).
   constexpr int PF = 16;
   const bool acc_thread = tid < (NRES > 0 ? 2 * D : D);   // NT covers them (static_assert above)
   // contributor i's partial for this head: row (c_lo + i + group) * qh + (h mod qh),
@@ -1038,48 +1037,86 @@ __global__ void __launch_bounds__(APPEND ? kAppendThreads : kMergeThreads, APPEN
   const float* pbase = a.partials + ((size_t)(c_lo + hgq) * a.qh + h % a.qh) * a.pstride;
   const size_t cstride = (size_t)a.qh * a.pstride;
   const float* pc = pbase + 2 + tid;
-  float xa[PF];
+  float L = 0.f;
+  if constexpr (APPEND) {
+    // Every warp combines the contributors itself: lane k reads contributor k's
+    // (m, l), the maximum and the softmax sum are taken across the lanes, and
+    // each lane's weight reaches the others by shuffles.  No shared memory for
+    // the weights: the CTA stays small enough to start beside the decode CTAs.
+    if (acc_thread) {   // whole warps (2D or D threads)
+      float M = s_cur, v = 0.f;   // running maximum; L and v are relative to it
+#pragma unroll 1
+      for (int i0 = 0; i0 < nc; i0 += PF) {
+        float x[PF];
 #pragma unroll
-  for (int k = 0; k < PF; ++k) xa[k] = (acc_thread && k < nc) ? __ldcg(pc + (size_t)k * cstride) : 0.f;
-  if (warp == 0) {
-    // (m, l) of each contributor, read once: m parked in w_s, l in l_s
-    float M = s_cur;
-    for (int i = lane; i < nc; i += 32) {
-      const float2 ml = __ldcg(reinterpret_cast<const float2*>(pbase + (size_t)i * cstride));
-      w_s[i] = ml.x;
-      l_s[i] = ml.y;
-      M = fmaxf(M, ml.x);
+        for (int k = 0; k < PF; ++k) x[k] = i0 + k < nc ? __ldcg(pc + (size_t)(i0 + k) * cstride) : 0.f;
+        const float2 ml = lane < PF && i0 + lane < nc
+                              ? __ldcg(reinterpret_cast<const float2*>(pbase + (size_t)(i0 + lane) * cstride))
+                              : make_float2(-INFINITY, 0.f);
+        float Mb = fmaxf(M, ml.x);
+        for (int off = 16; off > 0; off >>= 1) Mb = fmaxf(Mb, __shfl_xor_sync(0xffffffffu, Mb, off));
+        const float r = exp2f(M - Mb);
+        M = Mb;
+        const float wl = ml.x == -INFINITY ? 0.f : exp2f(ml.x - M);   // lane's contributor weight
+        float lsum = wl * ml.y;
+        for (int off = 16; off > 0; off >>= 1) lsum += __shfl_xor_sync(0xffffffffu, lsum, off);
+        L = fmaf(L, r, lsum);
+        v *= r;
+#pragma unroll
+        for (int k = 0; k < PF; ++k) v = fmaf(__shfl_sync(0xffffffffu, wl, k), x[k], v);   // contributor order
+      }
+      const float wc = exp2f(s_cur - M);   // the current token
+      L += wc;
+      if (tid < D) va_s[tid] = fmaf(wc, vcur, v);
+      else vr_s[tid - D] = v;
     }
-    for (int off = 16; off > 0; off >>= 1) M = fmaxf(M, __shfl_xor_sync(0xffffffffu, M, off));
-    float L = 0.f;
-    for (int i = lane; i < nc; i += 32) {
-      const float w = exp2f(w_s[i] - M);
-      w_s[i] = w;
-      L = fmaf(w, l_s[i], L);
+  } else {
+    // warp 0 reads the (m, l) pairs and parks the weights in shared memory while
+    // every thread loads its element of the first PF contributors' accumulators
+    float xa[PF];
+#pragma unroll
+    for (int k = 0; k < PF; ++k) xa[k] = (acc_thread && k < nc) ? __ldcg(pc + (size_t)k * cstride) : 0.f;
+    if (warp == 0) {
+      // (m, l) of each contributor, read once: m parked in w_s, l in l_s
+      float M = s_cur;
+      for (int i = lane; i < nc; i += 32) {
+        const float2 ml = __ldcg(reinterpret_cast<const float2*>(pbase + (size_t)i * cstride));
+        w_s[i] = ml.x;
+        l_s[i] = ml.y;
+        M = fmaxf(M, ml.x);
+      }
+      for (int off = 16; off > 0; off >>= 1) M = fmaxf(M, __shfl_xor_sync(0xffffffffu, M, off));
+      float L = 0.f;
+      for (int i = lane; i < nc; i += 32) {
+        const float w = exp2f(w_s[i] - M);
+        w_s[i] = w;
+        L = fmaf(w, l_s[i], L);
+      }
+      for (int off = 16; off > 0; off >>= 1) L += __shfl_xor_sync(0xffffffffu, L, off);
+      if (lane == 0) { ml_s[0] = M; ml_s[1] = L + exp2f(s_cur - M); }
     }
-    for (int off = 16; off > 0; off >>= 1) L += __shfl_xor_sync(0xffffffffu, L, off);
-    if (lane == 0) { ml_s[0] = M; ml_s[1] = L + exp2f(s_cur - M); }
-  }
-  __syncthreads();
-  const float M = ml_s[0], L = ml_s[1];
-  // thread = (channel, anchor | residual accumulator)
-  if (acc_thread) {
-    float v = 0.f;
-#pragma unroll
-    for (int k = 0; k < PF; ++k)
-      if (k < nc) v = fmaf(w_s[k], xa[k], v);
-    // the rest in batches of PF independent loads (one L2 round trip per batch),
-    // summed in contributor order as above
-    for (int i0 = PF; i0 < nc; i0 += PF) {
-      float x[PF];
-#pragma unroll
-      for (int k = 0; k < PF; ++k) x[k] = i0 + k < nc ? __ldcg(pc + (size_t)(i0 + k) * cstride) : 0.f;
+    __syncthreads();
+    const float M = ml_s[0];
+    L = ml_s[1];
+    // thread = (channel, anchor | residual accumulator)
+    if (acc_thread) {
+      float v = 0.f;
 #pragma unroll
       for (int k = 0; k < PF; ++k)
-        if (i0 + k < nc) v = fmaf(w_s[i0 + k], x[k], v);
+        if (k < nc) v = fmaf(w_s[k], xa[k], v);
+      // the rest in batches of PF independent loads (one L2 round trip per batch),
+      // summed in contributor order as above
+      for (int i0 = PF; i0 < nc; i0 += PF) {
+        float x[PF];
+#pragma unroll
+        for (int k = 0; k < PF; ++k) x[k] = i0 + k < nc ? __ldcg(pc + (size_t)(i0 + k) * cstride) : 0.f;
+#pragma unroll
+        for (int k = 0; k < PF; ++k)
+          if (i0 + k < nc) v = fmaf(w_s[i0 + k], x[k], v);
+      }
+      if (tid < D) va_s[tid] = fmaf(exp2f(s_cur - M), vcur, v);
+      else vr_s[tid - D] = v;
     }
-    if (tid < D) va_s[tid] = fmaf(exp2f(s_cur - M), vcur, v);
-    else vr_s[tid - D] = v;
   }
   __syncthreads();
   float o = 0.f;
@@ -1102,10 +1139,11 @@ __global__ void __launch_bounds__(APPEND ? kAppendThreads : kMergeThreads, APPEN
       float t0 = 0.f, t1 = 0.f, t2 = 0.f, t3 = 0.f;
 #pragma unroll 4
       for (int k = 0; k < D / 2; k += 4) {
-        t0 = fmaf(rc[(k + 0) * D], vr[k + 0], t0);
-        t1 = fmaf(rc[(k + 1) * D], vr[k + 1], t1);
-        t2 = fmaf(rc[(k + 2) * D], vr[k + 2], t2);
-        t3 = fmaf(rc[(k + 3) * D], vr[k + 3], t3);
+        const float4 x = *reinterpret_cast<const float4*>(vr + k);
+        t0 = fmaf(rc[(k + 0) * D], x.x, t0);
+        t1 = fmaf(rc[(k + 1) * D], x.y, t1);
+        t2 = fmaf(rc[(k + 2) * D], x.z, t2);
+        t3 = fmaf(rc[(k + 3) * D], x.w, t3);
       }
       o = (t0 + t1) + (t2 + t3);
       if (hh == 1) rt_s[c] = o;
