@@ -13,11 +13,12 @@
 //     scoring products use.  decode_kernel streams the cache and writes one partial
 //     softmax state per (CTA, segment).  merge_kernel (one CTA per (row,
 //     head)) combines the partials, adds the current BF16 token, applies R^T
-//     once and writes the output.  decode_kernel and merge_kernel are
-//     launched as programmatic dependents of the kernel before them: their
-//     prologues (work split, first cache copies; R staged in shared memory)
-//     overlap that kernel, and each waits for it (griddepcontrol.wait) only
-//     before reading what it wrote.
+//     once and writes the output.  All three are launched as programmatic
+//     dependents of the kernel before them: what needs only the call's inputs
+//     (the prep's whole query pack; the decode kernel's work split and first
+//     cache copies; the merge's R in shared memory and current token) overlaps
+//     that kernel, and each waits for it (griddepcontrol.wait) only before
+//     reading what it wrote or writing what it may still read.
 //   * Work units are (row, head, 128 tokens).  A fixed grid of
 //     num_SMs x (CTAs resident per SM) takes equal contiguous ranges of the flattened
 //     unit list (ranges cross (row, head) boundaries), so every SM streams
