@@ -207,18 +207,22 @@ def run_reference(args, w):
     budget = args.ref_budget or max(0.2, min(2.0, 150.0 / (args.steps + args.warmup)))
     smp = OracleSample(w, w.context)
     per_step = smp.row_calls_per_step(w.batch)
+    # A step of this arm is a bounded sample of the decode step (about `budget`
+    # seconds of its (row, head) attention calls): ms_per_step is the sample's
+    # own time, and the throughput counts the fraction of a decode step done.
     times, total_n, total_s = [], 0, 0.0
     for i in range(args.warmup + args.steps):
         n, el = smp.run(budget)
         if i >= args.warmup:
-            times.append(el / n * per_step)
+            times.append(el)
             total_n += n
             total_s += el
     ms = 1000 * statistics.mean(times)
-    val = w.batch / (ms / 1000)
+    val = w.batch * (total_n / per_step) / total_s
     sample = (f"each step: about {budget:.2f} s of (row, head) attention calls at {w.context} tokens "
-              f"(float64 NumPy rebuild from the cache bytes + softmax), extrapolated to {per_step} row-calls; "
-              f"{total_n} row-calls in {total_s:.1f} s over the timed steps")
+              f"(float64 NumPy rebuild from the cache bytes + softmax) out of the {per_step} row-calls "
+              f"of a decode step; {total_n} row-calls in {total_s:.1f} s over the timed steps "
+              f"(a whole decode step would take {per_step * total_s / total_n:.0f} s)")
     line = {"metric": METRIC, "value": val, "unit": "tokens/s", "impl": "reference", "n_gpus": args.gpus,
             "steps": args.steps, "warmup": args.warmup, "ms_per_step": ms, "higher_is_better": True,
             "scaling": "weak", "vs_baseline": None, "dtype": "f64", "data": "synthetic",
