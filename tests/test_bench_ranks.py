@@ -73,3 +73,25 @@ def test_algorithmic_bytes_follow_the_record_sizes():
     chained = bench.algorithmic_bytes_per_step(w, B, N, chained=True)
     assert chained["per_loop"][0] == 2 * (72 + 3 * 42) * N * rows + small
     assert chained["per_loop"][2] == shared["per_loop"][2]
+
+
+def test_reference_arm_step_is_the_timed_sample(monkeypatch, capsys):
+    """The reference arm's step is one bounded oracle sample: its ms_per_step is
+    the sample's own time (steps x ms_per_step fits the run's clock), and its
+    tokens/s counts the fraction of a decode step the samples covered."""
+    import json
+    import time
+    import types
+
+    import synth
+    monkeypatch.setenv("RANK", "0")
+    w = synth.WORKLOADS["toy"]
+    args = types.SimpleNamespace(ref_budget=0.05, steps=3, warmup=1, gpus=1, chained=False)
+    t0 = time.perf_counter()
+    bench.run_reference(args, w)
+    wall_ms = (time.perf_counter() - t0) * 1e3
+    line = json.loads(capsys.readouterr().out.strip().splitlines()[-1])
+    assert line["impl"] == "reference" and line["steps"] == 3
+    assert 0 < line["ms_per_step"] * line["steps"] <= wall_ms
+    assert line["value"] > 0 and line["cpu_baseline"]["value"] == line["value"]
+    assert line["e2e"]["h2d_bytes_per_step"] == 0 and line["e2e"]["value"] == line["value"]
