@@ -919,8 +919,8 @@ __global__ void __launch_bounds__(APPEND ? kAppendThreads : kMergeThreads, APPEN
   constexpr int NT = APPEND ? kAppendThreads : kMergeThreads;
   static_assert(NRES == 0 ? NT >= D : NT >= 2 * D, "a thread per accumulator element");
   extern __shared__ __align__(16) float R_s[];   // [D][D] when NRES > 0; the append's scratch with APPEND
-  __shared__ float w_s[APPEND ? 1 : kMaxContrib];   // contributor weights (merge without the append)
-  __shared__ float l_s[APPEND ? 1 : kMaxContrib];
+  __shared__ float w_s[NRES == 0 ? 1 : kMaxContrib];   // contributor weights (residual-loop merges)
+  __shared__ float l_s[NRES == 0 ? 1 : kMaxContrib];
   __shared__ float ml_s[2];
   __shared__ float va_s[D];
   __shared__ __align__(16) float vr_s[D];
@@ -1038,11 +1038,14 @@ __global__ void __launch_bounds__(APPEND ? kAppendThreads : kMergeThreads, APPEN
   const size_t cstride = (size_t)a.qh * a.pstride;
   const float* pc = pbase + 2 + tid;
   float L = 0.f;
-  if constexpr (APPEND) {
-    // Every warp combines the contributors itself: lane k reads contributor k's
-    // (m, l), the maximum and the softmax sum are taken across the lanes, and
-    // each lane's weight reaches the others by shuffles.  No shared memory for
-    // the weights: the CTA stays small enough to start beside the decode CTAs.
+  if constexpr (NRES == 0) {
+    // Anchor-loop merges, with and without the append (the two must agree bit
+    // for bit): every warp combines the contributors itself.  Lane k reads
+    // contributor k's (m, l), the maximum and the softmax sum are taken across
+    // the lanes, and each lane's weight reaches the others by shuffles.  No
+    // shared memory for the weights: the appending CTA stays small enough to
+    // start beside the decode CTAs.  (In the residual-loop merge, eight warps
+    // redoing this cost more than the barrier it saves.)
     if (acc_thread) {   // whole warps (2D or D threads)
       float M = s_cur, v = 0.f;   // running maximum; L and v are relative to it
 #pragma unroll 1

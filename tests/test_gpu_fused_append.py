@@ -107,3 +107,42 @@ def test_fused_call_empty_rows_and_capacity():
     assert np.array_equal(gbuf, obuf), f"{int((gbuf != obuf).sum())} cache bytes differ"
     st = gpu.status.cpu().numpy()
     assert st[0] == 0 and st[1] == 1
+
+
+@pytest.mark.parametrize("chained", [False, True])
+def test_fused_call_with_many_partials_per_head(chained):
+    """Long rows at batch 1: every 128-token unit has its own decode CTA, so a
+    (row, head) has 24 partial states, more than the merge combines in one
+    batch.  The fused call still equals rq_decode_attention + rq_append bit for
+    bit, and the oracle within 2e-3 (every cache byte equal)."""
+    case = Case(L=1, P=4, G=1, H=2, d=128, g=32, B=1, Nmax=3200, chained=chained, seed=71)
+    R32, R = rotation32(128)
+    sep, fused = GpuCache(case, R32), GpuCache(case, R32)
+    geom = _geom(case)
+    obuf = np.zeros(geom.total_bytes, dtype=np.uint8)
+    start = np.array([0], dtype=np.int64)
+    n0 = 3050                                   # 24 units: 23 full, one of 106 tokens
+    kvb, kv = kv_for(case, 72, n0)
+    for c in (sep, fused):
+        c.append(0, 0, kvb, start)
+    oracle.append(obuf, geom, R, 0, 0, kv, start, chained=chained)
+    seq = start + n0
+    scale = 1.0 / math.sqrt(128)
+    for step in range(2):
+        kvb_c, kv_c = kv_for(case, 300 + step, 1)
+        qb, q = synth.queries(400 + step, 1, 2, 128)
+        out_s = sep.decode(0, 0, 3, qb, kvb_c[3, 0, :, :, 0], kvb_c[3, 1, :, :, 0], seq, scale)
+        sep.append(0, 0, kvb_c, seq)
+        out_f = fused.decode_append(0, 0, qb, kvb_c[..., 0, :], seq, scale)
+        ref, ok = oracle.decode_attention_append(obuf, geom, R, 0, 0, q, kv_c[..., 0, :], seq, scale,
+                                                 chained=chained)
+        assert ok.all()
+        o_s, o_f = out_s.cpu().numpy(), out_f.cpu().numpy()
+        assert np.array_equal(o_s, o_f), f"step {step}: fused output differs from the two calls"
+        err = float(np.abs(o_f - ref).max())
+        assert err <= ATOL, f"step {step}: max |gpu - oracle| = {err:.3e}"
+        g_f = fused.bytes_host()
+        assert np.array_equal(sep.bytes_host(), g_f)
+        assert np.array_equal(g_f, obuf), f"step {step}: {int((g_f != obuf).sum())} bytes differ from the oracle"
+        seq = seq + 1
+    assert fused.status.tolist() == [0, 0, 0, 0]
