@@ -20,10 +20,12 @@
  *     stream).  Work is enqueued asynchronously on it.  The decode calls
  *     launch their kernels as programmatic dependents of the work before
  *     them on the stream, and those kernels read their inputs (queries,
- *     current K/V, seq_lens, cache) before waiting for it: a caller's
- *     kernel that releases its dependents early (griddepcontrol.launch_
- *     dependents) must have written those inputs before it does.  Kernels
- *     launched without that release are complete before a call starts.
+ *     current K/V, seq_lens, cache) before waiting for it.  A kernel that
+ *     does not release its dependents early (no griddepcontrol.launch_
+ *     dependents) has completed before a call starts, so any such kernel may
+ *     write the inputs; a kernel that does release early must not be the one
+ *     that writes them (its writes are visible only to a kernel that has
+ *     waited for it).
  *   - Argument errors are found on the host before anything is enqueued and
  *     return a status; nothing is launched then.  A failed launch returns
  *     RQ_ERR_CUDA.  Faults inside a kernel surface on a later CUDA call.
