@@ -472,3 +472,25 @@ def test_residual_codes_against_the_float64_reading(d, g):
                 assert np.array_equal(gv[nm], ov[nm]), f"anchor plane {nm} differs (b={b}, h={h})"
     stats = check_residual_parity(gbuf, ob64, geom, comp["u"], 0, 0, n, case.B, case.H)
     print(f"d={d} g={g} against the float64 reading: {stats}")
+
+
+@pytest.mark.parametrize("chained", [False, True])
+def test_decode_with_many_partials_per_head(chained):
+    """Long rows at batch 1: every 128-token unit has its own decode CTA, so each
+    (row, head) has 24 partial states and the merge combines them in two
+    batches.  Every loop within 2e-3 of the oracle; repeated calls equal."""
+    case = Case(L=1, P=4, G=1, H=2, d=128, g=32, B=1, Nmax=3200, seed=19, chained=chained)
+    n = 3050                                   # 24 units: 23 full, one of 106 tokens
+    gpu, geom, obuf, R, _ = _build_both(case, chunks=[n])
+    assert np.array_equal(gpu.bytes_host(), obuf)
+    scale = 1.0 / math.sqrt(128)
+    seq = np.full(1, n)
+    for loop in range(4):
+        qb, q, kcb, kc, vcb, vc = _queries(case, 20, loop)
+        out = gpu.decode(0, 0, loop, qb, kcb, vcb, seq, scale)
+        again = gpu.decode(0, 0, loop, qb, kcb, vcb, seq, scale)
+        assert torch.equal(out, again)
+        ref = oracle.decode_attention(obuf, geom, R, 0, 0, loop, q, kc, vc, seq, scale, chained=chained)
+        err = float(np.abs(out.cpu().numpy() - ref).max())
+        assert err <= ATOL, f"loop {loop}: max abs err {err:.3e}"
+    assert gpu.status.tolist() == [0, 0, 0, 0]
