@@ -400,11 +400,13 @@ __global__ void __launch_bounds__(kPrepThreads) qprep_kernel(DecodeArgs a) {
 }
 
 // PAGED: the cache uses the block-table layout (tile addresses through the table).
-template <int D, int GS, int NRES, bool PAGED>
 // Anchor-only calls: at most 72 registers, so that an append CTA of the merge
-// kernel (64 registers) fits beside three decode CTAs on an SM
-__global__ void __launch_bounds__(kThreads, (Cfg<D, GS, NRES>::FIT)) __maxnreg__((Cfg<D, GS, NRES>::MAXREG))
-    decode_kernel(DecodeArgs a) {
+// kernel (64 registers) fits beside three decode CTAs on an SM; LEAN (64
+// registers) leaves room for two, for anchor-loop calls with more append CTAs
+// than SMs (their second wave would otherwise wait for the decode kernel).
+template <int D, int GS, int NRES, bool PAGED, bool LEAN = false>
+__global__ void __launch_bounds__(kThreads, (Cfg<D, GS, NRES>::FIT))
+    __maxnreg__((LEAN ? 64 : Cfg<D, GS, NRES>::MAXREG)) decode_kernel(DecodeArgs a) {
   using C = Cfg<D, GS, NRES>;
   using LY = typename C::template Lay<PAGED>;
   constexpr int NG = C::NG, STAGES = C::STAGES, NITEM = C::NITEM, UTOK = C::UTOK;
@@ -1162,6 +1164,7 @@ cudaError_t launch_t(const DecodeArgs& a, int num_sms, cudaStream_t stream) {
   using C = Cfg<D, GS, NRES>;
   auto k = decode_kernel<D, GS, NRES, PAGED>;
   auto km = merge_kernel<D, (NRES > 0 ? 1 : 0), false>;
+  const int bhs = a.batch * a.g.Hq;   // (row, query head) pairs
   size_t km_smem = NRES > 0 ? (size_t)D * D * sizeof(float) : 0;
   if (a.g.mode & RQ_MODE_HADAMARD) km_smem = 0;   // no R to stage
   int km_threads = kMergeThreads, km_extra = 0;
@@ -1171,6 +1174,11 @@ cudaError_t launch_t(const DecodeArgs& a, int num_sms, cudaStream_t stream) {
       km_smem = TokenAppendSmem::bytes(a.g.P);
       km_threads = kAppendThreads;
       km_extra = a.batch * a.g.H;   // the V-coding CTAs, one per (row, KV head)
+      // more append CTAs than SMs: the lean decode kernel lets two sit beside its
+      // three CTAs per SM (ouro8k batch 8: anchor-loop call 45.2 -> 42.6 us; the
+      // Huginn shape, 220 CTAs: 31.2 -> 25.2 us; at 128 CTAs the 72-register
+      // kernel is 1 % faster)
+      if (bhs + km_extra > num_sms) k = decode_kernel<D, GS, 0, PAGED, true>;
     }
   constexpr size_t merge_smem = NRES > 0 ? (size_t)D * D * sizeof(float) : 0;
   // Kernel attributes are per device: they are set, and the resident decode CTAs
@@ -1183,16 +1191,25 @@ cudaError_t launch_t(const DecodeArgs& a, int num_sms, cudaStream_t stream) {
   if (dev < 0 || dev >= kMaxDevices) return cudaErrorInvalidDevice;
   int per_sm = per_sm_dev[dev].load(std::memory_order_acquire);
   if (per_sm == 0) {
+    auto k0 = decode_kernel<D, GS, NRES, PAGED>;   // the lean variant is set up beside it
     // the stages and the kernel's own shared memory must fit one CTA's limit
     int optin = 0;
     e0 = cudaDeviceGetAttribute(&optin, cudaDevAttrMaxSharedMemoryPerBlockOptin, dev);
     if (e0 != cudaSuccess) return e0;
     cudaFuncAttributes fa;
-    e0 = cudaFuncGetAttributes(&fa, k);
+    e0 = cudaFuncGetAttributes(&fa, k0);
     if (e0 != cudaSuccess) return e0;
     if ((size_t)C::SMEM + fa.sharedSizeBytes > (size_t)optin) return cudaErrorNotSupported;
-    cudaError_t e = cudaFuncSetAttribute(k, cudaFuncAttributeMaxDynamicSharedMemorySize, C::SMEM);
+    cudaError_t e = cudaFuncSetAttribute(k0, cudaFuncAttributeMaxDynamicSharedMemorySize, C::SMEM);
     if (e != cudaSuccess) return e;
+    if constexpr (NRES == 0) {   // both anchor-only decode kernels (same shared memory)
+      e = cudaFuncSetAttribute(decode_kernel<D, GS, 0, PAGED, true>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                               C::SMEM);
+      if (e != cudaSuccess) return e;
+      e = cudaFuncSetAttribute(decode_kernel<D, GS, 0, PAGED, true>, cudaFuncAttributePreferredSharedMemoryCarveout,
+                               100);
+      if (e != cudaSuccess) return e;
+    }
     e = cudaFuncSetAttribute(merge_kernel<D, (NRES > 0 ? 1 : 0), false>,
                              cudaFuncAttributeMaxDynamicSharedMemorySize, (int)merge_smem);
     if (e != cudaSuccess) return e;
@@ -1200,7 +1217,7 @@ cudaError_t launch_t(const DecodeArgs& a, int num_sms, cudaStream_t stream) {
     // split between L1 and shared memory is fixed while CTAs are resident, so
     // a kernel that asks for another split waits for SMs to drain instead of
     // starting beside the kernel before it (its programmatic-dependent launch).
-    e = cudaFuncSetAttribute(k, cudaFuncAttributePreferredSharedMemoryCarveout, 100);
+    e = cudaFuncSetAttribute(k0, cudaFuncAttributePreferredSharedMemoryCarveout, 100);
     if (e != cudaSuccess) return e;
     e = cudaFuncSetAttribute(qprep_kernel<D, GS, NRES>, cudaFuncAttributePreferredSharedMemoryCarveout, 100);
     if (e != cudaSuccess) return e;
@@ -1212,7 +1229,7 @@ cudaError_t launch_t(const DecodeArgs& a, int num_sms, cudaStream_t stream) {
       if (e != cudaSuccess) return e;
     }
     int occ = 0;
-    e = cudaOccupancyMaxActiveBlocksPerMultiprocessor(&occ, k, kThreads, C::SMEM);
+    e = cudaOccupancyMaxActiveBlocksPerMultiprocessor(&occ, k0, kThreads, C::SMEM);
     if (e != cudaSuccess) return e;
     if (occ < 1) return cudaErrorNotSupported;
     per_sm = occ < C::MINB ? occ : C::MINB;
@@ -1220,7 +1237,6 @@ cudaError_t launch_t(const DecodeArgs& a, int num_sms, cudaStream_t stream) {
   }
   const int grid = num_sms * per_sm;
   if (grid > kMaxContrib) return cudaErrorNotSupported;   // merge_kernel's contributor table
-  const int bhs = a.batch * a.g.Hq;   // (row, query head) pairs
   cudaError_t e = launch_dependent(qprep_kernel<D, GS, NRES>, dim3(bhs), dim3(kPrepThreads), 0, stream, a);
   if (e != cudaSuccess) return e;
   e = launch_dependent(k, dim3(grid), dim3(kThreads), (size_t)C::SMEM, stream, a);
