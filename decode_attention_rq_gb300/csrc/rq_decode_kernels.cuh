@@ -1200,10 +1200,12 @@ cudaError_t launch_t(const DecodeArgs& a, int num_sms, cudaStream_t stream) {
       km_threads = kAppendThreads;
       km_extra = a.batch * a.g.H;   // the V-coding CTAs, one per (row, KV head)
       // more append CTAs than SMs: the lean decode kernel lets two sit beside its
-      // three CTAs per SM (ouro8k batch 8: anchor-loop call 45.2 -> 42.6 us; the
-      // Huginn shape, 220 CTAs: 31.2 -> 25.2 us; at 128 CTAs the 72-register
-      // kernel is 1 % faster)
-      if (bhs + km_extra > num_sms) k = decode_kernel<D, GS, 0, PAGED, true>;
+      // three CTAs per SM (the Huginn shape, 220 CTAs: anchor-loop call 31.2 ->
+      // 25.2 us; ouro8k batch 8, 256 CTAs: 45.2 -> 42.6 us; batch 16, 512 CTAs:
+      // 77.2 -> 75.3 us).  With 128 CTAs, or 1024 (batch 32: 144.5 against
+      // 147.1 us), the 72-register kernel is faster.
+      const int coders = bhs + km_extra;
+      if (coders > num_sms && coders <= 4 * num_sms) k = decode_kernel<D, GS, 0, PAGED, true>;
     }
   constexpr size_t merge_smem = NRES > 0 ? (size_t)D * D * sizeof(float) : 0;
   // Kernel attributes are per device: they are set, and the resident decode CTAs
