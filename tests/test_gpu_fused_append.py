@@ -146,3 +146,43 @@ def test_fused_call_with_many_partials_per_head(chained):
         assert np.array_equal(g_f, obuf), f"step {step}: {int((g_f != obuf).sum())} bytes differ from the oracle"
         seq = seq + 1
     assert fused.status.tolist() == [0, 0, 0, 0]
+
+
+def test_fused_call_with_more_coding_ctas_than_sms():
+    """Batch 2 x 80 heads: 320 token-coding CTAs, more than the GPU's SMs, so the
+    call runs the 64-register anchor-only decode kernel beside them.  Outputs and
+    cache bytes equal the separate calls (the 72-register kernel, then
+    rq_append) bit for bit, and the oracle within 2e-3."""
+    import torch
+    H = 80
+    assert 2 * 2 * H > torch.cuda.get_device_properties(0).multi_processor_count
+    case = Case(L=1, P=4, G=1, H=H, d=128, g=32, B=2, Nmax=256, seed=73)
+    R32, R = rotation32(128)
+    sep, fused = GpuCache(case, R32), GpuCache(case, R32)
+    geom = _geom(case)
+    obuf = np.zeros(geom.total_bytes, dtype=np.uint8)
+    start = np.array([0, 17], dtype=np.int64)
+    n0 = 150
+    kvb, kv = kv_for(case, 74, n0)
+    for c in (sep, fused):
+        c.append(0, 0, kvb, start)
+    oracle.append(obuf, geom, R, 0, 0, kv, start)
+    seq = start + n0
+    scale = 1.0 / math.sqrt(128)
+    for step in range(2):
+        kvb_c, kv_c = kv_for(case, 500 + step, 1)
+        qb, q = synth.queries(600 + step, 2, H, 128)
+        out_s = sep.decode(0, 0, 3, qb, kvb_c[3, 0, :, :, 0], kvb_c[3, 1, :, :, 0], seq, scale)
+        sep.append(0, 0, kvb_c, seq)
+        out_f = fused.decode_append(0, 0, qb, kvb_c[..., 0, :], seq, scale)
+        ref, ok = oracle.decode_attention_append(obuf, geom, R, 0, 0, q, kv_c[..., 0, :], seq, scale)
+        assert ok.all()
+        o_s, o_f = out_s.cpu().numpy(), out_f.cpu().numpy()
+        assert np.array_equal(o_s, o_f), f"step {step}: fused output differs from the two calls"
+        err = float(np.abs(o_f - ref).max())
+        assert err <= ATOL, f"step {step}: max |gpu - oracle| = {err:.3e}"
+        g_f = fused.bytes_host()
+        assert np.array_equal(sep.bytes_host(), g_f)
+        assert np.array_equal(g_f, obuf), f"step {step}: {int((g_f != obuf).sum())} bytes differ from the oracle"
+        seq = seq + 1
+    assert fused.status.tolist() == [0, 0, 0, 0]
